@@ -1,0 +1,137 @@
+"""GB300-native (sm_103a) forward of the DeepSeek-V4.1 Engram layer.
+
+The compute lives in the CUDA library ``libengram_gb300.so`` (C ABI in
+``include/engram.h``); this package only marshals arguments to it.  There
+is no CPU or PyTorch fallback: without the built library every call raises.
+
+    from hashed_gram_engram_gb300 import Engram
+    layer = Engram(dim=4096, hc_mult=4, max_ngram_size=3, n_heads=8, head_dim=64,
+                   max_tokens=64, table=table, rows=rows, wkv=wkv,
+                   q_weight=q, k_weight=k)
+    out = layer.forward(hidden, hash_ids, token_mask)
+"""
+from __future__ import annotations
+
+import ctypes
+
+import numpy as np
+
+from . import _lib
+from ._lib import (EngramError, engram_config, engram_create, engram_debug_intermediates,
+                   engram_debug_staged_rows, engram_destroy, engram_device_error,
+                   engram_forward, engram_forward_host, engram_last_error, engram_layout,
+                   engram_lookup, engram_weights, ENGRAM_WKV_BF16, ENGRAM_WKV_MXFP8,
+                   ENGRAM_TABLE_DEVICE, ENGRAM_TABLE_HOST_PINNED, ENGRAM_DEVERR_BAD_HASH_ID,
+                   ENGRAM_DEVERR_TIMEOUT)
+
+__all__ = [
+    "Engram", "EngramError", "engram_config", "engram_weights", "engram_create",
+    "engram_destroy", "engram_lookup", "engram_forward", "engram_forward_host",
+    "engram_last_error", "engram_device_error", "engram_layout", "engram_debug_intermediates",
+    "engram_debug_staged_rows", "ENGRAM_WKV_BF16", "ENGRAM_WKV_MXFP8", "ENGRAM_TABLE_DEVICE",
+    "ENGRAM_TABLE_HOST_PINNED", "ENGRAM_DEVERR_BAD_HASH_ID", "ENGRAM_DEVERR_TIMEOUT",
+]
+
+
+def library_path() -> str:
+    return _lib.LIB_PATH
+
+
+class Engram:
+    """One Engram layer bound to borrowed weights (class Engram's forward).
+
+    Tensors are torch tensors on the handle's device (the table may be a
+    pinned host tensor with ``table_location=ENGRAM_TABLE_HOST_PINNED``).
+    The object keeps references to them so they outlive the handle.
+    """
+
+    def __init__(self, *, dim, hc_mult, max_ngram_size, n_heads, head_dim, max_tokens,
+                 table, rows, wkv, q_weight, k_weight, row_offset=None, wkv_scale=None,
+                 eps=1e-6, clamp=1e-6, wkv_format=None, table_location=None, device=None):
+        import torch
+        self.dim, self.hc_mult, self.head_dim = int(dim), int(hc_mult), int(head_dim)
+        self.n_hash_cols = (int(max_ngram_size) - 1) * int(n_heads)
+        self.max_tokens = int(max_tokens)
+        rows = np.ascontiguousarray(np.asarray(rows, dtype=np.int64))
+        if row_offset is None:
+            row_offset = np.concatenate([[0], np.cumsum(rows)[:-1]])
+        row_offset = np.ascontiguousarray(np.asarray(row_offset, dtype=np.int64))
+        if wkv_format is None:
+            wkv_format = ENGRAM_WKV_MXFP8 if wkv_scale is not None else ENGRAM_WKV_BF16
+        if table_location is None:
+            table_location = ENGRAM_TABLE_DEVICE if table.is_cuda else ENGRAM_TABLE_HOST_PINNED
+        if device is None:
+            device = wkv.device.index if wkv.device.index is not None else torch.cuda.current_device()
+        cfg = engram_config(dim=self.dim, hc_mult=self.hc_mult,
+                            max_ngram_size=int(max_ngram_size), n_heads=int(n_heads),
+                            head_dim=self.head_dim, eps=float(eps), clamp=float(clamp),
+                            max_tokens=self.max_tokens, wkv_format=int(wkv_format),
+                            table_location=int(table_location), device=int(device), reserved=0)
+        w = engram_weights(table=table.data_ptr(), row_offset=row_offset.ctypes.data,
+                           rows=rows.ctypes.data, wkv=wkv.data_ptr(),
+                           wkv_scale=None if wkv_scale is None else wkv_scale.data_ptr(),
+                           q_weight=q_weight.data_ptr(), k_weight=k_weight.data_ptr())
+        self._keep = (table, wkv, wkv_scale, q_weight, k_weight, rows, row_offset)
+        self.device = int(device)
+        self.handle = engram_create(cfg, w)
+
+    def close(self):
+        if getattr(self, "handle", None):
+            engram_destroy(self.handle)
+            self.handle = None
+
+    def __del__(self):
+        try:
+            self.close()
+        except Exception:
+            pass
+
+    def lookup(self, hash_ids, background=False, stream=None):
+        """Engram.prepare_embeddings: gather the rows of hash_ids [T, C]."""
+        T = hash_ids.shape[0]
+        engram_lookup(self.handle, hash_ids, hash_ids.stride(0) if T else self.n_hash_cols, T,
+                      int(bool(background)), stream)
+
+    def forward(self, hidden, hash_ids=None, token_mask=None, out=None, stream=None):
+        """Engram.forward: returns hidden + gate * value (a new tensor unless out is given).
+
+        hash_ids=None consumes the rows of the last lookup()."""
+        import torch
+        T = hidden.shape[0]
+        if out is None:
+            out = torch.empty_like(hidden)
+        if stream is None:
+            stream = torch.cuda.current_stream(hidden.device)
+        ids_stride = hash_ids.stride(0) if hash_ids is not None and T else self.n_hash_cols
+        mask = None
+        if token_mask is not None:
+            mask = token_mask if token_mask.dtype == torch.uint8 else token_mask.to(torch.uint8)
+        engram_forward(self.handle, hidden, hidden.stride(), hash_ids, ids_stride, mask, out,
+                       out.stride(), T, stream)
+        return out
+
+    __call__ = forward
+
+    def forward_host(self, hidden_host, hash_ids_host, token_mask_host, out_host, stream=None):
+        T = hidden_host.shape[0]
+        engram_forward_host(self.handle, hidden_host, hash_ids_host, token_mask_host, out_host,
+                            T, stream)
+
+    def device_error(self, clear=True) -> int:
+        return engram_device_error(self.handle, int(clear))
+
+    def intermediates(self, T, stream=None):
+        """fp32 gate [T, H] and value [T, D] of the last forward (validation hook)."""
+        import torch
+        dev = torch.device("cuda", self.device)
+        gate = torch.empty((T, self.hc_mult), dtype=torch.float32, device=dev)
+        value = torch.empty((T, self.dim), dtype=torch.float32, device=dev)
+        engram_debug_intermediates(self.handle, gate, value, T, stream)
+        return gate, value
+
+    def staged_rows(self, T, stream=None):
+        import torch
+        rows = torch.empty((T, self.n_hash_cols * self.head_dim), dtype=torch.bfloat16,
+                           device=torch.device("cuda", self.device))
+        engram_debug_staged_rows(self.handle, rows, T, stream)
+        return rows

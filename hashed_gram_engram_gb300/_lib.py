@@ -1,0 +1,210 @@
+"""ctypes binding of ``libengram_gb300.so`` (declared in ``include/engram.h``).
+
+Argument marshalling only: every step of the forward runs in the CUDA
+library.  Functions keep the C names.  Pointer arguments accept an int
+address, ``None`` (NULL), or any object with ``data_ptr()`` (a torch tensor).
+Streams accept an int handle, ``None`` (0), or an object with
+``cuda_stream`` (a torch.cuda.Stream).  A non-zero return raises
+``EngramError`` carrying the code.
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+import threading
+
+HERE = os.path.dirname(os.path.abspath(__file__))
+LIB_PATH = os.path.join(HERE, "libengram_gb300.so")
+
+ENGRAM_OK = 0
+ENGRAM_ERR_INVALID_ARG = -1
+ENGRAM_ERR_UNSUPPORTED = -2
+ENGRAM_ERR_T_EXCEEDS_MAX = -3
+ENGRAM_ERR_OOM = -4
+ENGRAM_ERR_NO_UVA = -5
+ENGRAM_ERR_DEVICE = -6
+ENGRAM_ERR_CUDA = -7
+ERROR_NAMES = {
+    -1: "INVALID_ARG", -2: "UNSUPPORTED", -3: "T_EXCEEDS_MAX", -4: "OOM", -5: "NO_UVA",
+    -6: "DEVICE", -7: "CUDA",
+}
+ENGRAM_DEVERR_BAD_HASH_ID = 1
+ENGRAM_DEVERR_TIMEOUT = 2
+ENGRAM_WKV_BF16 = 0
+ENGRAM_WKV_MXFP8 = 1
+ENGRAM_TABLE_DEVICE = 0
+ENGRAM_TABLE_HOST_PINNED = 1
+
+# Every symbol include/engram.h declares.
+EXPORTED = (
+    "engram_create", "engram_destroy", "engram_lookup", "engram_forward",
+    "engram_forward_host", "engram_last_error", "engram_device_error", "engram_layout",
+    "engram_debug_intermediates", "engram_debug_staged_rows", "engram_profile_enable",
+    "engram_profile_read",
+)
+
+
+class EngramError(RuntimeError):
+    def __init__(self, code: int, what: str = ""):
+        self.code = code
+        super().__init__(f"{what}: ENGRAM_ERR_{ERROR_NAMES.get(code, code)} ({code})")
+
+
+class engram_config(ctypes.Structure):
+    _fields_ = [
+        ("dim", ctypes.c_int64), ("hc_mult", ctypes.c_int64),
+        ("max_ngram_size", ctypes.c_int64), ("n_heads", ctypes.c_int64),
+        ("head_dim", ctypes.c_int64), ("eps", ctypes.c_double), ("clamp", ctypes.c_double),
+        ("max_tokens", ctypes.c_int64), ("wkv_format", ctypes.c_int32),
+        ("table_location", ctypes.c_int32), ("device", ctypes.c_int32),
+        ("reserved", ctypes.c_int32),
+    ]
+
+
+class engram_weights(ctypes.Structure):
+    _fields_ = [
+        ("table", ctypes.c_void_p), ("row_offset", ctypes.c_void_p), ("rows", ctypes.c_void_p),
+        ("wkv", ctypes.c_void_p), ("wkv_scale", ctypes.c_void_p),
+        ("q_weight", ctypes.c_void_p), ("k_weight", ctypes.c_void_p),
+    ]
+
+
+_lock = threading.Lock()
+_lib = None
+
+
+def load(path: str | None = None):
+    """Load the CUDA library; raises if it has not been built."""
+    global _lib
+    with _lock:
+        if _lib is not None:
+            return _lib
+        p = path or LIB_PATH
+        if not os.path.exists(p):
+            raise RuntimeError(
+                f"{p} is missing: build the CUDA library first "
+                "(python -c 'import __graft_entry__ as g; g.build()')")
+        L = ctypes.CDLL(p)
+        vp, i64, i32 = ctypes.c_void_p, ctypes.c_int64, ctypes.c_int32
+        sig = {
+            "engram_create": [vp, vp, vp],
+            "engram_destroy": [vp],
+            "engram_lookup": [vp, vp, i64, i64, ctypes.c_int, vp],
+            "engram_forward": [vp, vp, vp, vp, i64, vp, vp, vp, i64, vp],
+            "engram_forward_host": [vp, vp, vp, vp, vp, i64, vp],
+            "engram_last_error": [vp, ctypes.c_int],
+            "engram_device_error": [vp, vp, ctypes.c_int],
+            "engram_layout": [i64, i32, i32, i32, vp, vp],
+            "engram_debug_intermediates": [vp, vp, vp, i64, vp],
+            "engram_debug_staged_rows": [vp, vp, i64, vp],
+            "engram_profile_enable": [vp, ctypes.c_int],
+            "engram_profile_read": [vp, vp],
+        }
+        for name, args in sig.items():
+            f = getattr(L, name)
+            f.argtypes = args
+            f.restype = ctypes.c_int
+        _lib = L
+        return L
+
+
+def _ptr(x):
+    if x is None:
+        return None
+    if isinstance(x, int):
+        return x
+    if hasattr(x, "data_ptr"):
+        return x.data_ptr() if x.numel() > 0 else None
+    if hasattr(x, "ctypes"):
+        return x.ctypes.data
+    raise TypeError(f"cannot take a pointer of {type(x)}")
+
+
+def _stream(s):
+    if s is None:
+        return None
+    if isinstance(s, int):
+        return s
+    return s.cuda_stream
+
+
+def _check(rc, what):
+    if rc != ENGRAM_OK:
+        raise EngramError(rc, what)
+    return rc
+
+
+def _i64x3(v):
+    return (ctypes.c_int64 * 3)(*[int(x) for x in v])
+
+
+def engram_create(cfg: engram_config, weights: engram_weights) -> int:
+    h = ctypes.c_void_p()
+    _check(load().engram_create(ctypes.byref(cfg), ctypes.byref(weights), ctypes.byref(h)),
+           "engram_create")
+    return h.value
+
+
+def engram_destroy(h: int) -> None:
+    _check(load().engram_destroy(h), "engram_destroy")
+
+
+def engram_lookup(h, hash_ids, ids_row_stride, T, background=0, stream=None):
+    return _check(load().engram_lookup(h, _ptr(hash_ids), int(ids_row_stride), int(T),
+                                       int(background), _stream(stream)), "engram_lookup")
+
+
+def engram_forward(h, hidden, hidden_strides, hash_ids, ids_row_stride, token_mask, out,
+                   out_strides, T, stream=None):
+    return _check(load().engram_forward(
+        h, _ptr(hidden), _i64x3(hidden_strides), _ptr(hash_ids), int(ids_row_stride),
+        _ptr(token_mask), _ptr(out), _i64x3(out_strides), int(T), _stream(stream)),
+        "engram_forward")
+
+
+def engram_forward_host(h, hidden_host, hash_ids_host, token_mask_host, out_host, T,
+                        stream=None):
+    return _check(load().engram_forward_host(
+        h, _ptr(hidden_host), _ptr(hash_ids_host), _ptr(token_mask_host), _ptr(out_host),
+        int(T), _stream(stream)), "engram_forward_host")
+
+
+def engram_last_error(h, sync=0) -> int:
+    return load().engram_last_error(h, int(sync))
+
+
+def engram_device_error(h, clear=1) -> int:
+    bits = ctypes.c_uint32()
+    _check(load().engram_device_error(h, ctypes.byref(bits), int(clear)), "engram_device_error")
+    return bits.value
+
+
+def engram_layout(vocab_size, max_ngram_size, n_heads, n_layers=1):
+    cols = (max_ngram_size - 1) * n_heads
+    primes = (ctypes.c_int64 * (cols * n_layers))()
+    offsets = (ctypes.c_int64 * (cols * n_layers))()
+    _check(load().engram_layout(int(vocab_size), int(max_ngram_size), int(n_heads),
+                                int(n_layers), primes, offsets), "engram_layout")
+    return ([list(primes[l * cols:(l + 1) * cols]) for l in range(n_layers)],
+            [list(offsets[l * cols:(l + 1) * cols]) for l in range(n_layers)])
+
+
+def engram_debug_intermediates(h, gate, value, T, stream=None):
+    return _check(load().engram_debug_intermediates(h, _ptr(gate), _ptr(value), int(T),
+                                                    _stream(stream)),
+                  "engram_debug_intermediates")
+
+
+def engram_debug_staged_rows(h, rows, T, stream=None):
+    return _check(load().engram_debug_staged_rows(h, _ptr(rows), int(T), _stream(stream)),
+                  "engram_debug_staged_rows")
+
+
+def engram_profile_enable(h, enable=1):
+    return _check(load().engram_profile_enable(h, int(enable)), "engram_profile_enable")
+
+
+def engram_profile_read(h):
+    ms = (ctypes.c_float * 3)()
+    _check(load().engram_profile_read(h, ms), "engram_profile_read")
+    return list(ms)

@@ -1,0 +1,472 @@
+// C ABI of the Engram forward: handle life cycle, argument checks, the
+// workspace, TMA descriptors and the launch sequence of one call.
+//
+// The sequence of engram_forward (Engram.forward, with the gather of
+// Engram.prepare_embeddings folded in when hash ids are given):
+//   gather   (plain launch: ordered after everything before it on the stream)
+//   wkv      (programmatic dependent launch: weight tiles stream in while the
+//             gather runs; token tiles wait for it)
+//   gate     (programmatic dependent launch: hidden is read while the wkv
+//             kernel drains)
+// T <= 256 takes the token-as-N (GEMV-shaped, stream-K) projection, larger T
+// the token-as-M tiles with the fused gate-partials epilogue.
+#include <cstdio>
+#include <cstdlib>
+#include <cstring>
+#include <new>
+
+#include "internal.h"
+
+using namespace engram;
+
+namespace {
+
+typedef CUresult (*EncodeTiledFn)(CUtensorMap*, CUtensorMapDataType, cuuint32_t, void*,
+                                  const cuuint64_t*, const cuuint64_t*, const cuuint32_t*,
+                                  const cuuint32_t*, CUtensorMapInterleave, CUtensorMapSwizzle,
+                                  CUtensorMapL2promotion, CUtensorMapFloatOOBfill);
+
+EncodeTiledFn encode_fn() {
+    static EncodeTiledFn fn = nullptr;
+    if (fn == nullptr) {
+        void* p = nullptr;
+        cudaDriverEntryPointQueryResult q;
+        if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &p, 12000,
+                                             cudaEnableDefault, &q) == cudaSuccess &&
+            q == cudaDriverEntryPointSuccess)
+            fn = reinterpret_cast<EncodeTiledFn>(p);
+    }
+    return fn;
+}
+
+// 2-D K-major operand [rows, cols] of `elem` bytes, box = 128 bytes of K x
+// box_rows, 128-byte swizzle (the layout the tcgen05 descriptors expect).
+bool make_map(CUtensorMap* m, const void* base, CUtensorMapDataType dt, int elem, int64_t cols,
+              int64_t rows, int box_rows) {
+    EncodeTiledFn fn = encode_fn();
+    if (fn == nullptr) return false;
+    cuuint64_t dims[2] = {static_cast<cuuint64_t>(cols), static_cast<cuuint64_t>(rows)};
+    cuuint64_t strides[1] = {static_cast<cuuint64_t>(cols * elem)};
+    cuuint32_t box[2] = {static_cast<cuuint32_t>(kKBlockBytes / elem),
+                         static_cast<cuuint32_t>(box_rows)};
+    cuuint32_t estr[2] = {1, 1};
+    return fn(m, dt, 2, const_cast<void*>(base), dims, strides, box, estr,
+              CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+              CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+              CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
+// Keeps the caller's current device across an entry point.
+struct DeviceGuard {
+    int prev = -1;
+    bool ok = false;
+    explicit DeviceGuard(int dev) {
+        if (cudaGetDevice(&prev) != cudaSuccess) prev = -1;
+        ok = (prev == dev) || cudaSetDevice(dev) == cudaSuccess;
+    }
+    ~DeviceGuard() {
+        int cur = -1;
+        if (prev >= 0 && cudaGetDevice(&cur) == cudaSuccess && cur != prev) cudaSetDevice(prev);
+    }
+};
+
+bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
+
+template <class T>
+cudaError_t dalloc(T** p, size_t bytes, bool zero) {
+    *p = nullptr;
+    if (bytes == 0) return cudaSuccess;
+    cudaError_t e = cudaMalloc(reinterpret_cast<void**>(p), bytes);
+    if (e != cudaSuccess) {
+        *p = nullptr;
+        return e;
+    }
+    if (zero) e = cudaMemset(*p, 0, bytes);
+    return e;
+}
+
+void free_handle(engram_handle* h) {
+    if (h == nullptr) return;
+    void* ptrs[] = {h->d_row_offset, h->d_rows,      h->ws.staged,   h->ws.staged_q,
+                    h->ws.staged_s,  h->ws.kvpart,   h->ws.partials, h->ws.value,
+                    h->ws.gate,      h->ws.qk,       h->ws.wscale_rows, h->ws.err,
+                    h->ws.host_hidden, h->ws.host_ids, h->ws.host_mask};
+    for (void* p : ptrs)
+        if (p) cudaFree(p);
+    for (cudaEvent_t ev : h->ev)
+        if (ev) cudaEventDestroy(ev);
+    delete h;
+}
+
+int set_err(engram_handle* h, int code) {
+    if (h) h->last_error = code;
+    return code;
+}
+
+int cuda_err(engram_handle* h, cudaError_t e) {
+    if (e == cudaSuccess) return set_err(h, ENGRAM_OK);
+    return set_err(h, e == cudaErrorMemoryAllocation ? ENGRAM_ERR_OOM : ENGRAM_ERR_CUDA);
+}
+
+bool ranges_overlap(const void* a, int64_t a_bytes, const void* b, int64_t b_bytes) {
+    const uintptr_t pa = reinterpret_cast<uintptr_t>(a), pb = reinterpret_cast<uintptr_t>(b);
+    return pa < pb + static_cast<uintptr_t>(b_bytes) && pb < pa + static_cast<uintptr_t>(a_bytes);
+}
+
+// Bytes spanned by a [T, H, D] bf16 view with non-negative strides.
+int64_t span_bytes(const int64_t* s, int64_t T, int64_t H, int64_t D) {
+    return ((T - 1) * s[0] + (H - 1) * s[1] + (D - 1) * s[2] + 1) * 2;
+}
+
+int check_view(const void* p, const int64_t* s, int64_t H, int64_t D) {
+    if (p == nullptr || s == nullptr) return ENGRAM_ERR_INVALID_ARG;
+    if (s[0] < 0 || s[1] < 0 || s[2] != 1) return s[2] != 1 && s[2] > 0 ? ENGRAM_ERR_UNSUPPORTED
+                                                                        : ENGRAM_ERR_INVALID_ARG;
+    if (!aligned16(p) || (s[0] % 8) != 0 || (s[1] % 8) != 0) return ENGRAM_ERR_UNSUPPORTED;
+    (void)H;
+    (void)D;
+    return ENGRAM_OK;
+}
+
+}  // namespace
+
+extern "C" {
+
+int engram_layout(int64_t vocab_size, int32_t max_ngram_size, int32_t n_heads, int32_t n_layers,
+                  int64_t* primes, int64_t* offsets) {
+    if (vocab_size < 1 || max_ngram_size < 2 || n_heads < 1 || n_layers < 1 || !primes ||
+        !offsets)
+        return ENGRAM_ERR_INVALID_ARG;
+    const int64_t cols = static_cast<int64_t>(max_ngram_size - 1) * n_heads;
+    const int64_t total = cols * n_layers;
+    auto is_prime = [](int64_t n) {
+        if (n < 2) return false;
+        if (n % 2 == 0) return n == 2;
+        for (int64_t d = 3; d * d <= n; d += 2)
+            if (n % d == 0) return false;
+        return true;
+    };
+    int64_t used = 0;  // primes[0..used) are taken
+    for (int32_t l = 0; l < n_layers; ++l) {
+        for (int32_t o = 0; o < max_ngram_size - 1; ++o) {
+            int64_t cur = vocab_size - 1;
+            for (int32_t hd = 0; hd < n_heads; ++hd) {
+                bool taken = true;
+                while (taken) {
+                    do ++cur; while (!is_prime(cur));
+                    taken = false;
+                    for (int64_t i = 0; i < used && !taken; ++i) taken = primes[i] == cur;
+                }
+                primes[used++] = cur;
+            }
+        }
+        int64_t acc = 0;
+        for (int64_t c = 0; c < cols; ++c) {
+            offsets[l * cols + c] = acc;
+            acc += primes[l * cols + c];
+        }
+    }
+    (void)total;
+    return ENGRAM_OK;
+}
+
+int engram_create(const engram_config* cfg, const engram_weights* w, engram_t** out) {
+    if (out == nullptr) return ENGRAM_ERR_INVALID_ARG;
+    *out = nullptr;
+    if (cfg == nullptr || w == nullptr) return ENGRAM_ERR_INVALID_ARG;
+    const engram_config c = *cfg;
+    if (c.dim <= 0 || c.hc_mult <= 0 || c.max_ngram_size < 2 || c.n_heads < 1 ||
+        c.head_dim <= 0 || c.max_tokens <= 0 || !(c.eps >= 0.0) || !(c.clamp >= 0.0) ||
+        c.reserved != 0 || (c.wkv_format != ENGRAM_WKV_BF16 && c.wkv_format != ENGRAM_WKV_MXFP8) ||
+        (c.table_location != ENGRAM_TABLE_DEVICE && c.table_location != ENGRAM_TABLE_HOST_PINNED))
+        return ENGRAM_ERR_INVALID_ARG;
+    if (w->table == nullptr || w->row_offset == nullptr || w->rows == nullptr ||
+        w->wkv == nullptr || w->q_weight == nullptr || w->k_weight == nullptr)
+        return ENGRAM_ERR_INVALID_ARG;
+    if (c.wkv_format == ENGRAM_WKV_MXFP8 && w->wkv_scale == nullptr) return ENGRAM_ERR_INVALID_ARG;
+    const int64_t C = (c.max_ngram_size - 1) * c.n_heads;
+    const int64_t K = C * c.head_dim;
+    const int64_t N = c.dim * (c.hc_mult + 1);
+    // What the kernels are built for.
+    if (c.dim % kBNPrefill != 0 || c.dim > 8192 || c.hc_mult > 4 || c.head_dim % 8 != 0 ||
+        32 % (c.head_dim / 8) != 0 || K % 128 != 0 || K > (1 << 20) ||
+        (c.wkv_format == ENGRAM_WKV_MXFP8) || !aligned16(w->table) || !aligned16(w->wkv) ||
+        c.max_tokens > (1 << 24))
+        return ENGRAM_ERR_UNSUPPORTED;
+    for (int64_t i = 0; i < C; ++i)
+        if (w->rows[i] <= 0 || w->row_offset[i] < 0) return ENGRAM_ERR_INVALID_ARG;
+
+    DeviceGuard guard(c.device);
+    if (!guard.ok) return ENGRAM_ERR_CUDA;
+    int sms = 0, uva = 0;
+    if (cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, c.device) != cudaSuccess ||
+        cudaDeviceGetAttribute(&uva, cudaDevAttrUnifiedAddressing, c.device) != cudaSuccess)
+        return ENGRAM_ERR_CUDA;
+
+    const void* table = w->table;
+    if (c.table_location == ENGRAM_TABLE_HOST_PINNED) {
+        cudaPointerAttributes pa;
+        if (!uva) return ENGRAM_ERR_NO_UVA;
+        if (cudaPointerGetAttributes(&pa, w->table) != cudaSuccess) {
+            cudaGetLastError();
+            return ENGRAM_ERR_NO_UVA;
+        }
+        if (pa.type != cudaMemoryTypeHost || pa.devicePointer == nullptr) return ENGRAM_ERR_NO_UVA;
+        table = pa.devicePointer;
+    }
+
+    engram_handle* h = new (std::nothrow) engram_handle();
+    if (h == nullptr) return ENGRAM_ERR_OOM;
+    std::memset(static_cast<void*>(h), 0, sizeof(*h));
+    h->cfg = c;
+    h->C = C;
+    h->K = K;
+    h->N = N;
+    h->num_sms = sms;
+    h->table = static_cast<const uint16_t*>(table);
+    h->wkv = w->wkv;
+    h->wkv_scale = w->wkv_scale;
+    h->q = static_cast<const uint16_t*>(w->q_weight);
+    h->k = static_cast<const uint16_t*>(w->k_weight);
+    h->staged_T = -1;
+
+    Workspace& ws = h->ws;
+    ws.rows_alloc = (c.max_tokens + 255) / 256 * 256;
+    const int64_t tdec = c.max_tokens < kMaxDecodeT ? c.max_tokens : kMaxDecodeT;
+    ws.kv_tpitch = (tdec + 15) / 16 * 16;
+    const int64_t m_tiles = N / kBM;
+    cudaError_t e = cudaSuccess;
+    auto step = [&](cudaError_t r) {
+        if (e == cudaSuccess) e = r;
+    };
+    step(dalloc(&h->d_row_offset, C * sizeof(int64_t), false));
+    step(dalloc(&h->d_rows, C * sizeof(int64_t), false));
+    step(dalloc(&ws.staged, ws.rows_alloc * K * 2, true));
+    step(dalloc(&ws.kvpart, 2 * m_tiles * ws.kv_tpitch * 128 * sizeof(float), true));
+    if (c.max_tokens > kMaxDecodeT) {
+        step(dalloc(&ws.partials, ws.rows_alloc * c.hc_mult * (c.dim / kBNPrefill) * sizeof(float2),
+                    true));
+        step(dalloc(&ws.value, ws.rows_alloc * c.dim * 2, true));
+    }
+    step(dalloc(&ws.gate, ws.rows_alloc * c.hc_mult * sizeof(float), true));
+    step(dalloc(&ws.qk, c.hc_mult * c.dim * sizeof(float), false));
+    step(dalloc(&ws.err, sizeof(unsigned), true));
+    if (e == cudaSuccess)
+        e = cudaMemcpy(h->d_row_offset, w->row_offset, C * sizeof(int64_t), cudaMemcpyHostToDevice);
+    if (e == cudaSuccess)
+        e = cudaMemcpy(h->d_rows, w->rows, C * sizeof(int64_t), cudaMemcpyHostToDevice);
+    if (e == cudaSuccess) e = launch_qk(h, 0);
+    if (e == cudaSuccess) e = gemm_setup_attributes();
+    if (e == cudaSuccess) e = cudaDeviceSynchronize();
+    if (e != cudaSuccess) {
+        free_handle(h);
+        return e == cudaErrorMemoryAllocation ? ENGRAM_ERR_OOM : ENGRAM_ERR_CUDA;
+    }
+
+    bool ok = make_map(&h->tm_w_m, h->wkv, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, K, N, kBM) &&
+              make_map(&h->tm_w_n, h->wkv, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, K, N, kBNPrefill) &&
+              make_map(&h->tm_act_m, ws.staged, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, K,
+                       ws.rows_alloc, kBM);
+    for (int i = 0; i < 16 && ok; ++i)
+        ok = make_map(&h->tm_act_n[i], ws.staged, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, K,
+                      ws.rows_alloc, 16 * (i + 1));
+    if (!ok) {
+        free_handle(h);
+        return ENGRAM_ERR_CUDA;
+    }
+    *out = h;
+    return ENGRAM_OK;
+}
+
+int engram_destroy(engram_t* h) {
+    if (h == nullptr) return ENGRAM_OK;
+    DeviceGuard guard(h->cfg.device);
+    cudaDeviceSynchronize();
+    free_handle(h);
+    return ENGRAM_OK;
+}
+
+int engram_lookup(engram_t* h, const int32_t* hash_ids, int64_t ids_row_stride, int64_t T,
+                  int background, cudaStream_t stream) {
+    if (h == nullptr) return ENGRAM_ERR_INVALID_ARG;
+    if (T < 0) return set_err(h, ENGRAM_ERR_INVALID_ARG);
+    if (T > h->cfg.max_tokens) return set_err(h, ENGRAM_ERR_T_EXCEEDS_MAX);
+    if (T == 0) {
+        h->staged_T = 0;
+        return set_err(h, ENGRAM_OK);
+    }
+    if (hash_ids == nullptr || ids_row_stride < h->C) return set_err(h, ENGRAM_ERR_INVALID_ARG);
+    DeviceGuard guard(h->cfg.device);
+    cudaError_t e = launch_gather(h, hash_ids, ids_row_stride, T, background != 0, false, stream,
+                                  false);
+    if (e != cudaSuccess) return cuda_err(h, e);
+    h->staged_T = T;
+    return set_err(h, ENGRAM_OK);
+}
+
+int engram_forward(engram_t* h, const void* hidden, const int64_t hidden_strides[3],
+                   const int32_t* hash_ids, int64_t ids_row_stride, const uint8_t* token_mask,
+                   void* out, const int64_t out_strides[3], int64_t T, cudaStream_t stream) {
+    if (h == nullptr) return ENGRAM_ERR_INVALID_ARG;
+    if (T < 0) return set_err(h, ENGRAM_ERR_INVALID_ARG);
+    if (T > h->cfg.max_tokens) return set_err(h, ENGRAM_ERR_T_EXCEEDS_MAX);
+    if (T == 0) return set_err(h, ENGRAM_OK);
+    const int64_t H = h->cfg.hc_mult, D = h->cfg.dim;
+    int rc = check_view(hidden, hidden_strides, H, D);
+    if (rc != ENGRAM_OK) return set_err(h, rc);
+    rc = check_view(out, out_strides, H, D);
+    if (rc != ENGRAM_OK) return set_err(h, rc);
+    const bool same = hidden == out && hidden_strides[0] == out_strides[0] &&
+                      hidden_strides[1] == out_strides[1];
+    if (!same && ranges_overlap(hidden, span_bytes(hidden_strides, T, H, D), out,
+                                span_bytes(out_strides, T, H, D)))
+        return set_err(h, ENGRAM_ERR_INVALID_ARG);
+    if (hash_ids != nullptr && ids_row_stride < h->C) return set_err(h, ENGRAM_ERR_INVALID_ARG);
+    if (hash_ids == nullptr && h->staged_T != T) return set_err(h, ENGRAM_ERR_INVALID_ARG);
+
+    DeviceGuard guard(h->cfg.device);
+    const bool prof = h->profiling != 0;
+    bool first = true;
+    cudaError_t e = cudaSuccess;
+    auto mark = [&](int i) {
+        if (prof && e == cudaSuccess) e = cudaEventRecord(h->ev[i], stream);
+    };
+    h->ev_ran[0] = hash_ids != nullptr;
+    h->ev_ran[1] = h->ev_ran[2] = true;
+    mark(0);
+    if (hash_ids != nullptr) {
+        e = launch_gather(h, hash_ids, ids_row_stride, T, false, false, stream, false);
+        if (e != cudaSuccess) return cuda_err(h, e);
+        h->staged_T = T;
+        first = false;
+    }
+    mark(1);
+    if (T <= kMaxDecodeT) {
+        if (e == cudaSuccess) e = launch_wkv_tokens_n(h, T, stream, !first && !prof);
+        mark(2);
+        if (e == cudaSuccess)
+            e = launch_gate_from_kvpart(h, hidden, hidden_strides, token_mask, out, out_strides, T,
+                                        stream, !prof);
+        h->last_path = 1;
+    } else {
+        if (e == cudaSuccess)
+            e = launch_wkv_tokens_m(h, hidden, hidden_strides[0], hidden_strides[1], T, stream,
+                                    !first && !prof);
+        mark(2);
+        if (e == cudaSuccess)
+            e = launch_gate_from_partials(h, hidden, hidden_strides, token_mask, out, out_strides,
+                                          T, stream, !prof);
+        h->last_path = 2;
+    }
+    mark(3);
+    return cuda_err(h, e);
+}
+
+int engram_forward_host(engram_t* h, const void* hidden_host, const int32_t* hash_ids_host,
+                        const uint8_t* token_mask_host, void* out_host, int64_t T,
+                        cudaStream_t stream) {
+    if (h == nullptr) return ENGRAM_ERR_INVALID_ARG;
+    if (T < 0) return set_err(h, ENGRAM_ERR_INVALID_ARG);
+    if (T > h->cfg.max_tokens) return set_err(h, ENGRAM_ERR_T_EXCEEDS_MAX);
+    if (T == 0) return set_err(h, ENGRAM_OK);
+    if (hidden_host == nullptr || hash_ids_host == nullptr || out_host == nullptr)
+        return set_err(h, ENGRAM_ERR_INVALID_ARG);
+    DeviceGuard guard(h->cfg.device);
+    const int64_t H = h->cfg.hc_mult, D = h->cfg.dim, C = h->C;
+    Workspace& ws = h->ws;
+    cudaError_t e = cudaSuccess;
+    if (ws.host_hidden == nullptr) {
+        e = dalloc(reinterpret_cast<uint16_t**>(&ws.host_hidden), ws.rows_alloc * H * D * 2, false);
+        if (e == cudaSuccess) e = dalloc(&ws.host_ids, ws.rows_alloc * C * sizeof(int32_t), false);
+        if (e == cudaSuccess) e = dalloc(&ws.host_mask, ws.rows_alloc, false);
+        if (e != cudaSuccess) return cuda_err(h, e);
+    }
+    const size_t hb = static_cast<size_t>(T * H * D * 2);
+    e = cudaMemcpyAsync(ws.host_hidden, hidden_host, hb, cudaMemcpyHostToDevice, stream);
+    if (e == cudaSuccess)
+        e = cudaMemcpyAsync(ws.host_ids, hash_ids_host, static_cast<size_t>(T * C * 4),
+                            cudaMemcpyHostToDevice, stream);
+    if (e == cudaSuccess && token_mask_host != nullptr)
+        e = cudaMemcpyAsync(ws.host_mask, token_mask_host, static_cast<size_t>(T),
+                            cudaMemcpyHostToDevice, stream);
+    if (e != cudaSuccess) return cuda_err(h, e);
+    const int64_t st[3] = {H * D, D, 1};
+    int rc = engram_forward(h, ws.host_hidden, st, ws.host_ids, C,
+                            token_mask_host != nullptr ? ws.host_mask : nullptr, ws.host_hidden, st,
+                            T, stream);
+    if (rc != ENGRAM_OK) return rc;
+    e = cudaMemcpyAsync(out_host, ws.host_hidden, hb, cudaMemcpyDeviceToHost, stream);
+    return cuda_err(h, e);
+}
+
+int engram_last_error(engram_t* h, int sync) {
+    if (h == nullptr) return ENGRAM_ERR_INVALID_ARG;
+    if (sync) {
+        uint32_t bits = 0;
+        int rc = engram_device_error(h, &bits, 1);
+        if (rc != ENGRAM_OK) return rc;
+        if (bits != 0) return ENGRAM_ERR_DEVICE;
+    }
+    return h->last_error;
+}
+
+int engram_device_error(engram_t* h, uint32_t* bits, int clear) {
+    if (h == nullptr || bits == nullptr) return ENGRAM_ERR_INVALID_ARG;
+    DeviceGuard guard(h->cfg.device);
+    cudaError_t e = cudaDeviceSynchronize();
+    if (e == cudaSuccess) e = cudaMemcpy(bits, h->ws.err, sizeof(unsigned), cudaMemcpyDeviceToHost);
+    if (e == cudaSuccess && clear) e = cudaMemset(h->ws.err, 0, sizeof(unsigned));
+    if (e != cudaSuccess) return ENGRAM_ERR_CUDA;
+    return ENGRAM_OK;
+}
+
+int engram_debug_intermediates(engram_t* h, float* gate, float* value, int64_t T,
+                               cudaStream_t stream) {
+    if (h == nullptr || T < 0 || T > h->cfg.max_tokens) return ENGRAM_ERR_INVALID_ARG;
+    if (T == 0) return ENGRAM_OK;
+    DeviceGuard guard(h->cfg.device);
+    cudaError_t e = cudaSuccess;
+    if (gate != nullptr)
+        e = cudaMemcpyAsync(gate, h->ws.gate, T * h->cfg.hc_mult * sizeof(float),
+                            cudaMemcpyDeviceToDevice, stream);
+    if (e == cudaSuccess && value != nullptr) {
+        if (h->last_path == 0) return ENGRAM_ERR_INVALID_ARG;
+        e = launch_debug_value(h, value, T, stream);
+    }
+    return e == cudaSuccess ? ENGRAM_OK : ENGRAM_ERR_CUDA;
+}
+
+int engram_debug_staged_rows(engram_t* h, void* rows, int64_t T, cudaStream_t stream) {
+    if (h == nullptr || rows == nullptr || T < 0 || T > h->cfg.max_tokens)
+        return ENGRAM_ERR_INVALID_ARG;
+    if (T == 0) return ENGRAM_OK;
+    DeviceGuard guard(h->cfg.device);
+    cudaError_t e = cudaMemcpyAsync(rows, h->ws.staged, T * h->K * 2, cudaMemcpyDeviceToDevice,
+                                    stream);
+    return e == cudaSuccess ? ENGRAM_OK : ENGRAM_ERR_CUDA;
+}
+
+int engram_profile_enable(engram_t* h, int enable) {
+    if (h == nullptr) return ENGRAM_ERR_INVALID_ARG;
+    DeviceGuard guard(h->cfg.device);
+    if (enable && h->ev[0] == nullptr) {
+        for (cudaEvent_t& ev : h->ev)
+            if (cudaEventCreate(&ev) != cudaSuccess) return set_err(h, ENGRAM_ERR_CUDA);
+    }
+    h->profiling = enable != 0;
+    return set_err(h, ENGRAM_OK);
+}
+
+int engram_profile_read(engram_t* h, float ms[3]) {
+    if (h == nullptr || ms == nullptr || h->ev[0] == nullptr) return ENGRAM_ERR_INVALID_ARG;
+    DeviceGuard guard(h->cfg.device);
+    if (cudaEventSynchronize(h->ev[3]) != cudaSuccess) return set_err(h, ENGRAM_ERR_CUDA);
+    for (int i = 0; i < 3; ++i) {
+        ms[i] = 0.f;
+        if (h->ev_ran[i] && cudaEventElapsedTime(&ms[i], h->ev[i], h->ev[i + 1]) != cudaSuccess)
+            return set_err(h, ENGRAM_ERR_CUDA);
+    }
+    return set_err(h, ENGRAM_OK);
+}
+
+}  // extern "C"

@@ -1,0 +1,161 @@
+// Hash-row gather (ParallelEngramEmbedding.lookup feeding Engram.staged_rows,
+// "vllm.models.deepseek_v4_1.common.engram"):
+//   staged[t, c*E + j] = table[row_offset[c] + ids[t, c], j]
+// One thread moves one 16-byte chunk; the E/8 threads of a row are
+// consecutive lanes, so every 128-byte row is one fully used request.  Each
+// thread keeps kUnroll independent row reads in flight to cover the
+// latency of random rows in HBM or, for an offloaded table, in host memory
+// across the host link.  A persistent grid near the SM count (halved for
+// background lookups) follows the page's note that the table dwarfs TLB
+// reach.  Optionally the same pass emits the MXFP8 form of the rows: e4m3
+// codes and one E8M0 scale per 32 consecutive k (smallest power of two that
+// keeps the block maximum within 448; round-to-nearest-even, saturating).
+#include <cuda_fp8.h>
+
+#include "internal.h"
+#include "ptx.cuh"
+
+namespace engram {
+namespace {
+
+constexpr int kGatherThreads = 256;
+constexpr int kUnroll = 4;
+
+struct GatherArgs {
+    const uint16_t* table;
+    const int64_t* row_offset;
+    const int64_t* rows;
+    const int32_t* ids;
+    int64_t ids_stride;
+    uint16_t* staged;  // [T, K]
+    uint8_t* codes;    // [T, K]     (quantize only)
+    uint8_t* scales;   // [T, K/32]  (quantize only)
+    int64_t n_chunks;  // T * C * cpr
+    int C, E, K, cpr_shift;
+    unsigned* err;
+};
+
+// Exponent e of the E8M0 scale: the smallest integer with
+// amax <= 448 * 2^e (amax = 0 -> 0), clamped to [-127, 127].  448 = 1.75*2^8,
+// so for amax = 1.m * 2^u the answer is u - 8, plus one when 1.m > 1.75.
+__device__ __forceinline__ int mx_scale_exponent(float amax) {
+    const uint32_t b = __float_as_uint(amax);
+    const int ef = static_cast<int>((b >> 23) & 0xFFu);
+    if (ef == 0) return (b & 0x7FFFFFu) ? -127 : 0;
+    int e = ef - 127 - 8 + (((b & 0x7FFFFFu) > 0x600000u) ? 1 : 0);
+    return e < -127 ? -127 : (e > 127 ? 127 : e);
+}
+
+template <bool kQuant>
+__global__ void __launch_bounds__(kGatherThreads) gather_rows_kernel(const GatherArgs a) {
+    pdl_wait();
+    const int64_t stride = static_cast<int64_t>(gridDim.x) * kGatherThreads;
+    const int lane = threadIdx.x & 31;
+    const int64_t warp0 = static_cast<int64_t>(blockIdx.x) * kGatherThreads + (threadIdx.x & ~31);
+    const int cpr_mask = (1 << a.cpr_shift) - 1;
+    unsigned bad = 0;
+    // The loop bound is warp-uniform so every lane reaches the shuffles.
+    for (int64_t base = warp0; base < a.n_chunks; base += stride * kUnroll) {
+        uint4 v[kUnroll];
+        int64_t dst[kUnroll];
+#pragma unroll
+        for (int u = 0; u < kUnroll; ++u) {
+            const int64_t g = base + lane + u * stride;
+            v[u] = make_uint4(0u, 0u, 0u, 0u);
+            dst[u] = -1;
+            if (g < a.n_chunks) {
+                const int64_t r = g >> a.cpr_shift;  // (t, c) row
+                const int j = static_cast<int>(g & cpr_mask);
+                const int64_t t = r / a.C;
+                const int c = static_cast<int>(r - t * a.C);
+                const int64_t id = a.ids[t * a.ids_stride + c];
+                dst[u] = r * a.E + j * 8;
+                if (id >= 0 && id < __ldg(a.rows + c)) {
+                    const uint16_t* src = a.table + (__ldg(a.row_offset + c) + id) * a.E + j * 8;
+                    v[u] = ld_stream_v4(src);
+                } else {
+                    bad = 1;
+                }
+            }
+        }
+#pragma unroll
+        for (int u = 0; u < kUnroll; ++u) {
+            if (dst[u] >= 0) st_v4(a.staged + dst[u], v[u]);
+            if constexpr (kQuant) {
+                // 4 consecutive lanes hold one 32-element block.
+                uint32_t w[4] = {v[u].x, v[u].y, v[u].z, v[u].w};
+                uint32_t m = 0;
+#pragma unroll
+                for (int i = 0; i < 4; ++i) {
+                    m = max(m, w[i] & 0x7FFFu);
+                    m = max(m, (w[i] >> 16) & 0x7FFFu);
+                }
+                m = max(m, __shfl_xor_sync(0xFFFFFFFFu, m, 1));
+                m = max(m, __shfl_xor_sync(0xFFFFFFFFu, m, 2));
+                const int e = mx_scale_exponent(__uint_as_float(m << 16));
+                const float inv = __uint_as_float(static_cast<uint32_t>(127 - e) << 23);
+                if (dst[u] >= 0) {
+                    uint32_t packed[2];
+#pragma unroll
+                    for (int i = 0; i < 2; ++i) {
+                        const __nv_fp8x2_storage_t lo = __nv_cvt_float2_to_fp8x2(
+                            make_float2(bf16lo(w[2 * i]) * inv, bf16hi(w[2 * i]) * inv),
+                            __NV_SATFINITE, __NV_E4M3);
+                        const __nv_fp8x2_storage_t hi = __nv_cvt_float2_to_fp8x2(
+                            make_float2(bf16lo(w[2 * i + 1]) * inv, bf16hi(w[2 * i + 1]) * inv),
+                            __NV_SATFINITE, __NV_E4M3);
+                        packed[i] = static_cast<uint32_t>(lo) | (static_cast<uint32_t>(hi) << 16);
+                    }
+                    *reinterpret_cast<uint2*>(a.codes + dst[u]) = make_uint2(packed[0], packed[1]);
+                    if ((lane & 3) == 0) a.scales[dst[u] >> 5] = static_cast<uint8_t>(e + 127);
+                }
+            }
+        }
+    }
+    if (bad) atomicOr(a.err, ENGRAM_DEVERR_BAD_HASH_ID);
+    pdl_launch_dependents();
+}
+
+}  // namespace
+
+cudaError_t launch_gather(const engram_handle* h, const int32_t* ids, int64_t ids_stride,
+                          int64_t T, bool background, bool quantize, cudaStream_t s, bool pdl) {
+    GatherArgs a;
+    a.table = h->table;
+    a.row_offset = h->d_row_offset;
+    a.rows = h->d_rows;
+    a.ids = ids;
+    a.ids_stride = ids_stride;
+    a.staged = h->ws.staged;
+    a.codes = h->ws.staged_q;
+    a.scales = h->ws.staged_s;
+    a.C = static_cast<int>(h->C);
+    a.E = static_cast<int>(h->cfg.head_dim);
+    a.K = static_cast<int>(h->K);
+    int cpr = a.E / 8, shift = 0;
+    while ((1 << shift) < cpr) ++shift;
+    a.cpr_shift = shift;
+    a.n_chunks = T * h->C * cpr;
+    a.err = h->ws.err;
+
+    const int64_t per_block = static_cast<int64_t>(kGatherThreads) * kUnroll;
+    int64_t blocks = (a.n_chunks + per_block - 1) / per_block;
+    const int64_t cap = background ? (h->num_sms / 2 > 0 ? h->num_sms / 2 : 1)
+                                   : static_cast<int64_t>(h->num_sms) * 8;
+    if (blocks > cap) blocks = cap;
+    if (blocks < 1) blocks = 1;
+
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3(static_cast<unsigned>(blocks));
+    cfg.blockDim = dim3(kGatherThreads);
+    cfg.stream = s;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = pdl ? 1 : 0;
+    if (quantize) return cudaLaunchKernelEx(&cfg, gather_rows_kernel<true>, a);
+    return cudaLaunchKernelEx(&cfg, gather_rows_kernel<false>, a);
+}
+
+}  // namespace engram

@@ -1,0 +1,191 @@
+/*
+ * engram.h -- C ABI of the GB300 (sm_103a) Engram layer forward.
+ *
+ * One Engram layer, as documented on the vLLM API page
+ * "vllm.models.deepseek_v4_1.common.engram" (class Engram): hash ids fetch
+ * one row per hash column from prime-sized hashed n-gram tables; the wkv
+ * projection turns the concatenated rows into one key per hc copy plus a
+ * shared value; a gate -- sigmoid of the signed square root of a normalised
+ * dot product of the residual stream against the key -- scales the value
+ * that is added to the stream; a False token mask leaves a position
+ * untouched.
+ *
+ * Notation: T tokens, D = dim (hidden_size), H = hc_mult, C = n_hash_cols =
+ * (max_ngram_size - 1) * n_heads, E = head_dim, K = C * E, N = D * (H + 1).
+ *
+ * Conventions for every entry point:
+ *   - Pointers named "device" are CUDA device pointers (or, for the table of
+ *     a host-offloaded handle, pinned host memory the GPU can address).
+ *     The caller owns every buffer it passes; weights are borrowed by the
+ *     handle and must outlive it.  The handle owns its workspace.
+ *   - Work is enqueued on the given cudaStream_t (0 = legacy default stream)
+ *     and the call returns without synchronising.  Ordering against work on
+ *     other streams is the caller's, with CUDA events.
+ *   - Return value: ENGRAM_OK (0) or a negative ENGRAM_ERR_* code.  No entry
+ *     point aborts, traps or prints.  Errors found on the device (a hash id
+ *     outside its table, a pipeline wait that gave up) set a sticky flag that
+ *     engram_last_error() reports.
+ *   - T == 0 is valid everywhere and launches nothing.
+ */
+#ifndef ENGRAM_GB300_H
+#define ENGRAM_GB300_H
+
+#include <stdint.h>
+#include <cuda_runtime_api.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+#define ENGRAM_OK 0
+#define ENGRAM_ERR_INVALID_ARG (-1)   /* null pointer, bad shape or stride */
+#define ENGRAM_ERR_UNSUPPORTED (-2)   /* valid but not built: misalignment, H > 4, ... */
+#define ENGRAM_ERR_T_EXCEEDS_MAX (-3) /* T larger than the handle's max_tokens */
+#define ENGRAM_ERR_OOM (-4)           /* workspace allocation failed */
+#define ENGRAM_ERR_NO_UVA (-5)        /* host-offloaded table needs unified addressing */
+#define ENGRAM_ERR_DEVICE (-6)        /* the device reported an error (see below) */
+#define ENGRAM_ERR_CUDA (-7)          /* a CUDA runtime call or launch failed */
+
+/* Bits of the sticky device error word returned by engram_device_error(). */
+#define ENGRAM_DEVERR_BAD_HASH_ID 1u  /* an id outside [0, rows[c]): its row was zeroed */
+#define ENGRAM_DEVERR_TIMEOUT 2u      /* a bounded pipeline wait gave up; outputs invalid */
+
+#define ENGRAM_WKV_BF16 0   /* wkv bf16 [N, K] */
+#define ENGRAM_WKV_MXFP8 1  /* wkv e4m3 [N, K] with E8M0 scales [N/32, K/32] */
+
+#define ENGRAM_TABLE_DEVICE 0       /* table rows in HBM */
+#define ENGRAM_TABLE_HOST_PINNED 1  /* table rows in pinned host memory, read over the
+                                       host link by the GPU (zero copy) */
+
+/* Layer configuration (the HF config fields hidden_size, hc_mult,
+ * rms_norm_eps, engram_max_ngram_size, engram_n_heads, engram_head_dim, and
+ * the scheduler's max_num_batched_tokens, per class Engram.__init__). */
+typedef struct engram_config {
+    int64_t dim;            /* D; multiple of 256 */
+    int64_t hc_mult;        /* H; 1..4 */
+    int64_t max_ngram_size; /* >= 2 */
+    int64_t n_heads;        /* >= 1 */
+    int64_t head_dim;       /* E; multiple of 8, and C*E a multiple of 128 */
+    double eps;             /* rms_norm_eps (1e-6 for DeepSeek-V4.1) */
+    double clamp;           /* lower clamp of |dot| before the square root (1e-6) */
+    int64_t max_tokens;     /* largest T any call will pass; sizes the workspace */
+    int32_t wkv_format;     /* ENGRAM_WKV_* */
+    int32_t table_location; /* ENGRAM_TABLE_* */
+    int32_t device;         /* CUDA device ordinal the handle lives on */
+    int32_t reserved;       /* must be 0 */
+} engram_config;
+
+/* Weights, all borrowed.  Device pointers unless stated. */
+typedef struct engram_weights {
+    const void* table;          /* bf16 [sum(rows), E] row-major: every hash column's
+                                   bucket concatenated (class ParallelEngramEmbedding);
+                                   pinned host memory when table_location is HOST_PINNED;
+                                   16-byte aligned */
+    const int64_t* row_offset;  /* HOST array [C]: first table row of column c */
+    const int64_t* rows;        /* HOST array [C]: rows in column c (a prime per
+                                   class EngramLayout) */
+    const void* wkv;            /* [N, K] row-major, K contiguous (the Linear layout);
+                                   bf16, or e4m3 codes for MXFP8; 16-byte aligned */
+    const uint8_t* wkv_scale;   /* MXFP8 only: E8M0 [N/32, K/32] row-major, one scale
+                                   per 32x32 weight block; NULL for bf16 */
+    const void* q_weight;       /* bf16 [H, D] */
+    const void* k_weight;       /* bf16 [H, D] */
+} engram_weights;
+
+typedef struct engram_handle engram_t;
+
+/* Create a handle on cfg->device: checks the configuration, copies the
+ * row layout, precomputes q*k in fp32, allocates the workspace for
+ * max_tokens (the counterpart of Engram.staged_rows) and builds the TMA
+ * descriptors.  Synchronous.  Errors: INVALID_ARG, UNSUPPORTED, NO_UVA
+ * (host-offloaded table without unified addressing, mirroring the
+ * RuntimeError of ParallelEngramEmbedding.__init__), OOM, CUDA.  On error
+ * *out is set to NULL. */
+int engram_create(const engram_config* cfg, const engram_weights* w, engram_t** out);
+
+/* Free the workspace (synchronises the device first).  NULL is accepted. */
+int engram_destroy(engram_t* h);
+
+/* Gather the rows of T tokens into the handle's staged-rows buffer
+ * (Engram.prepare_embeddings / ParallelEngramEmbedding.lookup):
+ *   staged[t, c*E + j] = table[row_offset[c] + hash_ids[t*ids_row_stride + c], j].
+ * hash_ids: device int32, per-column local ids in [0, rows[c]); row stride
+ * ids_row_stride >= C elements (column stride 1).  An id outside its range
+ * gives a zero row and sets ENGRAM_DEVERR_BAD_HASH_ID.  background != 0
+ * limits the grid to half of the SMs, leaving the rest to concurrent work.
+ * A later engram_forward with hash_ids == NULL consumes these rows. */
+int engram_lookup(engram_t* h, const int32_t* hash_ids, int64_t ids_row_stride, int64_t T,
+                  int background, cudaStream_t stream);
+
+/* Engram.forward: out = hidden + gate * value per (t, h), where
+ *   key_h = kv[t, h*D:(h+1)*D], value = kv[t, H*D:(H+1)*D], kv = rows . wkv^T
+ *   hr = rsqrt(mean_d hidden^2 + eps), kr = rsqrt(mean_d key_h^2 + eps)
+ *   dot = sum_d(hidden * q[h] * k[h] * key_h) * hr * kr / sqrt(D)
+ *   gate = sigmoid(sign(dot) * sqrt(max(|dot|, clamp)))
+ * (the finish kernel of "vllm.models.deepseek_v41.amd.engram" with one rank).
+ * Positions whose token_mask byte is 0 copy hidden's bits unchanged.
+ *   hidden, out: device bf16 [T, H, D]; strides in ELEMENTS {t, h, d}; the d
+ *       stride must be 1 and the t and h strides multiples of 8 (16-byte rows).
+ *       out may be the same buffer as hidden with the same strides (in place);
+ *       any other overlap is INVALID_ARG.
+ *   hash_ids: as for engram_lookup, or NULL to use the rows staged by the
+ *       last engram_lookup (which must have had the same T).
+ *   token_mask: device bytes [T] (0 = False), or NULL for no mask.
+ * The gate is computed in fp32 from an fp32 projection; out is rounded to
+ * bf16 with round-to-nearest-even. */
+int engram_forward(engram_t* h, const void* hidden, const int64_t hidden_strides[3],
+                   const int32_t* hash_ids, int64_t ids_row_stride,
+                   const uint8_t* token_mask, void* out, const int64_t out_strides[3],
+                   int64_t T, cudaStream_t stream);
+
+/* The same forward over HOST buffers: copies hidden, hash_ids and token_mask
+ * (pinned host memory for asynchronous copies) into handle-owned device
+ * buffers, runs engram_forward, and copies out back to the host buffer, all
+ * on `stream`.  Contiguous [T, H, D] hidden/out.  The first call allocates
+ * the host-path buffers for max_tokens. */
+int engram_forward_host(engram_t* h, const void* hidden_host, const int32_t* hash_ids_host,
+                        const uint8_t* token_mask_host, void* out_host, int64_t T,
+                        cudaStream_t stream);
+
+/* Host-side error of the last call on this handle.  With sync != 0 the
+ * device is synchronised and the sticky device error word is read and
+ * cleared: a non-zero word returns ENGRAM_ERR_DEVICE. */
+int engram_last_error(engram_t* h, int sync);
+
+/* Read (and clear, if clear != 0) the sticky device error word into *bits
+ * (ENGRAM_DEVERR_* bits).  Synchronises the device. */
+int engram_device_error(engram_t* h, uint32_t* bits, int clear);
+
+/* class EngramLayout: bucket sizes for n_layers layers.  For every layer
+ * and n-gram order 2..max_ngram_size the counter restarts at vocab_size - 1
+ * and each of n_heads heads takes the next prime above it not used before.
+ * primes, offsets: HOST [n_layers, (max_ngram_size-1)*n_heads]; offsets are
+ * the exclusive cumulative sums within a layer.  Pure host function. */
+int engram_layout(int64_t vocab_size, int32_t max_ngram_size, int32_t n_heads,
+                  int32_t n_layers, int64_t* primes, int64_t* offsets);
+
+/* Validation hook (not part of the layer's semantics): after a forward on
+ * this handle's stream, writes the fp32 gate [T, H] and value [T, D] of the
+ * last call into device buffers, on `stream`.  A gate of 0 marks masked
+ * tokens. */
+int engram_debug_intermediates(engram_t* h, float* gate, float* value, int64_t T,
+                               cudaStream_t stream);
+
+/* Validation hook: copy the staged rows [T, K] bf16 (the gather output) of
+ * the last lookup into `rows` (device), on `stream`. */
+int engram_debug_staged_rows(engram_t* h, void* rows, int64_t T, cudaStream_t stream);
+
+/* Measurement hook: with enable != 0, later engram_forward calls record a
+ * CUDA event before and after each of their kernels on the call's stream
+ * (this serialises the kernels, so programmatic launch overlap is lost).
+ * engram_profile_read waits for the last recorded forward and writes the
+ * durations in milliseconds of its gather, wkv and gate kernels into
+ * ms[0..2] (0 for a kernel that did not run). */
+int engram_profile_enable(engram_t* h, int enable);
+int engram_profile_read(engram_t* h, float ms[3]);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* ENGRAM_GB300_H */

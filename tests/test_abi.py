@@ -1,0 +1,84 @@
+"""Host-side checks of the C ABI (no GPU needed): the library builds, loads
+and exports every entry point include/engram.h declares, the host-only
+layout function agrees with the oracle, and the product package has no
+route to the oracle."""
+import ctypes
+import os
+import re
+import subprocess
+
+import numpy as np
+import pytest
+
+import oracle
+import workloads as W
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+
+
+def _declared_functions():
+    names = set()
+    for fn in os.listdir(os.path.join(ROOT, "include")):
+        if fn.endswith(".h"):
+            src = open(os.path.join(ROOT, "include", fn)).read()
+            names |= set(re.findall(r"^\s*int\s+(engram_\w+)\s*\(", src, re.M))
+    return names
+
+
+@pytest.fixture(scope="module")
+def lib():
+    import __graft_entry__ as g
+    g.build()
+    from hashed_gram_engram_gb300 import _lib
+    return _lib.load()
+
+
+def test_library_exports_every_declared_symbol(lib):
+    from hashed_gram_engram_gb300 import _lib
+    declared = _declared_functions()
+    assert declared, "no declarations found"
+    assert declared == set(_lib.EXPORTED)
+    out = subprocess.run(["nm", "-D", "--defined-only", _lib.LIB_PATH], capture_output=True,
+                         text=True, check=True).stdout
+    exported = set(re.findall(r"\sT\s(engram_\w+)$", out, re.M))
+    assert declared <= exported
+
+
+def test_library_targets_sm103a_only(lib):
+    from hashed_gram_engram_gb300 import build
+    assert "arch=compute_103a,code=sm_103a" in build.ARCH
+
+
+def test_layout_entry_point_matches_oracle(lib):
+    for vocab, ng, heads, layers in ((2 ** 19, 3, 8, 1), (1000, 4, 3, 3), (2 ** 23, 3, 8, 1)):
+        from hashed_gram_engram_gb300 import engram_layout
+        p, o = engram_layout(vocab, ng, heads, layers)
+        rp, ro = oracle.layout(vocab, ng, heads, layers)
+        assert np.array_equal(np.array(p), rp) and np.array_equal(np.array(o), ro)
+    assert list(engram_layout(2 ** 19, 3, 8)[0][0]) == list(W.PRIMES_2POW19)
+
+
+def test_layout_rejects_bad_arguments(lib):
+    buf = (ctypes.c_int64 * 8)()
+    assert lib.engram_layout(0, 3, 4, 1, buf, buf) == -1
+    assert lib.engram_layout(100, 1, 4, 1, buf, buf) == -1
+    assert lib.engram_layout(100, 3, 4, 1, None, buf) == -1
+
+
+def test_null_handle_arguments_are_rejected_without_a_gpu(lib):
+    st = (ctypes.c_int64 * 3)(0, 0, 1)
+    assert lib.engram_lookup(None, None, 0, 1, 0, None) == -1
+    assert lib.engram_forward(None, None, st, None, 0, None, None, st, 1, None) == -1
+    assert lib.engram_destroy(None) == 0
+    out = ctypes.c_void_p()
+    assert lib.engram_create(None, None, ctypes.byref(out)) == -1
+    assert out.value is None
+
+
+def test_product_package_never_reaches_the_oracle():
+    pkg = os.path.join(ROOT, "hashed_gram_engram_gb300")
+    for dirpath, _, files in os.walk(pkg):
+        for fn in files:
+            if fn.endswith((".py", ".cu", ".cuh", ".h")):
+                src = open(os.path.join(dirpath, fn)).read()
+                assert "oracle" not in src, f"{fn} mentions the oracle"

@@ -1,0 +1,216 @@
+"""GPU parity: the CUDA path through the C ABI against the oracle.
+
+Element-by-element on sizes the oracle finishes in seconds (several tiles
+and ragged tails on both wkv schedules), whole-output at the decode
+config, sampled tokens at the prefill config, plus the edge cases: T = 0,
+maximum T, all-False masks, in-place and strided views, out-of-range ids,
+and run-to-run determinism."""
+import dataclasses
+
+import numpy as np
+import pytest
+import torch
+
+import workloads as W
+from engram_case import Case, compare, np_bf16
+from hashed_gram_engram_gb300 import EngramError, ENGRAM_DEVERR_BAD_HASH_ID
+
+pytestmark = pytest.mark.gpu
+
+
+@pytest.fixture(scope="module", autouse=True)
+def _built():
+    import __graft_entry__ as g
+    g.build()
+
+
+@pytest.fixture(scope="module")
+def tiny():
+    return Case(W.TINY, max_tokens=1024)
+
+
+def _run(case, inp, T=None):
+    out = case.layer.forward(inp["hidden"], inp["hash_ids"], inp["token_mask"])
+    torch.cuda.synchronize()
+    T = inp["hidden"].shape[0] if T is None else T
+    gate, value = case.layer.intermediates(T)
+    torch.cuda.synchronize()
+    return out, gate, value
+
+
+def test_tiny_forward_matches_oracle(tiny):
+    inp = tiny.step_inputs()
+    out, gate, value = _run(tiny, inp)
+    ref = tiny.oracle(inp)
+    compare(tiny, inp, out, ref, gate=gate, value=value)
+    # the gather is bit-exact
+    rows = tiny.layer.staged_rows(W.TINY.T)
+    torch.cuda.synchronize()
+    assert np.array_equal(W.bits(rows), ref["rows"].reshape(W.TINY.T, -1))
+    assert tiny.layer.device_error() == 0
+
+
+@pytest.mark.parametrize("T", [1, 5, 16, 31, 100, 255, 256])
+def test_tokens_as_n_path_ragged_T(tiny, T):
+    inp = tiny.step_inputs(T=T, step=T)
+    out, gate, value = _run(tiny, inp)
+    compare(tiny, inp, out, tiny.oracle(inp), gate=gate, value=value)
+
+
+@pytest.mark.parametrize("T", [257, 300, 640, 1024])
+def test_tokens_as_m_path_ragged_T(tiny, T):
+    inp = tiny.step_inputs(T=T, step=T)
+    out, gate, value = _run(tiny, inp)
+    compare(tiny, inp, out, tiny.oracle(inp), gate=gate, value=value)
+
+
+def test_separate_lookup_then_forward(tiny):
+    inp = tiny.step_inputs(T=40, step=7)
+    tiny.layer.lookup(inp["hash_ids"])
+    out = tiny.layer.forward(inp["hidden"], None, inp["token_mask"])
+    torch.cuda.synchronize()
+    compare(tiny, inp, out, tiny.oracle(inp))
+
+
+def test_background_lookup_matches(tiny):
+    inp = tiny.step_inputs(T=300, step=8)
+    tiny.layer.lookup(inp["hash_ids"], background=True)
+    out = tiny.layer.forward(inp["hidden"], None, inp["token_mask"])
+    torch.cuda.synchronize()
+    compare(tiny, inp, out, tiny.oracle(inp))
+
+
+def test_all_false_mask_passes_hidden_through(tiny):
+    for T in (16, 300):
+        inp = tiny.step_inputs(T=T, step=9)
+        inp["token_mask"] = torch.zeros(T, dtype=torch.uint8, device="cuda")
+        h = inp["hidden"]
+        h[0, 0, :4] = torch.tensor([-0.0, float("inf"), float("-inf"), 1e-40],
+                                   dtype=torch.bfloat16)
+        out, gate, _ = _run(tiny, inp)
+        assert torch.equal(out.view(torch.int16), h.view(torch.int16))
+        assert torch.all(gate == 0)
+
+
+def test_gate_range_and_shared_value(tiny):
+    inp = tiny.step_inputs(T=64, step=10)
+    inp["token_mask"] = None
+    out, gate, value = _run(tiny, inp)
+    g = gate.double().cpu().numpy()
+    assert np.all((g > 0) & (g < 1)) and np.all(np.abs(g - 0.5) >= 2.4e-4)
+
+
+def test_in_place_and_strided_views(tiny):
+    T = 48
+    inp = tiny.step_inputs(T=T, step=11)
+    ref = tiny.oracle(inp)
+    H, D = W.TINY.hc_mult, W.TINY.dim
+    # strided: hc copies padded apart, tokens padded apart
+    big = torch.zeros((T, H + 1, D + 64), dtype=torch.bfloat16, device="cuda")
+    big[:, :H, :D] = inp["hidden"]
+    hv = big[:, :H, :D]
+    outbig = torch.full((T, H, D + 8), 7.0, dtype=torch.bfloat16, device="cuda")
+    ov = outbig[:, :, :D]
+    tiny.layer.forward(hv, inp["hash_ids"], inp["token_mask"], out=ov)
+    torch.cuda.synchronize()
+    compare(tiny, inp, ov, ref)
+    assert torch.all(outbig[:, :, D:] == 7.0)
+    # in place
+    h2 = inp["hidden"].clone()
+    tiny.layer.forward(h2, inp["hash_ids"], inp["token_mask"], out=h2)
+    torch.cuda.synchronize()
+    assert torch.equal(h2.view(torch.int16), ov.contiguous().view(torch.int16))
+
+
+def test_strided_hash_ids(tiny):
+    T = 70
+    inp = tiny.step_inputs(T=T, step=12)
+    wide = torch.full((T, W.TINY.n_hash_cols + 5), -1, dtype=torch.int32, device="cuda")
+    wide[:, :W.TINY.n_hash_cols] = inp["hash_ids"]
+    out = tiny.layer.forward(inp["hidden"], wide[:, :W.TINY.n_hash_cols], inp["token_mask"])
+    torch.cuda.synchronize()
+    compare(tiny, inp, out, tiny.oracle(inp))
+
+
+def test_deterministic_across_runs(tiny):
+    for T in (77, 513):
+        inp = tiny.step_inputs(T=T, step=13)
+        a = tiny.layer.forward(inp["hidden"], inp["hash_ids"], inp["token_mask"])
+        b = tiny.layer.forward(inp["hidden"], inp["hash_ids"], inp["token_mask"])
+        torch.cuda.synchronize()
+        assert torch.equal(a.view(torch.int16), b.view(torch.int16))
+
+
+def test_zero_tokens_and_limits(tiny):
+    empty_h = torch.empty((0, W.TINY.hc_mult, W.TINY.dim), dtype=torch.bfloat16, device="cuda")
+    empty_ids = torch.empty((0, W.TINY.n_hash_cols), dtype=torch.int32, device="cuda")
+    out = tiny.layer.forward(empty_h, empty_ids)
+    assert out.shape == empty_h.shape
+    tiny.layer.lookup(empty_ids)
+    big = tiny.step_inputs(T=1025, step=14)
+    with pytest.raises(EngramError) as e:
+        tiny.layer.forward(big["hidden"], big["hash_ids"])
+    assert e.value.code == -3
+    inp = tiny.step_inputs(T=8, step=15)
+    with pytest.raises(EngramError) as e:  # overlapping, non-identical out
+        tiny.layer.forward(inp["hidden"][1:], inp["hash_ids"][1:], out=inp["hidden"][:-1])
+    assert e.value.code == -1
+    with pytest.raises(EngramError) as e:  # staged rows of another T
+        tiny.layer.lookup(inp["hash_ids"][:4])
+        tiny.layer.forward(inp["hidden"], None)
+    assert e.value.code == -1
+    torch.cuda.synchronize()
+    assert tiny.layer.device_error() == 0
+
+
+def test_out_of_range_ids_zero_the_row_and_flag(tiny):
+    T = 20
+    inp = tiny.step_inputs(T=T, step=16)
+    ids = inp["hash_ids"].clone()
+    ids[3, 2] = W.TINY.rows[2]  # one past the end
+    ids[7, 5] = -4
+    tiny.layer.forward(inp["hidden"], ids, inp["token_mask"])
+    torch.cuda.synchronize()
+    assert tiny.layer.device_error() & ENGRAM_DEVERR_BAD_HASH_ID
+    rows = W.bits(tiny.layer.staged_rows(T)).reshape(T, W.TINY.n_hash_cols, W.TINY.head_dim)
+    assert not rows[3, 2].any() and not rows[7, 5].any()
+    assert tiny.layer.device_error() == 0  # cleared
+
+
+# ---------------------------------------------------------------- full configs
+
+@pytest.fixture(scope="module")
+def decode():
+    return Case(W.DECODE, max_tokens=W.PREFILL.T)
+
+
+def test_decode_config_full(decode):
+    inp = decode.step_inputs()
+    out, gate, value = _run(decode, inp)
+    res = compare(decode, inp, out, decode.oracle(inp), gate=gate, value=value)
+    assert decode.layer.device_error() == 0
+    print("decode", res)
+
+
+def test_prefill_config_sampled(decode):
+    wl = W.PREFILL
+    case = decode
+    case.wl = wl  # same weights and table; prefill ids, mask and T
+    try:
+        inp = case.step_inputs()
+        out, gate, value = _run(case, inp)
+        T = wl.T
+        m = W.bits(inp["token_mask"]).astype(bool)
+        rng = np.random.default_rng(0)
+        tokens = np.unique(np.concatenate([
+            [0, 1, 127, 128, T - 129, T - 1], rng.choice(T, 40, replace=False),
+            np.flatnonzero(~m)[:4]]))
+        ref = case.oracle(inp, tokens=tokens)
+        compare(case, inp, out, ref, tokens=tokens, gate=gate, value=value)
+        # properties at every token
+        assert np.array_equal(W.bits(out)[~m], W.bits(inp["hidden"])[~m])
+        g = gate.double().cpu().numpy()
+        assert np.all(g[~m] == 0) and np.all((g[m] > 0) & (g[m] < 1))
+        assert case.layer.device_error() == 0
+    finally:
+        case.wl = W.DECODE
