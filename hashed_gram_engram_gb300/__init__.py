@@ -20,7 +20,8 @@ from . import _lib
 from ._lib import (EngramError, engram_config, engram_create, engram_debug_intermediates,
                    engram_debug_staged_rows, engram_destroy, engram_device_error,
                    engram_forward, engram_forward_host, engram_last_error, engram_layout,
-                   engram_lookup, engram_weights, ENGRAM_WKV_BF16, ENGRAM_WKV_MXFP8,
+                   engram_lookup, engram_profile_enable, engram_profile_read,
+                   engram_weights, ENGRAM_WKV_BF16, ENGRAM_WKV_MXFP8,
                    ENGRAM_TABLE_DEVICE, ENGRAM_TABLE_HOST_PINNED, ENGRAM_DEVERR_BAD_HASH_ID,
                    ENGRAM_DEVERR_TIMEOUT)
 
@@ -28,7 +29,8 @@ __all__ = [
     "Engram", "EngramError", "engram_config", "engram_weights", "engram_create",
     "engram_destroy", "engram_lookup", "engram_forward", "engram_forward_host",
     "engram_last_error", "engram_device_error", "engram_layout", "engram_debug_intermediates",
-    "engram_debug_staged_rows", "ENGRAM_WKV_BF16", "ENGRAM_WKV_MXFP8", "ENGRAM_TABLE_DEVICE",
+    "engram_debug_staged_rows", "engram_profile_enable", "engram_profile_read",
+    "ENGRAM_WKV_BF16", "ENGRAM_WKV_MXFP8", "ENGRAM_TABLE_DEVICE",
     "ENGRAM_TABLE_HOST_PINNED", "ENGRAM_DEVERR_BAD_HASH_ID", "ENGRAM_DEVERR_TIMEOUT",
 ]
 
