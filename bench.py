@@ -4,9 +4,12 @@ A step is one whole forward (gather, wkv projection, gate and residual) of
 one batch of synthetic inputs resident in HBM, through the C ABI.  The
 headline workload is the decode step (T = 64, dim 4096, hc_mult 4, 16 hash
 columns of head_dim 64, bf16 wkv [20480, 1024]); the prefill step
-(T = 8192) is reported alongside.  L2 (129 MB) is flushed by writing a
-512 MB buffer between timed steps; each step is timed with CUDA events on
-its stream.
+(T = 8192) is reported alongside.  Decode steps rotate over several
+independently seeded layers whose weights together exceed the 129 MB L2,
+so every step reads its weights from HBM; the rotation is captured in a
+CUDA graph and timed with CUDA events on its stream.  The single-step
+latency with L2 flushed (a 512 MB write) before every step is reported
+too.
 
   python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
 
@@ -42,6 +45,7 @@ def parse():
     p.add_argument("--no-prefill", action="store_true")
     p.add_argument("--no-cpu-baseline", action="store_true")
     p.add_argument("--cpu-seconds", type=float, default=10.0)
+    p.add_argument("--layers", type=int, default=6)
     return p.parse_args()
 
 
@@ -179,6 +183,19 @@ def run_reference(args):
     print(json.dumps(line), flush=True)
 
 
+def make_layer(W, Engram, wl, device_index, max_tokens, layer_seed):
+    import dataclasses
+    wl_l = dataclasses.replace(wl, seed=wl.seed + 101 * layer_seed)
+    table = W.make_table(wl_l, "cuda")
+    wts = W.make_weights(wl_l, "cuda")
+    layer = Engram(dim=wl.dim, hc_mult=wl.hc_mult, max_ngram_size=wl.max_ngram_size,
+                   n_heads=wl.n_heads, head_dim=wl.head_dim, max_tokens=max_tokens,
+                   table=table, rows=wl.rows, row_offset=W.row_offsets(wl.rows),
+                   wkv=wts["wkv"], q_weight=wts["q_weight"], k_weight=wts["k_weight"],
+                   eps=wl.eps, clamp=wl.clamp, device=device_index)
+    return wl_l, layer, table, wts
+
+
 def main():
     args = parse()
     if args.impl == "reference":
@@ -203,84 +220,115 @@ def main():
         dist.barrier()
     g.build()
     hbm_peak, bf16_peak, peak_kind = peaks()
+    stream = torch.cuda.Stream(dev)
+    torch.cuda.set_stream(stream)
 
+    # Decode: a rotation over NL independently seeded layers (each its own
+    # table, wkv, q, k, hidden and ids).  Their packed weights (NL x 40 MiB)
+    # exceed the 129 MB L2, so consecutive steps read weights from HBM and no
+    # flush is needed between them.  The rotation is captured in a CUDA graph
+    # (as a serving engine runs decode) and replayed.
     wl = W.DECODE
-    table = W.make_table(wl, "cuda")
-    wts = W.make_weights(wl, "cuda")
-    layer = Engram(dim=wl.dim, hc_mult=wl.hc_mult, max_ngram_size=wl.max_ngram_size,
-                   n_heads=wl.n_heads, head_dim=wl.head_dim, max_tokens=W.PREFILL.T,
-                   table=table, rows=wl.rows, row_offset=W.row_offsets(wl.rows),
-                   wkv=wts["wkv"], q_weight=wts["q_weight"], k_weight=wts["k_weight"],
-                   eps=wl.eps, clamp=wl.clamp, device=local)
-    step = W.make_step_inputs(wl, "cuda", step=rank)
-    hidden, ids, mask = step["hidden"], step["hash_ids"], step["token_mask"]
-    out = torch.empty_like(hidden)
-    flush = torch.empty(L2_FLUSH_BYTES, dtype=torch.uint8, device=dev)
-    stream = torch.cuda.current_stream(dev)
-
-    def timed(fn, K, profile=False):
-        starts = [torch.cuda.Event(enable_timing=True) for _ in range(K)]
-        ends = [torch.cuda.Event(enable_timing=True) for _ in range(K)]
-        prof = []
-        for i in range(K):
-            flush.zero_()
-            starts[i].record(stream)
-            fn()
-            ends[i].record(stream)
-            if profile:
-                prof.append(engram_profile_read(layer.handle))
-        torch.cuda.synchronize()
-        return [s.elapsed_time(e) for s, e in zip(starts, ends)], prof
-
-    fwd = lambda: layer.forward(hidden, ids, mask, out=out, stream=stream)  # noqa: E731
-    for _ in range(max(3, args.warmup)):
-        fwd()
+    NL = args.layers
+    layers = []
+    for l in range(NL):
+        wl_l, layer, table, wts = make_layer(W, Engram, wl, local, W.PREFILL.T if l == 0 else wl.T,
+                                             l + 1000 * rank)
+        st = W.make_step_inputs(wl_l, "cuda", step=rank)
+        layers.append(dict(wl=wl_l, layer=layer, table=table, wts=wts, hidden=st["hidden"],
+                           ids=st["hash_ids"], out=torch.empty_like(st["hidden"])))
     torch.cuda.synchronize()
+
+    def step(L):
+        L["layer"].forward(L["hidden"], L["ids"], None, out=L["out"], stream=stream)
+
+    for _ in range(max(3, args.warmup)):
+        for L in layers:
+            step(L)
+    torch.cuda.synchronize()
+    per_graph = NL * max(1, 24 // NL)
+    graph = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(graph, stream=stream):
+        for i in range(per_graph):
+            step(layers[i % NL])
+    for _ in range(3):
+        graph.replay()
+    torch.cuda.synchronize()
+    replays = max(1, args.steps // per_graph)
+    steps = replays * per_graph
 
     clocks = Clocks(local)
     clocks.start()
     if world > 1:
         dist.barrier()
     torch.cuda.synchronize()
-    ms, _ = timed(fwd, args.steps)
+    e0 = torch.cuda.Event(enable_timing=True)
+    e1 = torch.cuda.Event(enable_timing=True)
+    e0.record(stream)
+    for _ in range(replays):
+        graph.replay()
+    e1.record(stream)
     torch.cuda.synchronize()
     if world > 1:
         dist.barrier()
     clk = clocks.stop()
-    total_ms = sum(ms)
+    total_ms = e0.elapsed_time(e1)
     t = torch.tensor([total_ms], dtype=torch.float64, device=dev)
     if world > 1:
         dist.all_reduce(t, op=dist.ReduceOp.MAX)
     total_ms = float(t.item())
-    value = world * wl.T * args.steps / (total_ms / 1e3)
+    ms_step = total_ms / steps
+    value = world * wl.T * steps / (total_ms / 1e3)
 
-    # per-kernel durations (events between the kernels: serialised launches)
-    engram_profile_enable(layer.handle, 1)
-    _, prof = timed(fwd, min(args.steps, 200), profile=True)
-    engram_profile_enable(layer.handle, 0)
-    prof = np.array(prof)
-    k_gather, k_wkv, k_gate = [float(np.median(prof[:, i])) for i in range(3)]
-    wkv_bytes = wl.N * wl.K * 2 + wl.T * wl.K * 2
     step_bytes = (wl.N * wl.K * 2 + 2 * wl.T * wl.hc_mult * wl.dim * 2 + wl.T * wl.K * 2
                   + wl.T * wl.n_hash_cols * 4 + 2 * wl.hc_mult * wl.dim * 2)
-    achieved = wkv_bytes / (k_wkv * 1e-3) / 1e9
+    # one kernel per step: its average duration is the step time (launch gaps included)
+    achieved = step_bytes / (ms_step * 1e-3) / 1e9
     traffic = None
     tr_path = os.path.join(ROOT, "profiles", "traffic.json")
     if os.path.exists(tr_path):
         try:
-            traffic = json.load(open(tr_path)).get("wkv_tokens_n_decode")
+            traffic = json.load(open(tr_path)).get("decode_fused")
         except Exception:
             traffic = None
 
+    # single-step latency with L2 flushed before the step (cold code, page
+    # tables and weights), and the kernel's own event time
+    L0 = layers[0]
+    flush = torch.empty(L2_FLUSH_BYTES, dtype=torch.uint8, device=dev)
+    lat = []
+    engram_profile_enable(L0["layer"].handle, 1)
+    kern = []
+    for i in range(min(args.steps, 200)):
+        flush.zero_()
+        a0 = torch.cuda.Event(enable_timing=True)
+        a1 = torch.cuda.Event(enable_timing=True)
+        a0.record(stream)
+        step(L0)
+        a1.record(stream)
+        kern.append(engram_profile_read(L0["layer"].handle)[1])
+        torch.cuda.synchronize()
+        lat.append(a0.elapsed_time(a1))
+    engram_profile_enable(L0["layer"].handle, 0)
+    del flush
+
     # end to end through the host-buffer entry point
-    hid_h = hidden.cpu().pin_memory()
-    ids_h = ids.cpu().pin_memory()
+    hid_h = L0["hidden"].cpu().pin_memory()
+    ids_h = L0["ids"].cpu().pin_memory()
     out_h = torch.empty_like(hid_h).pin_memory()
-    fwd_h = lambda: layer.forward_host(hid_h, ids_h, None, out_h, stream=stream)  # noqa: E731
+    fwd_h = lambda: L0["layer"].forward_host(hid_h, ids_h, None, out_h, stream=stream)  # noqa: E731
     for _ in range(3):
         fwd_h()
-    ms_h, _ = timed(fwd_h, min(args.steps, 500))
-    e2e_ms = float(np.mean(ms_h))
+    torch.cuda.synchronize()
+    ne = min(args.steps, 500)
+    b0 = torch.cuda.Event(enable_timing=True)
+    b1 = torch.cuda.Event(enable_timing=True)
+    b0.record(stream)
+    for _ in range(ne):
+        fwd_h()
+    b1.record(stream)
+    torch.cuda.synchronize()
+    e2e_ms = b0.elapsed_time(b1) / ne
     th = torch.tensor([e2e_ms], dtype=torch.float64, device=dev)
     if world > 1:
         dist.all_reduce(th, op=dist.ReduceOp.MAX)
@@ -288,49 +336,63 @@ def main():
 
     line = {
         "metric": METRIC, "value": value, "unit": "tokens/s", "n_gpus": world,
-        "steps": args.steps, "warmup": args.warmup, "ms_per_step": total_ms / args.steps,
+        "steps": steps, "warmup": args.warmup, "ms_per_step": ms_step,
         "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "bf16",
         "data": "synthetic",
         "config": {"workload": "decode", "T": wl.T, "dim": wl.dim, "hc_mult": wl.hc_mult,
                    "n_hash_cols": wl.n_hash_cols, "head_dim": wl.head_dim,
                    "table_rows": wl.total_rows, "wkv": "bf16 [20480, 1024]", "mask": None,
-                   "l2": "flushed (512 MB write) before every timed step",
+                   "layers_rotated": NL,
+                   "l2": f"inputs larger than L2: {NL} layers' weights ({NL * 40} MiB) rotated",
+                   "timing": f"CUDA graph of {per_graph} steps replayed {replays}x, events on "
+                             "the launch stream",
                    "parallelism": f"replicas x{world} (token-sharded, no collective)"},
-        "roofline": {"bound": "hbm", "kernel": "wkv_gemm_bf16 (token-as-N, stream-K)",
+        "roofline": {"bound": "hbm",
+                     "kernel": "decode_fused_kernel (gather4 + tcgen05 wkv + gate, one launch)",
                      "achieved": achieved, "peak": hbm_peak, "unit": "GB/s",
                      "frac": achieved / hbm_peak, "traffic": traffic,
-                     "peak_kind": peak_kind, "algorithmic_bytes": wkv_bytes,
-                     "kernel_ms": k_wkv},
-        "step_roofline": {"algorithmic_bytes": step_bytes,
-                          "achieved_gbs": step_bytes / (total_ms / args.steps * 1e-3) / 1e9,
-                          "frac": step_bytes / (total_ms / args.steps * 1e-3) / 1e9 / hbm_peak},
-        "kernel_ms": {"gather": k_gather, "wkv": k_wkv, "gate": k_gate},
+                     "peak_kind": peak_kind, "algorithmic_bytes": step_bytes,
+                     "kernel_ms": ms_step},
+        "latency_l2_flushed_us": {"step_median": 1e3 * float(np.median(lat)),
+                                  "kernel_median": 1e3 * float(np.median(kern))},
         "e2e": {"value": wl.T / (e2e_ms * 1e-3) * world, "unit": "tokens/s",
                 "h2d_bytes_per_step": int(hid_h.numel() * 2 + ids_h.numel() * 4),
                 "d2h_bytes_per_step": int(out_h.numel() * 2)},
-        "gpu_launches": 3 * args.steps,
+        "gpu_launches": steps,
         "clocks": clk,
     }
 
     if not args.no_prefill:
         pw = W.PREFILL
+        layer = L0["layer"]
         pstep = W.make_step_inputs(pw, "cuda", step=rank)
         ph, pids, pmask = pstep["hidden"], pstep["hash_ids"], pstep["token_mask"]
         pout = torch.empty_like(ph)
         pf = lambda: layer.forward(ph, pids, pmask, out=pout, stream=stream)  # noqa: E731
         for _ in range(3):
             pf()
+        torch.cuda.synchronize()
         pk = max(5, min(50, args.steps))
-        pms, _ = timed(pf, pk)
+        c0 = torch.cuda.Event(enable_timing=True)
+        c1 = torch.cuda.Event(enable_timing=True)
+        c0.record(stream)
+        for _ in range(pk):
+            pf()
+        c1.record(stream)
+        torch.cuda.synchronize()
+        p_ms = c0.elapsed_time(c1) / pk
         engram_profile_enable(layer.handle, 1)
-        _, pprof = timed(pf, 10, profile=True)
+        pprof = []
+        for _ in range(10):
+            pf()
+            pprof.append(engram_profile_read(layer.handle))
         engram_profile_enable(layer.handle, 0)
         pprof = np.array(pprof)
         pw_ms = float(np.median(pprof[:, 1]))
         flops = 2.0 * pw.T * pw.N * pw.K
         line["prefill"] = {
-            "workload": "prefill", "T": pw.T, "tokens_per_s": pw.T / (float(np.mean(pms)) * 1e-3),
-            "ms_per_step": float(np.mean(pms)),
+            "workload": "prefill", "T": pw.T, "tokens_per_s": pw.T / (p_ms * 1e-3),
+            "ms_per_step": p_ms, "l2": "inputs larger than L2 (hidden 256 MiB per step)",
             "kernel_ms": {"gather": float(np.median(pprof[:, 0])), "wkv": pw_ms,
                           "gate": float(np.median(pprof[:, 2]))},
             "roofline": {"bound": "tensor", "kernel": "wkv_gemm_bf16 (token-as-M)",
@@ -340,10 +402,10 @@ def main():
         }
 
     if rank == 0 and world == 1 and not args.no_cpu_baseline:
-        host = dict(table=W.bits(table), row_offset=W.row_offsets(wl.rows),
-                    rows=np.asarray(wl.rows, np.int64), wkv=W.bits(wts["wkv"]),
-                    q=W.bits(wts["q_weight"]), k=W.bits(wts["k_weight"]))
-        inp = dict(hidden=W.bits(hidden), ids=ids.cpu().numpy(), mask=None)
+        host = dict(table=W.bits(L0["table"]), row_offset=W.row_offsets(wl.rows),
+                    rows=np.asarray(wl.rows, np.int64), wkv=W.bits(L0["wts"]["wkv"]),
+                    q=W.bits(L0["wts"]["q_weight"]), k=W.bits(L0["wts"]["k_weight"]))
+        inp = dict(hidden=W.bits(L0["hidden"]), ids=L0["ids"].cpu().numpy(), mask=None)
         tps, n, el = cpu_oracle_tokens_per_s(wl, host, inp, args.cpu_seconds)
         line["cpu_baseline"] = {"value": tps, "unit": "tokens/s", "cores": 1, "kind": "oracle",
                                 "sample": f"{n} decode-step tokens ({el:.1f} s, "
@@ -351,7 +413,8 @@ def main():
                                 "host_cores": os.cpu_count()}
     if rank == 0:
         print(json.dumps(line), flush=True)
-    layer.close()
+    for L in layers:
+        L["layer"].close()
     if world > 1:
         dist.destroy_process_group()
 

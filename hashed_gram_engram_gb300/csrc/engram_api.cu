@@ -90,6 +90,7 @@ void free_handle(engram_handle* h) {
     void* ptrs[] = {h->d_row_offset, h->d_rows,      h->ws.staged,   h->ws.staged_q,
                     h->ws.staged_s,  h->ws.kvpart,   h->ws.partials, h->ws.value,
                     h->ws.gate,      h->ws.qk,       h->ws.wscale_rows, h->ws.err,
+                    h->ws.wpack,     h->ws.fpart,    h->ws.fvalue,   h->ws.grid_bar,
                     h->ws.host_hidden, h->ws.host_ids, h->ws.host_mask};
     for (void* p : ptrs)
         if (p) cudaFree(p);
@@ -249,6 +250,11 @@ int engram_create(const engram_config* cfg, const engram_weights* w, engram_t** 
         step(dalloc(&ws.value, ws.rows_alloc * c.dim * 2, true));
     }
     step(dalloc(&ws.gate, ws.rows_alloc * c.hc_mult * sizeof(float), true));
+    // fused decode kernel workspace, sized for the largest T it serves
+    step(dalloc(&ws.wpack, N * K * 2, false));
+    step(dalloc(&ws.fpart, ws.kv_tpitch * sms * 8 * sizeof(float), true));
+    step(dalloc(&ws.fvalue, ws.kv_tpitch * c.dim * sizeof(float), true));
+    step(dalloc(&ws.grid_bar, 4 * sizeof(unsigned), true));
     step(dalloc(&ws.qk, c.hc_mult * c.dim * sizeof(float), false));
     step(dalloc(&ws.err, sizeof(unsigned), true));
     if (e == cudaSuccess)
@@ -256,7 +262,9 @@ int engram_create(const engram_config* cfg, const engram_weights* w, engram_t** 
     if (e == cudaSuccess)
         e = cudaMemcpy(h->d_rows, w->rows, C * sizeof(int64_t), cudaMemcpyHostToDevice);
     if (e == cudaSuccess) e = launch_qk(h, 0);
+    if (e == cudaSuccess) e = pack_weights(h, 0);
     if (e == cudaSuccess) e = gemm_setup_attributes();
+    if (e == cudaSuccess) e = fused_setup_attributes();
     if (e == cudaSuccess) e = cudaDeviceSynchronize();
     if (e != cudaSuccess) {
         free_handle(h);
@@ -331,6 +339,21 @@ int engram_forward(engram_t* h, const void* hidden, const int64_t hidden_strides
     auto mark = [&](int i) {
         if (prof && e == cudaSuccess) e = cudaEventRecord(h->ev[i], stream);
     };
+    if (fused_supported(h, T)) {
+        // decode: one cooperative kernel, the gather included when ids are given
+        h->ev_ran[0] = false;
+        h->ev_ran[1] = true;
+        h->ev_ran[2] = false;
+        mark(0);
+        mark(1);
+        e = launch_decode_fused(h, hidden, hidden_strides, hash_ids, ids_row_stride, token_mask,
+                                out, out_strides, T, stream);
+        if (hash_ids != nullptr) h->staged_T = T;  // the kernel staged the rows
+        mark(2);
+        mark(3);
+        h->last_path = 3;
+        return cuda_err(h, e);
+    }
     h->ev_ran[0] = hash_ids != nullptr;
     h->ev_ran[1] = h->ev_ran[2] = true;
     mark(0);
@@ -341,14 +364,7 @@ int engram_forward(engram_t* h, const void* hidden, const int64_t hidden_strides
         first = false;
     }
     mark(1);
-    if (T <= kMaxDecodeT) {
-        if (e == cudaSuccess) e = launch_wkv_tokens_n(h, T, stream, !first && !prof);
-        mark(2);
-        if (e == cudaSuccess)
-            e = launch_gate_from_kvpart(h, hidden, hidden_strides, token_mask, out, out_strides, T,
-                                        stream, !prof);
-        h->last_path = 1;
-    } else {
+    {
         if (e == cudaSuccess)
             e = launch_wkv_tokens_m(h, hidden, hidden_strides[0], hidden_strides[1], T, stream,
                                     !first && !prof);
@@ -416,6 +432,11 @@ int engram_device_error(engram_t* h, uint32_t* bits, int clear) {
     cudaError_t e = cudaDeviceSynchronize();
     if (e == cudaSuccess) e = cudaMemcpy(bits, h->ws.err, sizeof(unsigned), cudaMemcpyDeviceToHost);
     if (e == cudaSuccess && clear) e = cudaMemset(h->ws.err, 0, sizeof(unsigned));
+    if (e == cudaSuccess && (*bits & ENGRAM_DEVERR_TIMEOUT)) {
+        // an unwound launch can leave the grid barrier's arrival count
+        // short: start it again from zero
+        e = cudaMemset(h->ws.grid_bar, 0, 4 * sizeof(unsigned));
+    }
     if (e != cudaSuccess) return ENGRAM_ERR_CUDA;
     return ENGRAM_OK;
 }
@@ -431,7 +452,8 @@ int engram_debug_intermediates(engram_t* h, float* gate, float* value, int64_t T
                             cudaMemcpyDeviceToDevice, stream);
     if (e == cudaSuccess && value != nullptr) {
         if (h->last_path == 0) return ENGRAM_ERR_INVALID_ARG;
-        e = launch_debug_value(h, value, T, stream);
+        e = h->last_path == 3 ? launch_fused_debug_value(h, value, T, stream)
+                              : launch_debug_value(h, value, T, stream);
     }
     return e == cudaSuccess ? ENGRAM_OK : ENGRAM_ERR_CUDA;
 }

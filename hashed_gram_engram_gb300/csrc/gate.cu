@@ -223,11 +223,11 @@ __global__ void qk_kernel(const uint16_t* q, const uint16_t* k, float* qk, int64
 // fp32 value [T, D] of the last forward, for validation.
 __global__ void debug_value_kernel(const float* kvpart, int m_tiles, int tpitch, int k_blocks,
                                    int total, int grid, const uint16_t* value, int H, int D,
-                                   int T, bool from_kvpart, float* out) {
+                                   int T, int path, float* out) {
     const int64_t i = static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x;
     if (i >= static_cast<int64_t>(T) * D) return;
     const int t = static_cast<int>(i / D), d = static_cast<int>(i % D);
-    if (!from_kvpart) {
+    if (path == 2) {
         out[i] = __uint_as_float(static_cast<uint32_t>(value[i]) << 16);
         return;
     }
@@ -318,8 +318,8 @@ cudaError_t launch_debug_value(const engram_handle* h, float* value, int64_t T, 
     const int64_t n = T * h->cfg.dim;
     debug_value_kernel<<<static_cast<unsigned>((n + 255) / 256), 256, 0, s>>>(
         h->ws.kvpart, sc.m_tiles, static_cast<int>(h->ws.kv_tpitch), sc.k_blocks, sc.total,
-        sc.grid, h->ws.value, static_cast<int>(h->cfg.hc_mult), static_cast<int>(h->cfg.dim),
-        static_cast<int>(T), h->last_path == 1, value);
+        sc.grid, h->ws.value, static_cast<int>(h->cfg.hc_mult),
+        static_cast<int>(h->cfg.dim), static_cast<int>(T), h->last_path, value);
     return cudaGetLastError();
 }
 

@@ -16,6 +16,9 @@ constexpr int kBNPrefill = 256;   // kv columns per tile when tokens are the M s
 constexpr int kKBlockBytes = 128; // bytes of K per pipeline stage (one swizzle row)
 constexpr int kMaxDecodeT = 256;  // largest T served by the token-as-N (GEMV-shaped) path
 constexpr int kGemmSmemBytes = 192 * 1024 + 2048;  // > half an SM: one CTA per SM
+constexpr int kFusedSmemBytes = 225 * 1024;       // fused decode kernel
+constexpr int kMaxFusedT = 256;                   // largest T of the fused decode kernel
+constexpr int kMaxFusedSlice = 256;               // widest column slice of one CTA (MMA N)
 
 struct Workspace {
     // staged gather output (Engram.staged_rows): bf16 [rows_alloc, K]
@@ -39,10 +42,21 @@ struct Workspace {
     uint8_t* wscale_rows = nullptr;
     // sticky device error word
     unsigned* err = nullptr;
+    // fused decode kernel: wkv packed k-block-major as swizzled shared-memory
+    // images, per-(token, CTA) gate partial sums, the fp32 value, the
+    // grid-barrier counter
+    uint16_t* wpack = nullptr;
+    float* fpart = nullptr;     // [kv_tpitch][num_sms][8]
+    float* fvalue = nullptr;    // [kv_tpitch][D]
+    unsigned* grid_bar = nullptr;  // two {count, generation} grid barriers of the fused kernel
     // host path staging (engram_forward_host)
     void* host_hidden = nullptr;
     int32_t* host_ids = nullptr;
     uint8_t* host_mask = nullptr;
+};
+
+struct FusedPlan {
+    int Tn, mtiles, granules, k_blocks, grid, max_width;
 };
 
 struct DecodeSchedule {
@@ -96,6 +110,18 @@ cudaError_t launch_wkv_tokens_n(const engram_handle* h, int64_t T, cudaStream_t 
 cudaError_t launch_wkv_tokens_m(const engram_handle* h, const void* hidden, int64_t hs_t,
                                 int64_t hs_h, int64_t T, cudaStream_t s, bool pdl);
 cudaError_t gemm_setup_attributes();
+
+// decode_fused.cu
+FusedPlan fused_plan(const engram_handle* h, int64_t T);
+bool fused_supported(const engram_handle* h, int64_t T);
+cudaError_t fused_setup_attributes();
+cudaError_t pack_weights(const engram_handle* h, cudaStream_t s);
+cudaError_t launch_fused_debug_value(const engram_handle* h, float* value, int64_t T,
+                                     cudaStream_t s);
+// ids == nullptr: the rows were staged by engram_lookup
+cudaError_t launch_decode_fused(engram_handle* h, const void* hidden, const int64_t* hs,
+                                const int32_t* ids, int64_t ids_stride, const uint8_t* mask,
+                                void* out, const int64_t* os, int64_t T, cudaStream_t s);
 
 // gate.cu
 cudaError_t launch_gate_from_kvpart(const engram_handle* h, const void* hidden,

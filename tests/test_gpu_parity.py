@@ -187,9 +187,44 @@ def decode():
 def test_decode_config_full(decode):
     inp = decode.step_inputs()
     out, gate, value = _run(decode, inp)
-    res = compare(decode, inp, out, decode.oracle(inp), gate=gate, value=value)
+    ref = decode.oracle(inp)
+    res = compare(decode, inp, out, ref, gate=gate, value=value)
     assert decode.layer.device_error() == 0
     print("decode", res)
+    # the gather kernel (engram_lookup) is bit-exact on the full-size table, and
+    # the forward that consumes its staged rows matches the forward that
+    # gathers with tile::gather4 bit for bit
+    decode.layer.lookup(inp["hash_ids"])
+    rows = decode.layer.staged_rows(W.DECODE.T)
+    out2 = decode.layer.forward(inp["hidden"], None, inp["token_mask"])
+    torch.cuda.synchronize()
+    assert np.array_equal(W.bits(rows), ref["rows"].reshape(W.DECODE.T, -1))
+    assert torch.equal(out.view(torch.int16), out2.view(torch.int16))
+
+
+@pytest.mark.parametrize("T", [1, 17, 100, 128, 129, 256])
+def test_decode_shapes_ragged_T(decode, T):
+    inp = decode.step_inputs(T=T, step=T)
+    out, gate, value = _run(decode, inp)
+    tokens = None if T <= 128 else np.unique(np.r_[0, 1, T // 2, T - 2, T - 1,
+                                                   np.random.default_rng(T).choice(T, 12)])
+    compare(decode, inp, out, decode.oracle(inp, tokens=tokens), tokens=tokens, gate=gate,
+            value=value)
+
+
+def test_decode_out_of_range_ids_read_zero_rows(decode):
+    T = 32
+    inp = decode.step_inputs(T=T, step=99)
+    ids = inp["hash_ids"].clone()
+    ids[3, 2] = W.DECODE.rows[2]
+    ids[9, 15] = -7
+    ids[31, 0] = 2 ** 31 - 1
+    inp["hash_ids"] = ids
+    out, gate, value = _run(decode, inp)
+    ref = decode.oracle(inp)
+    assert ref["n_bad"] == 3
+    compare(decode, inp, out, ref, gate=gate, value=value)
+    assert decode.layer.device_error() & ENGRAM_DEVERR_BAD_HASH_ID
 
 
 def test_prefill_config_sampled(decode):
@@ -214,3 +249,36 @@ def test_prefill_config_sampled(decode):
         assert case.layer.device_error() == 0
     finally:
         case.wl = W.DECODE
+
+
+def test_graph_capture_replays_bit_identically(decode):
+    """A captured forward replays to the same bits (the grid barrier resets itself)."""
+    inp = decode.step_inputs(T=64, step=21)
+    ref = decode.layer.forward(inp["hidden"], inp["hash_ids"], None)
+    torch.cuda.synchronize()
+    s = torch.cuda.Stream()
+    out = torch.empty_like(inp["hidden"])
+    with torch.cuda.stream(s):
+        decode.layer.forward(inp["hidden"], inp["hash_ids"], None, out=out, stream=s)
+    s.synchronize()
+    g = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(g, stream=s):
+        decode.layer.forward(inp["hidden"], inp["hash_ids"], None, out=out, stream=s)
+    for _ in range(3):
+        out.zero_()
+        g.replay()
+        torch.cuda.synchronize()
+        assert torch.equal(out.view(torch.int16), ref.view(torch.int16))
+    assert decode.layer.device_error() == 0
+
+
+def test_forward_host_buffers(tiny):
+    inp = tiny.step_inputs(T=24, step=22)
+    ref = tiny.oracle(inp)
+    hid = inp["hidden"].cpu().pin_memory()
+    ids = inp["hash_ids"].cpu().pin_memory()
+    mask = inp["token_mask"].cpu().pin_memory()
+    out = torch.empty_like(hid).pin_memory()
+    tiny.layer.forward_host(hid, ids, mask, out)
+    torch.cuda.synchronize()
+    compare(tiny, inp, out, ref)
