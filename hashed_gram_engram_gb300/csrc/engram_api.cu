@@ -3,13 +3,12 @@
 //
 // The sequence of engram_forward (Engram.forward, with the gather of
 // Engram.prepare_embeddings folded in when hash ids are given):
-//   gather   (plain launch: ordered after everything before it on the stream)
-//   wkv      (programmatic dependent launch: weight tiles stream in while the
-//             gather runs; token tiles wait for it)
-//   gate     (programmatic dependent launch: hidden is read while the wkv
-//             kernel drains)
-// T <= 256 takes the token-as-N (GEMV-shaped, stream-K) projection, larger T
-// the token-as-M tiles with the fused gate-partials epilogue.
+//   decode (T <= 256 and a column slice of <= 256 per CTA): one cooperative
+//     kernel does gather, projection, gate and residual (decode_fused.cu);
+//   prefill: gather (plain launch: ordered after everything before it on
+//     the stream), wkv (programmatic dependent launch: weight tiles stream in
+//     while the gather runs; token tiles wait for it), gate (programmatic
+//     dependent launch: hidden is read while the wkv kernel drains).
 #include <cstdio>
 #include <cstdlib>
 #include <cstring>
@@ -88,7 +87,7 @@ cudaError_t dalloc(T** p, size_t bytes, bool zero) {
 void free_handle(engram_handle* h) {
     if (h == nullptr) return;
     void* ptrs[] = {h->d_row_offset, h->d_rows,      h->ws.staged,   h->ws.staged_q,
-                    h->ws.staged_s,  h->ws.kvpart,   h->ws.partials, h->ws.value,
+                    h->ws.staged_s,  h->ws.partials, h->ws.value,
                     h->ws.gate,      h->ws.qk,       h->ws.wscale_rows, h->ws.err,
                     h->ws.wpack,     h->ws.fpart,    h->ws.fvalue,   h->ws.grid_bar,
                     h->ws.host_hidden, h->ws.host_ids, h->ws.host_mask};
@@ -233,9 +232,8 @@ int engram_create(const engram_config* cfg, const engram_weights* w, engram_t** 
 
     Workspace& ws = h->ws;
     ws.rows_alloc = (c.max_tokens + 255) / 256 * 256;
-    const int64_t tdec = c.max_tokens < kMaxDecodeT ? c.max_tokens : kMaxDecodeT;
+    const int64_t tdec = c.max_tokens < kMaxFusedT ? c.max_tokens : kMaxFusedT;
     ws.kv_tpitch = (tdec + 15) / 16 * 16;
-    const int64_t m_tiles = N / kBM;
     cudaError_t e = cudaSuccess;
     auto step = [&](cudaError_t r) {
         if (e == cudaSuccess) e = r;
@@ -243,12 +241,11 @@ int engram_create(const engram_config* cfg, const engram_weights* w, engram_t** 
     step(dalloc(&h->d_row_offset, C * sizeof(int64_t), false));
     step(dalloc(&h->d_rows, C * sizeof(int64_t), false));
     step(dalloc(&ws.staged, ws.rows_alloc * K * 2, true));
-    step(dalloc(&ws.kvpart, 2 * m_tiles * ws.kv_tpitch * 128 * sizeof(float), true));
-    if (c.max_tokens > kMaxDecodeT) {
-        step(dalloc(&ws.partials, ws.rows_alloc * c.hc_mult * (c.dim / kBNPrefill) * sizeof(float2),
-                    true));
-        step(dalloc(&ws.value, ws.rows_alloc * c.dim * 2, true));
-    }
+    // prefill path (also taken by small T when a decode column slice would
+    // be too wide)
+    step(dalloc(&ws.partials, ws.rows_alloc * c.hc_mult * (c.dim / kBNPrefill) * sizeof(float2),
+                true));
+    step(dalloc(&ws.value, ws.rows_alloc * c.dim * 2, true));
     step(dalloc(&ws.gate, ws.rows_alloc * c.hc_mult * sizeof(float), true));
     // fused decode kernel workspace, sized for the largest T it serves
     step(dalloc(&ws.wpack, N * K * 2, false));
@@ -271,8 +268,7 @@ int engram_create(const engram_config* cfg, const engram_weights* w, engram_t** 
         return e == cudaErrorMemoryAllocation ? ENGRAM_ERR_OOM : ENGRAM_ERR_CUDA;
     }
 
-    bool ok = make_map(&h->tm_w_m, h->wkv, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, K, N, kBM) &&
-              make_map(&h->tm_w_n, h->wkv, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, K, N, kBNPrefill) &&
+    bool ok = make_map(&h->tm_w_n, h->wkv, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, K, N, kBNPrefill) &&
               make_map(&h->tm_act_m, ws.staged, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, K,
                        ws.rows_alloc, kBM);
     for (int i = 0; i < 16 && ok; ++i)

@@ -11,11 +11,8 @@
 // once.  The per-token sums are reduced in a fixed order (shuffle tree,
 // then warps in index order) and the run is deterministic.
 //
-// Two sources for the key sums and the value:
-//   - kvpart: fp32 projection partials of the token-as-N wkv path, one or
-//     two stream-K slots per 128-row tile, summed here in slot order;
-//   - partials: per 256-column key tile (sum key^2, sum hidden*q*k*key)
-//     written by the token-as-M wkv epilogue, plus its bf16 value.
+// The key sums come as per-256-column-tile partials (sum key^2,
+// sum hidden*q*k*key) written by the wkv epilogue, the value as bf16.
 // Hidden is read before the programmatic-launch wait, so its HBM read
 // overlaps the tail of the wkv kernel.
 #include "internal.h"
@@ -37,39 +34,23 @@ struct GateArgs {
     float* gate_out;  // [T, H]
     int T, D;
     float eps, clamp, inv_d, inv_sqrt_d;
-    // kvpart source
-    const float* kvpart;
-    int m_tiles, tpitch, k_blocks, total, grid;
-    // partials source
     const float2* partials;
     const uint16_t* value;
     int J;
 };
 
-// CTA of the stream-K partition that owns iteration x.
-__device__ __forceinline__ int owner_cta(int64_t x, int64_t total, int64_t grid) {
-    return static_cast<int>(((x + 1) * grid - 1) / total);
-}
-
-__device__ __forceinline__ void add8(float (&acc)[8], const float* p) {
-    const float4 a = *reinterpret_cast<const float4*>(p);
-    const float4 b = *reinterpret_cast<const float4*>(p + 4);
-    acc[0] += a.x; acc[1] += a.y; acc[2] += a.z; acc[3] += a.w;
-    acc[4] += b.x; acc[5] += b.y; acc[6] += b.z; acc[7] += b.w;
-}
-
-template <int H, bool kFromKvpart>
+template <int H>
 __global__ void __launch_bounds__(kGateThreads) gate_residual_kernel(const GateArgs a) {
-    __shared__ float red[kGateThreads / 32][3 * H];
+    __shared__ float red[kGateThreads / 32][H];
     __shared__ float gate_s[H];
     const int t = blockIdx.x;
     const int tid = threadIdx.x;
     const int nchunk = a.D >> 3;
     const bool active = a.mask == nullptr || a.mask[t] != 0;
 
-    float shh[H], skk[H], shk[H];
+    float shh[H];
 #pragma unroll
-    for (int h = 0; h < H; ++h) shh[h] = skk[h] = shk[h] = 0.f;
+    for (int h = 0; h < H; ++h) shh[h] = 0.f;
     uint4 hid[kMaxChunks][H];
     float val[kMaxChunks][8];
 
@@ -94,49 +75,17 @@ __global__ void __launch_bounds__(kGateThreads) gate_residual_kernel(const GateA
 
     pdl_wait();  // the projection is complete and visible past this point
 
-    // Phase 2: key sums and the value.
+    // Phase 2: the value.
 #pragma unroll
     for (int ci = 0; ci < kMaxChunks; ++ci) {
         const int c = tid + ci * blockDim.x;
         if (c < nchunk) {
             const int d = c * 8;
-            if constexpr (kFromKvpart) {
+            const uint4 vb = ld_nc_v4(a.value + static_cast<int64_t>(t) * a.D + d);
+            const uint32_t w[4] = {vb.x, vb.y, vb.z, vb.w};
 #pragma unroll
-                for (int h = 0; h <= H; ++h) {
-                    const int64_t n = static_cast<int64_t>(h) * a.D + d;
-                    const int tile = static_cast<int>(n >> 7);
-                    const int r = static_cast<int>(n & 127);
-                    const int64_t it0 = static_cast<int64_t>(tile) * a.k_blocks;
-                    const bool split = owner_cta(it0, a.total, a.grid) !=
-                                       owner_cta(it0 + a.k_blocks - 1, a.total, a.grid);
-                    float v[8] = {0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f};
-                    add8(v, a.kvpart + ((static_cast<int64_t>(tile) * a.tpitch + t) << 7) + r);
-                    if (split)
-                        add8(v, a.kvpart +
-                                    ((static_cast<int64_t>(a.m_tiles + tile) * a.tpitch + t) << 7) + r);
-                    if (h < H) {
-                        const float4 q0 = __ldg(reinterpret_cast<const float4*>(a.qk + h * a.D + d));
-                        const float4 q1 = __ldg(reinterpret_cast<const float4*>(a.qk + h * a.D + d + 4));
-                        const float qk[8] = {q0.x, q0.y, q0.z, q0.w, q1.x, q1.y, q1.z, q1.w};
-                        const uint32_t w[4] = {hid[ci][h].x, hid[ci][h].y, hid[ci][h].z, hid[ci][h].w};
-#pragma unroll
-                        for (int i = 0; i < 8; ++i) {
-                            const float x = (i & 1) ? bf16hi(w[i >> 1]) : bf16lo(w[i >> 1]);
-                            skk[h] = fmaf(v[i], v[i], skk[h]);
-                            shk[h] = fmaf(x * qk[i], v[i], shk[h]);
-                        }
-                    } else {
-#pragma unroll
-                        for (int i = 0; i < 8; ++i) val[ci][i] = v[i];
-                    }
-                }
-            } else {
-                const uint4 vb = ld_nc_v4(a.value + static_cast<int64_t>(t) * a.D + d);
-                const uint32_t w[4] = {vb.x, vb.y, vb.z, vb.w};
-#pragma unroll
-                for (int i = 0; i < 8; ++i)
-                    val[ci][i] = (i & 1) ? bf16hi(w[i >> 1]) : bf16lo(w[i >> 1]);
-            }
+            for (int i = 0; i < 8; ++i)
+                val[ci][i] = (i & 1) ? bf16hi(w[i >> 1]) : bf16lo(w[i >> 1]);
         }
     }
 
@@ -145,38 +94,23 @@ __global__ void __launch_bounds__(kGateThreads) gate_residual_kernel(const GateA
 #pragma unroll
     for (int h = 0; h < H; ++h) {
 #pragma unroll
-        for (int off = 16; off > 0; off >>= 1) {
+        for (int off = 16; off > 0; off >>= 1)
             shh[h] += __shfl_xor_sync(0xFFFFFFFFu, shh[h], off);
-            skk[h] += __shfl_xor_sync(0xFFFFFFFFu, skk[h], off);
-            shk[h] += __shfl_xor_sync(0xFFFFFFFFu, shk[h], off);
-        }
     }
     if (lane == 0) {
 #pragma unroll
-        for (int h = 0; h < H; ++h) {
-            red[warp][3 * h + 0] = shh[h];
-            red[warp][3 * h + 1] = skk[h];
-            red[warp][3 * h + 2] = shk[h];
-        }
+        for (int h = 0; h < H; ++h) red[warp][h] = shh[h];
     }
     __syncthreads();
     if (tid < H) {
         const int h = tid;
         float s_hh = 0.f, s_kk = 0.f, s_hk = 0.f;
-        for (int w = 0; w < nwarps; ++w) {
-            s_hh += red[w][3 * h + 0];
-            s_kk += red[w][3 * h + 1];
-            s_hk += red[w][3 * h + 2];
-        }
-        if constexpr (!kFromKvpart) {
-            s_kk = 0.f;
-            s_hk = 0.f;
-            const float2* p = a.partials + (static_cast<int64_t>(t) * H + h) * a.J;
-            for (int j = 0; j < a.J; ++j) {
-                const float2 v = p[j];
-                s_kk += v.x;
-                s_hk += v.y;
-            }
+        for (int w = 0; w < nwarps; ++w) s_hh += red[w][h];
+        const float2* p = a.partials + (static_cast<int64_t>(t) * H + h) * a.J;
+        for (int j = 0; j < a.J; ++j) {
+            const float2 v = p[j];
+            s_kk += v.x;
+            s_hk += v.y;
         }
         const float hr = 1.0f / sqrtf(s_hh * a.inv_d + a.eps);
         const float kr = 1.0f / sqrtf(s_kk * a.inv_d + a.eps);
@@ -221,26 +155,11 @@ __global__ void qk_kernel(const uint16_t* q, const uint16_t* k, float* qk, int64
 }
 
 // fp32 value [T, D] of the last forward, for validation.
-__global__ void debug_value_kernel(const float* kvpart, int m_tiles, int tpitch, int k_blocks,
-                                   int total, int grid, const uint16_t* value, int H, int D,
-                                   int T, int path, float* out) {
+__global__ void debug_value_kernel(const uint16_t* value, int64_t n, float* out) {
     const int64_t i = static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x;
-    if (i >= static_cast<int64_t>(T) * D) return;
-    const int t = static_cast<int>(i / D), d = static_cast<int>(i % D);
-    if (path == 2) {
-        out[i] = __uint_as_float(static_cast<uint32_t>(value[i]) << 16);
-        return;
-    }
-    const int64_t n = static_cast<int64_t>(H) * D + d;
-    const int tile = static_cast<int>(n >> 7), r = static_cast<int>(n & 127);
-    const int64_t it0 = static_cast<int64_t>(tile) * k_blocks;
-    float v = kvpart[((static_cast<int64_t>(tile) * tpitch + t) << 7) + r];
-    if (owner_cta(it0, total, grid) != owner_cta(it0 + k_blocks - 1, total, grid))
-        v += kvpart[((static_cast<int64_t>(m_tiles + tile) * tpitch + t) << 7) + r];
-    out[i] = v;
+    if (i < n) out[i] = __uint_as_float(static_cast<uint32_t>(value[i]) << 16);
 }
 
-template <bool kFromKvpart>
 cudaError_t launch_gate(const engram_handle* h, const void* hidden, const int64_t* hs,
                         const uint8_t* mask, void* out, const int64_t* os, int64_t T,
                         cudaStream_t s, bool pdl) {
@@ -260,13 +179,6 @@ cudaError_t launch_gate(const engram_handle* h, const void* hidden, const int64_
     a.clamp = static_cast<float>(h->cfg.clamp);
     a.inv_d = 1.0f / static_cast<float>(a.D);
     a.inv_sqrt_d = 1.0f / sqrtf(static_cast<float>(a.D));
-    const DecodeSchedule sc = decode_schedule(h);
-    a.kvpart = h->ws.kvpart;
-    a.m_tiles = sc.m_tiles;
-    a.tpitch = static_cast<int>(h->ws.kv_tpitch);
-    a.k_blocks = sc.k_blocks;
-    a.total = sc.total;
-    a.grid = sc.grid;
     a.partials = h->ws.partials;
     a.value = h->ws.value;
     a.J = a.D / kBNPrefill;
@@ -285,26 +197,20 @@ cudaError_t launch_gate(const engram_handle* h, const void* hidden, const int64_
     cfg.attrs = attr;
     cfg.numAttrs = pdl ? 1 : 0;
     switch (h->cfg.hc_mult) {
-        case 1: return cudaLaunchKernelEx(&cfg, gate_residual_kernel<1, kFromKvpart>, a);
-        case 2: return cudaLaunchKernelEx(&cfg, gate_residual_kernel<2, kFromKvpart>, a);
-        case 3: return cudaLaunchKernelEx(&cfg, gate_residual_kernel<3, kFromKvpart>, a);
-        case 4: return cudaLaunchKernelEx(&cfg, gate_residual_kernel<4, kFromKvpart>, a);
+        case 1: return cudaLaunchKernelEx(&cfg, gate_residual_kernel<1>, a);
+        case 2: return cudaLaunchKernelEx(&cfg, gate_residual_kernel<2>, a);
+        case 3: return cudaLaunchKernelEx(&cfg, gate_residual_kernel<3>, a);
+        case 4: return cudaLaunchKernelEx(&cfg, gate_residual_kernel<4>, a);
         default: return cudaErrorInvalidValue;
     }
 }
 
 }  // namespace
 
-cudaError_t launch_gate_from_kvpart(const engram_handle* h, const void* hidden,
-                                    const int64_t* hs, const uint8_t* mask, void* out,
-                                    const int64_t* os, int64_t T, cudaStream_t s, bool pdl) {
-    return launch_gate<true>(h, hidden, hs, mask, out, os, T, s, pdl);
-}
-
 cudaError_t launch_gate_from_partials(const engram_handle* h, const void* hidden,
                                       const int64_t* hs, const uint8_t* mask, void* out,
                                       const int64_t* os, int64_t T, cudaStream_t s, bool pdl) {
-    return launch_gate<false>(h, hidden, hs, mask, out, os, T, s, pdl);
+    return launch_gate(h, hidden, hs, mask, out, os, T, s, pdl);
 }
 
 cudaError_t launch_qk(const engram_handle* h, cudaStream_t s) {
@@ -314,12 +220,9 @@ cudaError_t launch_qk(const engram_handle* h, cudaStream_t s) {
 }
 
 cudaError_t launch_debug_value(const engram_handle* h, float* value, int64_t T, cudaStream_t s) {
-    const DecodeSchedule sc = decode_schedule(h);
     const int64_t n = T * h->cfg.dim;
-    debug_value_kernel<<<static_cast<unsigned>((n + 255) / 256), 256, 0, s>>>(
-        h->ws.kvpart, sc.m_tiles, static_cast<int>(h->ws.kv_tpitch), sc.k_blocks, sc.total,
-        sc.grid, h->ws.value, static_cast<int>(h->cfg.hc_mult),
-        static_cast<int>(h->cfg.dim), static_cast<int>(T), h->last_path, value);
+    debug_value_kernel<<<static_cast<unsigned>((n + 255) / 256), 256, 0, s>>>(h->ws.value, n,
+                                                                              value);
     return cudaGetLastError();
 }
 

@@ -14,7 +14,6 @@ namespace engram {
 constexpr int kBM = 128;          // MMA M: rows of the TMEM accumulator
 constexpr int kBNPrefill = 256;   // kv columns per tile when tokens are the M side
 constexpr int kKBlockBytes = 128; // bytes of K per pipeline stage (one swizzle row)
-constexpr int kMaxDecodeT = 256;  // largest T served by the token-as-N (GEMV-shaped) path
 constexpr int kGemmSmemBytes = 192 * 1024 + 2048;  // > half an SM: one CTA per SM
 constexpr int kFusedSmemBytes = 225 * 1024;       // fused decode kernel
 constexpr int kMaxFusedT = 256;                   // largest T of the fused decode kernel
@@ -27,10 +26,9 @@ struct Workspace {
     // MXFP8 activations: e4m3 codes [rows_alloc, K], E8M0 scales [rows_alloc, K/32]
     uint8_t* staged_q = nullptr;
     uint8_t* staged_s = nullptr;
-    // token-as-N path: fp32 kv partial sums [2][m_tiles][kDecodeTPitch][128]
-    float* kvpart = nullptr;
+    // tokens padded to 16 up to the fused kernel's largest T
     int64_t kv_tpitch = 0;
-    // token-as-M path: fp32 (sum key^2, sum hidden*q*k*key) per 256-column key
+    // prefill path: fp32 (sum key^2, sum hidden*q*k*key) per 256-column key
     // tile [rows_alloc][H][D/256] and the bf16 value [rows_alloc][D]
     float2* partials = nullptr;
     uint16_t* value = nullptr;
@@ -59,13 +57,6 @@ struct FusedPlan {
     int Tn, mtiles, granules, k_blocks, grid, max_width;
 };
 
-struct DecodeSchedule {
-    int m_tiles;      // N / 128
-    int k_blocks;     // K / (64 bf16 | 128 e4m3)
-    int total;        // m_tiles * k_blocks
-    int grid;         // CTAs; every CTA gets >= k_blocks iterations
-};
-
 }  // namespace engram
 
 struct engram_handle {
@@ -82,7 +73,6 @@ struct engram_handle {
     int64_t* d_rows;
     engram::Workspace ws;
     // TMA descriptors
-    CUtensorMap tm_w_m;                 // wkv as the M-side operand (box 128 rows)
     CUtensorMap tm_w_n;                 // wkv as the N-side operand (box 256 rows)
     CUtensorMap tm_act_m;               // staged rows as the M-side operand (box 128 rows)
     CUtensorMap tm_act_n[16];           // staged rows as the N-side operand (box 16..256 rows)
@@ -91,7 +81,7 @@ struct engram_handle {
     // last lookup
     int64_t staged_T;
     int last_error;
-    int last_path;  // 0 = none, 1 = token-as-N, 2 = token-as-M
+    int last_path;  // 0 = none, 2 = prefill kernels, 3 = fused decode kernel
     // measurement hook
     int profiling;
     cudaEvent_t ev[4];
@@ -105,8 +95,6 @@ cudaError_t launch_gather(const engram_handle* h, const int32_t* ids, int64_t id
                           int64_t T, bool background, bool quantize, cudaStream_t s, bool pdl);
 
 // wkv_gemm.cu
-DecodeSchedule decode_schedule(const engram_handle* h);
-cudaError_t launch_wkv_tokens_n(const engram_handle* h, int64_t T, cudaStream_t s, bool pdl);
 cudaError_t launch_wkv_tokens_m(const engram_handle* h, const void* hidden, int64_t hs_t,
                                 int64_t hs_h, int64_t T, cudaStream_t s, bool pdl);
 cudaError_t gemm_setup_attributes();
@@ -124,9 +112,6 @@ cudaError_t launch_decode_fused(engram_handle* h, const void* hidden, const int6
                                 void* out, const int64_t* os, int64_t T, cudaStream_t s);
 
 // gate.cu
-cudaError_t launch_gate_from_kvpart(const engram_handle* h, const void* hidden,
-                                    const int64_t* hs, const uint8_t* mask, void* out,
-                                    const int64_t* os, int64_t T, cudaStream_t s, bool pdl);
 cudaError_t launch_gate_from_partials(const engram_handle* h, const void* hidden,
                                       const int64_t* hs, const uint8_t* mask, void* out,
                                       const int64_t* os, int64_t T, cudaStream_t s, bool pdl);

@@ -6,22 +6,13 @@
 // h = 0..H-1 in columns [h*D, (h+1)*D), the shared value in [H*D, N)
 // ("vllm.models.deepseek_v4_1.common.engram", Engram.__init__ and forward).
 //
-// Two schedules share one warp-specialised kernel body:
-//
-//  * token-as-M (T > 256, prefill): 128 tokens x 256 kv columns per tile,
-//    persistent CTAs stride over tiles.  The epilogue never writes keys:
-//    for a key tile it reduces (sum key^2, sum hidden*q*k*key) over the
-//    tile's 256 dims -- the split-dim gate partials of
-//    _engram_gate_partials_kernel ("vllm.models.deepseek_v41.amd.engram"),
-//    here per N tile instead of per TP rank -- and for a value tile it
-//    stores the value in bf16.
-//
-//  * token-as-N (T <= 256, decode): the GEMV-shaped case.  128 weight rows
-//    per tile on M, all tokens on N, and a stream-K split of the
-//    (tile, k-block) iterations so that every SM streams the same number
-//    of weight bytes.  Each tile is covered by at most two CTAs; each writes
-//    its fp32 partial accumulator into its own slot and the gate kernel
-//    adds the slots in a fixed order.
+// This is the prefill schedule (T > 256; decode runs in decode_fused.cu):
+// 128 tokens x 256 kv columns per tile, persistent CTAs stride over tiles.
+// The epilogue never writes keys: for a key tile it reduces
+// (sum key^2, sum hidden*q*k*key) over the tile's 256 dims -- the
+// split-dim gate partials of _engram_gate_partials_kernel
+// ("vllm.models.deepseek_v41.amd.engram"), here per N tile instead of per
+// TP rank -- and for a value tile it stores the value in bf16.
 //
 // Roles (192 threads): warp 0 = TMA producer, warp 1 = TMEM owner and MMA
 // issuer, warps 2-5 = epilogue (TMEM lane quarter = warp % 4).  Two TMEM
@@ -41,63 +32,36 @@ constexpr int kMaxStages = 8;
 constexpr int kStageBudget = 192 * 1024;
 constexpr uint32_t kTmemCols = 512;
 
-enum { kTokensM = 0, kTokensN = 1 };
-
 struct GemmArgs {
     int m_tiles, n_tiles, k_blocks, total, T;
-    int bn;       // MMA N (256 for token-as-M; padded T for token-as-N)
+    int bn;       // MMA N: kv columns per tile
     int stages;
     uint32_t a_bytes, b_bytes;
     uint32_t idesc;
     int D, H, J;
-    // token-as-M epilogue
     const uint16_t* hidden;
     int64_t hs_t, hs_h;
     const float* qk;
     float2* partials;
     uint16_t* value;
-    // token-as-N epilogue
-    float* kvpart;
-    int tpitch;
     unsigned* err;
 };
 
 struct Unit {
-    int m, n, kb0, kb1, slot;
+    int m, n;
 };
 
-// Iterates this CTA's work units in order.
-template <int MODE>
+// Tiles of this CTA in order: blockIdx.x, blockIdx.x + gridDim.x, ...
 struct Schedule {
     const GemmArgs& a;
     int64_t cur, end;
-    __device__ explicit Schedule(const GemmArgs& args) : a(args) {
-        if (MODE == kTokensM) {
-            cur = blockIdx.x;
-            end = static_cast<int64_t>(a.m_tiles) * a.n_tiles;
-        } else {
-            cur = static_cast<int64_t>(blockIdx.x) * a.total / gridDim.x;
-            end = static_cast<int64_t>(blockIdx.x + 1) * a.total / gridDim.x;
-        }
-    }
+    __device__ explicit Schedule(const GemmArgs& args)
+        : a(args), cur(blockIdx.x), end(static_cast<int64_t>(args.m_tiles) * args.n_tiles) {}
     __device__ bool next(Unit& u) {
         if (cur >= end) return false;
-        if (MODE == kTokensM) {
-            u.m = static_cast<int>(cur / a.n_tiles);
-            u.n = static_cast<int>(cur % a.n_tiles);
-            u.kb0 = 0;
-            u.kb1 = a.k_blocks;
-            u.slot = 0;
-            cur += gridDim.x;
-        } else {
-            u.m = static_cast<int>(cur / a.k_blocks);
-            u.n = 0;
-            u.kb0 = static_cast<int>(cur - static_cast<int64_t>(u.m) * a.k_blocks);
-            const int64_t left = end - cur;
-            u.kb1 = static_cast<int>(left < a.k_blocks - u.kb0 ? u.kb0 + left : a.k_blocks);
-            u.slot = u.kb0 == 0 ? 0 : 1;
-            cur += u.kb1 - u.kb0;
-        }
+        u.m = static_cast<int>(cur / a.n_tiles);
+        u.n = static_cast<int>(cur % a.n_tiles);
+        cur += gridDim.x;
         return true;
     }
 };
@@ -107,7 +71,6 @@ __device__ __forceinline__ void fail(int* abort_flag, unsigned* err) {
     atomicOr(err, ENGRAM_DEVERR_TIMEOUT);
 }
 
-template <int MODE>
 __global__ void __launch_bounds__(kThreads, 1)
     wkv_gemm_bf16_kernel(const __grid_constant__ CUtensorMap tmA,
                          const __grid_constant__ CUtensorMap tmB, const GemmArgs a) {
@@ -156,16 +119,14 @@ __global__ void __launch_bounds__(kThreads, 1)
         if (lane == 0) {
             // The weight operand is independent of the gather; only the
             // token operand waits for the preceding kernel.
-            const CUtensorMap* tm_w = MODE == kTokensN ? &tmA : &tmB;
-            const CUtensorMap* tm_x = MODE == kTokensN ? &tmB : &tmA;
-            const uint64_t pol_w = MODE == kTokensN ? policy_evict_first() : policy_evict_last();
-            Schedule<MODE> sch(a);
+            const uint64_t pol_w = policy_evict_last();
+            Schedule sch(a);
             Unit u;
             bool ok = true, waited = false;
             int pro_kb[kMaxStages], pro_row[kMaxStages], pro_s[kMaxStages];
             int npro = 0;
             while (ok && sch.next(u)) {
-                for (int kb = u.kb0; kb < u.kb1; ++kb) {
+                for (int kb = 0; kb < a.k_blocks; ++kb) {
                     if (!waited && issued == a.stages) {
                         // Every stage holds a weight tile: now wait for the
                         // gather and add the token tiles of those stages
@@ -173,9 +134,8 @@ __global__ void __launch_bounds__(kThreads, 1)
                         pdl_wait();
                         waited = true;
                         for (int i = 0; i < npro; ++i)
-                            tma_load_2d(smem + pro_s[i] * stage_bytes +
-                                            (MODE == kTokensN ? a.a_bytes : 0),
-                                        tm_x, &full[pro_s[i]], pro_kb[i] * 64, pro_row[i]);
+                            tma_load_2d(smem + pro_s[i] * stage_bytes, &tmA, &full[pro_s[i]],
+                                        pro_kb[i] * 64, pro_row[i]);
                     }
                     const int s = static_cast<int>(issued % a.stages);
                     const uint32_t par = static_cast<uint32_t>((issued / a.stages) & 1);
@@ -183,21 +143,18 @@ __global__ void __launch_bounds__(kThreads, 1)
                         ok = false;
                         break;
                     }
-                    uint8_t* sa = smem + s * stage_bytes;
-                    uint8_t* sb = sa + a.a_bytes;
-                    uint8_t* sw = MODE == kTokensN ? sa : sb;
-                    uint8_t* sx = MODE == kTokensN ? sb : sa;
-                    const int w_row = MODE == kTokensN ? u.m * kBM : u.n * a.bn;
-                    const int x_row = MODE == kTokensN ? 0 : u.m * kBM;
+                    uint8_t* sx = smem + s * stage_bytes;
+                    uint8_t* sw = sx + a.a_bytes;
+                    const int x_row = u.m * kBM;
                     mbar_arrive_expect_tx(&full[s], stage_bytes);
-                    tma_load_2d_hint(sw, tm_w, &full[s], kb * 64, w_row, pol_w);
+                    tma_load_2d_hint(sw, &tmB, &full[s], kb * 64, u.n * a.bn, pol_w);
                     if (!waited) {
                         pro_kb[npro] = kb;
                         pro_row[npro] = x_row;
                         pro_s[npro] = s;
                         ++npro;
                     } else {
-                        tma_load_2d(sx, tm_x, &full[s], kb * 64, x_row);
+                        tma_load_2d(sx, &tmA, &full[s], kb * 64, x_row);
                     }
                     ++issued;
                 }
@@ -205,15 +162,15 @@ __global__ void __launch_bounds__(kThreads, 1)
             if (!waited) {
                 pdl_wait();
                 for (int i = 0; i < npro; ++i)
-                    tma_load_2d(smem + pro_s[i] * stage_bytes + (MODE == kTokensN ? a.a_bytes : 0),
-                                tm_x, &full[pro_s[i]], pro_kb[i] * 64, pro_row[i]);
+                    tma_load_2d(smem + pro_s[i] * stage_bytes, &tmA, &full[pro_s[i]],
+                                pro_kb[i] * 64, pro_row[i]);
             }
             pdl_launch_dependents();
             if (!ok) fail(abort_flag, a.err);
         }
     } else if (warp == 1) {
         if (lane == 0) {
-            Schedule<MODE> sch(a);
+            Schedule sch(a);
             Unit u;
             bool ok = true;
             int64_t it = 0;
@@ -227,7 +184,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                 }
                 tc_fence_after();
                 const uint32_t d_tmem = tmem_base + static_cast<uint32_t>(acc * a.bn);
-                for (int kb = u.kb0; kb < u.kb1; ++kb) {
+                for (int kb = 0; kb < a.k_blocks; ++kb) {
                     const int s = static_cast<int>(it % a.stages);
                     const uint32_t par = static_cast<uint32_t>((it / a.stages) & 1);
                     if (!mbar_wait(&full[s], par, abort_v)) {
@@ -241,7 +198,7 @@ __global__ void __launch_bounds__(kThreads, 1)
 #pragma unroll
                     for (int k = 0; k < 4; ++k)  // 4 x K16 per 64-element block
                         mma_bf16_ss(d_tmem, adesc + 2 * k, bdesc + 2 * k, a.idesc,
-                                    (kb > u.kb0 || k > 0) ? 1u : 0u);
+                                    (kb > 0 || k > 0) ? 1u : 0u);
                     mma_commit(&empty[s]);
                     ++it;
                 }
@@ -255,7 +212,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         // Epilogue: TMEM lane quarter q = warp % 4, one accumulator row per thread.
         const int q = warp & 3;
         const int row = q * 32 + lane;
-        Schedule<MODE> sch(a);
+        Schedule sch(a);
         Unit u;
         bool ok = true;
         int nu = 0;
@@ -264,7 +221,7 @@ __global__ void __launch_bounds__(kThreads, 1)
             const uint32_t apar = static_cast<uint32_t>((nu >> 1) & 1);
             const uint32_t taddr =
                 tmem_base + (static_cast<uint32_t>(q * 32) << 16) + static_cast<uint32_t>(acc * a.bn);
-            if constexpr (MODE == kTokensM) {
+            {
                 const int t = u.m * kBM + row;
                 const bool live = t < a.T;
                 const int col0 = u.n * kBNPrefill;
@@ -342,25 +299,6 @@ __global__ void __launch_bounds__(kThreads, 1)
                     __syncwarp();
                     if (lane == 0) mbar_arrive(&tempty[acc]);
                 }
-            } else {
-                if (!mbar_wait(&tfull[acc], apar, abort_v)) {
-                    ok = false;
-                    break;
-                }
-                tc_fence_after();
-                float* dst = a.kvpart +
-                             (static_cast<int64_t>(u.slot * a.m_tiles + u.m) * a.tpitch << 7) + row;
-                for (int c = 0; c < a.bn; c += 16) {
-                    uint32_t r[16];
-                    tmem_ld16(taddr + c, r);
-                    tmem_ld_wait();
-#pragma unroll
-                    for (int j = 0; j < 16; ++j)
-                        if (c + j < a.T) dst[static_cast<int64_t>(c + j) << 7] = __uint_as_float(r[j]);
-                }
-                tc_fence_before();
-                __syncwarp();
-                if (lane == 0) mbar_arrive(&tempty[acc]);
             }
             ++nu;
         }
@@ -390,24 +328,9 @@ __global__ void __launch_bounds__(kThreads, 1)
 
 }  // namespace
 
-DecodeSchedule decode_schedule(const engram_handle* h) {
-    DecodeSchedule s;
-    s.m_tiles = static_cast<int>(h->N / kBM);
-    s.k_blocks = static_cast<int>(h->K * (h->cfg.wkv_format == ENGRAM_WKV_MXFP8 ? 1 : 2) /
-                                  kKBlockBytes);
-    s.total = s.m_tiles * s.k_blocks;
-    // At least k_blocks iterations per CTA keeps every tile within two CTAs.
-    s.grid = h->num_sms < s.m_tiles ? h->num_sms : s.m_tiles;
-    return s;
-}
-
 cudaError_t gemm_setup_attributes() {
-    cudaError_t e = cudaFuncSetAttribute(wkv_gemm_bf16_kernel<kTokensM>,
-                                         cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                         kGemmSmemBytes);
-    if (e != cudaSuccess) return e;
-    return cudaFuncSetAttribute(wkv_gemm_bf16_kernel<kTokensN>,
-                                cudaFuncAttributeMaxDynamicSharedMemorySize, kGemmSmemBytes);
+    return cudaFuncSetAttribute(wkv_gemm_bf16_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                kGemmSmemBytes);
 }
 
 static cudaError_t launch(const void* fn, int grid, const CUtensorMap& tmA, const CUtensorMap& tmB,
@@ -425,30 +348,6 @@ static cudaError_t launch(const void* fn, int grid, const CUtensorMap& tmA, cons
     void* args[] = {const_cast<CUtensorMap*>(&tmA), const_cast<CUtensorMap*>(&tmB),
                     const_cast<GemmArgs*>(&a)};
     return cudaLaunchKernelExC(&cfg, fn, args);
-}
-
-cudaError_t launch_wkv_tokens_n(const engram_handle* h, int64_t T, cudaStream_t s, bool pdl) {
-    const DecodeSchedule sc = decode_schedule(h);
-    GemmArgs a = {};
-    a.m_tiles = sc.m_tiles;
-    a.n_tiles = 1;
-    a.k_blocks = sc.k_blocks;
-    a.total = sc.total;
-    a.T = static_cast<int>(T);
-    a.bn = static_cast<int>((T + 15) / 16 * 16);
-    a.a_bytes = kBM * kKBlockBytes;
-    a.b_bytes = static_cast<uint32_t>(a.bn) * kKBlockBytes;
-    a.stages = static_cast<int>(kStageBudget / (a.a_bytes + a.b_bytes));
-    if (a.stages > kMaxStages) a.stages = kMaxStages;
-    a.idesc = idesc_bf16(kBM, a.bn);
-    a.D = static_cast<int>(h->cfg.dim);
-    a.H = static_cast<int>(h->cfg.hc_mult);
-    a.J = a.D / kBNPrefill;
-    a.kvpart = h->ws.kvpart;
-    a.tpitch = static_cast<int>(h->ws.kv_tpitch);
-    a.err = h->ws.err;
-    return launch(reinterpret_cast<const void*>(wkv_gemm_bf16_kernel<kTokensN>), sc.grid,
-                  h->tm_w_m, h->tm_act_n[a.bn / 16 - 1], a, s, pdl);
 }
 
 cudaError_t launch_wkv_tokens_m(const engram_handle* h, const void* hidden, int64_t hs_t,
@@ -476,7 +375,7 @@ cudaError_t launch_wkv_tokens_m(const engram_handle* h, const void* hidden, int6
     a.value = h->ws.value;
     a.err = h->ws.err;
     const int grid = a.total < h->num_sms ? a.total : h->num_sms;
-    return launch(reinterpret_cast<const void*>(wkv_gemm_bf16_kernel<kTokensM>), grid, h->tm_act_m,
+    return launch(reinterpret_cast<const void*>(wkv_gemm_bf16_kernel), grid, h->tm_act_m,
                   h->tm_w_n, a, s, pdl);
 }
 
