@@ -19,7 +19,8 @@ import numpy as np
 from . import _lib
 from ._lib import (EngramError, engram_config, engram_create, engram_debug_intermediates,
                    engram_debug_staged_rows, engram_destroy, engram_device_error,
-                   engram_forward, engram_forward_host, engram_last_error, engram_layout,
+                   engram_forward, engram_forward_host, engram_gate_noalloc,
+                   engram_last_error, engram_layout,
                    engram_lookup, engram_profile_enable, engram_profile_read,
                    engram_weights, ENGRAM_WKV_BF16, ENGRAM_WKV_MXFP8,
                    ENGRAM_TABLE_DEVICE, ENGRAM_TABLE_HOST_PINNED, ENGRAM_DEVERR_BAD_HASH_ID,
@@ -28,6 +29,7 @@ from ._lib import (EngramError, engram_config, engram_create, engram_debug_inter
 __all__ = [
     "Engram", "EngramError", "engram_config", "engram_weights", "engram_create",
     "engram_destroy", "engram_lookup", "engram_forward", "engram_forward_host",
+    "engram_gate_noalloc",
     "engram_last_error", "engram_device_error", "engram_layout", "engram_debug_intermediates",
     "engram_debug_staged_rows", "engram_profile_enable", "engram_profile_read",
     "ENGRAM_WKV_BF16", "ENGRAM_WKV_MXFP8", "ENGRAM_TABLE_DEVICE",

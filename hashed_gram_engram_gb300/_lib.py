@@ -24,10 +24,12 @@ ENGRAM_ERR_OOM = -4
 ENGRAM_ERR_NO_UVA = -5
 ENGRAM_ERR_DEVICE = -6
 ENGRAM_ERR_CUDA = -7
+ENGRAM_ERR_SCRATCH_LIMIT = -8
 ERROR_NAMES = {
     -1: "INVALID_ARG", -2: "UNSUPPORTED", -3: "T_EXCEEDS_MAX", -4: "OOM", -5: "NO_UVA",
-    -6: "DEVICE", -7: "CUDA",
+    -6: "DEVICE", -7: "CUDA", -8: "SCRATCH_LIMIT",
 }
+ENGRAM_NOALLOC_MAX_PARTIALS = 131072
 ENGRAM_DEVERR_BAD_HASH_ID = 1
 ENGRAM_DEVERR_TIMEOUT = 2
 ENGRAM_WKV_BF16 = 0
@@ -40,7 +42,7 @@ EXPORTED = (
     "engram_create", "engram_destroy", "engram_lookup", "engram_forward",
     "engram_forward_host", "engram_last_error", "engram_device_error", "engram_layout",
     "engram_debug_intermediates", "engram_debug_staged_rows", "engram_profile_enable",
-    "engram_profile_read",
+    "engram_profile_read", "engram_gate_noalloc",
 )
 
 
@@ -99,6 +101,8 @@ def load(path: str | None = None):
             "engram_debug_staged_rows": [vp, vp, i64, vp],
             "engram_profile_enable": [vp, ctypes.c_int],
             "engram_profile_read": [vp, vp],
+            "engram_gate_noalloc": [vp, vp, vp, i64, vp, vp, vp, vp, vp, i64, i64, i64,
+                                    ctypes.c_double, ctypes.c_double, vp],
         }
         for name, args in sig.items():
             f = getattr(L, name)
@@ -135,7 +139,7 @@ def _check(rc, what):
 
 
 def _i64x3(v):
-    return (ctypes.c_int64 * 3)(*[int(x) for x in v])
+    return None if v is None else (ctypes.c_int64 * 3)(*[int(x) for x in v])
 
 
 def engram_create(cfg: engram_config, weights: engram_weights) -> int:
@@ -208,3 +212,13 @@ def engram_profile_read(h):
     ms = (ctypes.c_float * 3)()
     _check(load().engram_profile_read(h, ms), "engram_profile_read")
     return list(ms)
+
+
+def engram_gate_noalloc(hidden, hidden_strides, kv, kv_row_stride, q_weight, k_weight,
+                        token_mask, out, out_strides, T, H, D, eps=1e-6, clamp=1e-6,
+                        stream=None):
+    """Gate + masked residual over a caller-computed kv, no handle, no allocation."""
+    return _check(load().engram_gate_noalloc(
+        _ptr(hidden), _i64x3(hidden_strides), _ptr(kv), int(kv_row_stride), _ptr(q_weight),
+        _ptr(k_weight), _ptr(token_mask), _ptr(out), _i64x3(out_strides), int(T), int(H),
+        int(D), float(eps), float(clamp), _stream(stream)), "engram_gate_noalloc")

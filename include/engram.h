@@ -45,6 +45,8 @@ extern "C" {
 #define ENGRAM_ERR_NO_UVA (-5)        /* host-offloaded table needs unified addressing */
 #define ENGRAM_ERR_DEVICE (-6)        /* the device reported an error (see below) */
 #define ENGRAM_ERR_CUDA (-7)          /* a CUDA runtime call or launch failed */
+#define ENGRAM_ERR_SCRATCH_LIMIT (-8) /* engram_gate_noalloc: the call needs more than
+                                         ENGRAM_NOALLOC_MAX_PARTIALS scratch slots */
 
 /* Bits of the sticky device error word returned by engram_device_error(). */
 #define ENGRAM_DEVERR_BAD_HASH_ID 1u  /* an id outside [0, rows[c]): its row was zeroed */
@@ -174,6 +176,42 @@ int engram_debug_intermediates(engram_t* h, float* gate, float* value, int64_t T
 /* Validation hook: copy the staged rows [T, K] bf16 (the gather output) of
  * the last lookup into `rows` (device), on `stream`. */
 int engram_debug_staged_rows(engram_t* h, void* rows, int64_t T, cudaStream_t stream);
+
+/* Gate and masked residual only, over a projection computed by the caller,
+ * with NO handle and NO device memory allocation on any call.
+ *
+ * The documented Engram layer has no such entry point: it is here for
+ * callers that cannot allocate device memory while they serve -- engines
+ * that run the wkv projection with their own GEMM and have already given
+ * nearly all of HBM to their own pools (a cudaMalloc there can fail, and
+ * cudaMalloc/cudaFree synchronise the device).
+ *
+ * Arithmetic: as engram_forward, split into partial sums per 256-dim slice
+ * that are added in slice order (the partials/finish split of the gate in
+ * "vllm.models.deepseek_v41.amd.engram", slices in place of ranks).
+ *   hidden, out: device bf16 [T, H, D], strides as for engram_forward
+ *       (in place allowed, any other overlap with hidden or kv is INVALID_ARG).
+ *   kv: device bf16 [T, (H+1)*D] with row stride kv_row_stride >= (H+1)*D
+ *       elements (a multiple of 8): keys of copy h in columns [h*D, (h+1)*D),
+ *       the shared value in [H*D, (H+1)*D).
+ *   q_weight, k_weight: device bf16 [H, D] contiguous.
+ *   token_mask: device bytes [T] (0 = False) or NULL.
+ *   1 <= H <= 4; D a multiple of 256, at most 8192.
+ * Scratch: one fixed array of ENGRAM_NOALLOC_MAX_PARTIALS 16-byte slots per
+ * device, inside the library's device image; a call uses T * H * (D / 256)
+ * slots and returns ENGRAM_ERR_SCRATCH_LIMIT, launching nothing, if that is
+ * more.  No slot needs to start at zero (a call writes every slot it reads).
+ * Calls on one device share the array: two calls that can run at the same
+ * time (unordered streams, concurrent host threads) corrupt each other's
+ * results, so order them.  The first call on each device (T = 0 does only
+ * this) looks up the array's address and may load the library's device code
+ * there; make it before capturing a stream.  Uses the current device. */
+#define ENGRAM_NOALLOC_MAX_PARTIALS 131072
+int engram_gate_noalloc(const void* hidden, const int64_t hidden_strides[3], const void* kv,
+                        int64_t kv_row_stride, const void* q_weight, const void* k_weight,
+                        const uint8_t* token_mask, void* out, const int64_t out_strides[3],
+                        int64_t T, int64_t H, int64_t D, double eps, double clamp,
+                        cudaStream_t stream);
 
 /* Measurement hook: with enable != 0, later engram_forward calls record a
  * CUDA event before and after each of their kernels on the call's stream
