@@ -46,6 +46,9 @@ def parse():
     p.add_argument("--no-cpu-baseline", action="store_true")
     p.add_argument("--cpu-seconds", type=float, default=10.0)
     p.add_argument("--layers", type=int, default=6)
+    p.add_argument("--case", choices=["decode", "prefill"], default=None,
+                   help="only run W + K plain forwards of one layer of that workload (the "
+                        "small case profilers capture) and print a one-line summary")
     return p.parse_args()
 
 
@@ -183,6 +186,35 @@ def run_reference(args):
     print(json.dumps(line), flush=True)
 
 
+def source_digest(names):
+    """sha256 (12 hex) of kernel sources, to tell whether a stored ncu
+    figure still describes the kernel that runs."""
+    import hashlib
+    h = hashlib.sha256()
+    for n in names:
+        with open(os.path.join(ROOT, "hashed_gram_engram_gb300", "csrc", n), "rb") as f:
+            h.update(f.read())
+    return h.hexdigest()[:12]
+
+
+DECODE_SOURCES = ("decode_fused.cu", "ptx.cuh", "internal.h")
+DECODE_PROFILE = os.path.join(ROOT, "profiles", "decode_fused_kernel_decode_T64.md")
+
+
+def stored_traffic(path, sources):
+    """DRAM bytes per launch from a committed ncu summary, or None when the
+    summary is missing or was taken on other kernel sources."""
+    try:
+        for line in open(path):
+            if line.startswith("traffic:"):
+                kv = dict(x.split("=", 1) for x in line.split()[1:])
+                if kv.get("source_sha256") == source_digest(sources):
+                    return int(kv["dram_bytes_per_launch"])
+    except (OSError, ValueError, KeyError):
+        pass
+    return None
+
+
 def make_layer(W, Engram, wl, device_index, max_tokens, layer_seed):
     import dataclasses
     wl_l = dataclasses.replace(wl, seed=wl.seed + 101 * layer_seed)
@@ -196,10 +228,37 @@ def make_layer(W, Engram, wl, device_index, max_tokens, layer_seed):
     return wl_l, layer, table, wts
 
 
+def run_case(args):
+    """W + K plain forwards of one layer: the small case for ncu captures."""
+    import torch
+    import __graft_entry__ as g
+    import workloads as W
+    from hashed_gram_engram_gb300 import Engram
+    g.build()
+    torch.cuda.set_device(0)
+    stream = torch.cuda.Stream()
+    torch.cuda.set_stream(stream)
+    wl = W.DECODE if args.case == "decode" else W.PREFILL
+    wl_l, layer, _, _ = make_layer(W, Engram, wl, 0, wl.T, 0)
+    st = W.make_step_inputs(wl_l, "cuda")
+    out = torch.empty_like(st["hidden"])
+    n = max(3, args.warmup) + args.steps
+    for _ in range(n):
+        layer.forward(st["hidden"], st["hash_ids"], st["token_mask"], out=out, stream=stream)
+    torch.cuda.synchronize()
+    err = layer.device_error()
+    layer.close()
+    print(json.dumps({"case": args.case, "T": wl.T, "forwards": n, "device_error": err}),
+          flush=True)
+    return 0 if err == 0 else 1
+
+
 def main():
     args = parse()
     if args.impl == "reference":
         return run_reference(args)
+    if args.case is not None:
+        return run_case(args)
 
     import numpy as np
     import torch
@@ -284,13 +343,7 @@ def main():
                   + wl.T * wl.n_hash_cols * 4 + 2 * wl.hc_mult * wl.dim * 2)
     # one kernel per step: its average duration is the step time (launch gaps included)
     achieved = step_bytes / (ms_step * 1e-3) / 1e9
-    traffic = None
-    tr_path = os.path.join(ROOT, "profiles", "traffic.json")
-    if os.path.exists(tr_path):
-        try:
-            traffic = json.load(open(tr_path)).get("decode_fused")
-        except Exception:
-            traffic = None
+    traffic = stored_traffic(DECODE_PROFILE, DECODE_SOURCES)
 
     # single-step latency with L2 flushed before the step (cold code, page
     # tables and weights), and the kernel's own event time
@@ -420,4 +473,4 @@ def main():
 
 
 if __name__ == "__main__":
-    main()
+    sys.exit(main())
