@@ -18,7 +18,7 @@ import numpy as np
 
 from . import _lib
 from ._lib import (EngramError, engram_config, engram_create, engram_debug_intermediates,
-                   engram_debug_staged_rows, engram_destroy, engram_device_error,
+                   engram_debug_staged_mx, engram_debug_staged_rows, engram_destroy, engram_device_error,
                    engram_forward, engram_forward_host, engram_gate_noalloc,
                    engram_last_error, engram_layout,
                    engram_lookup, engram_profile_enable, engram_profile_read,
@@ -29,7 +29,7 @@ from ._lib import (EngramError, engram_config, engram_create, engram_debug_inter
 __all__ = [
     "Engram", "EngramError", "engram_config", "engram_weights", "engram_create",
     "engram_destroy", "engram_lookup", "engram_forward", "engram_forward_host",
-    "engram_gate_noalloc",
+    "engram_gate_noalloc", "engram_debug_staged_mx",
     "engram_last_error", "engram_device_error", "engram_layout", "engram_debug_intermediates",
     "engram_debug_staged_rows", "engram_profile_enable", "engram_profile_read",
     "ENGRAM_WKV_BF16", "ENGRAM_WKV_MXFP8", "ENGRAM_TABLE_DEVICE",
@@ -139,3 +139,13 @@ class Engram:
                            device=torch.device("cuda", self.device))
         engram_debug_staged_rows(self.handle, rows, T, stream)
         return rows
+
+    def staged_mx(self, T, stream=None):
+        """e4m3 codes [T, K] and E8M0 scales [T, K/32] of the staged rows (MXFP8)."""
+        import torch
+        dev = torch.device("cuda", self.device)
+        K = self.n_hash_cols * self.head_dim
+        codes = torch.empty((T, K), dtype=torch.uint8, device=dev)
+        scales = torch.empty((T, K // 32), dtype=torch.uint8, device=dev)
+        engram_debug_staged_mx(self.handle, codes, scales, T, stream)
+        return codes, scales

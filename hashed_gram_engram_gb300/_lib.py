@@ -42,7 +42,7 @@ EXPORTED = (
     "engram_create", "engram_destroy", "engram_lookup", "engram_forward",
     "engram_forward_host", "engram_last_error", "engram_device_error", "engram_layout",
     "engram_debug_intermediates", "engram_debug_staged_rows", "engram_profile_enable",
-    "engram_profile_read", "engram_gate_noalloc",
+    "engram_profile_read", "engram_gate_noalloc", "engram_debug_staged_mx",
 )
 
 
@@ -99,6 +99,7 @@ def load(path: str | None = None):
             "engram_layout": [i64, i32, i32, i32, vp, vp],
             "engram_debug_intermediates": [vp, vp, vp, i64, vp],
             "engram_debug_staged_rows": [vp, vp, i64, vp],
+            "engram_debug_staged_mx": [vp, vp, vp, i64, vp],
             "engram_profile_enable": [vp, ctypes.c_int],
             "engram_profile_read": [vp, vp],
             "engram_gate_noalloc": [vp, vp, vp, i64, vp, vp, vp, vp, vp, i64, i64, i64,
@@ -202,6 +203,11 @@ def engram_debug_intermediates(h, gate, value, T, stream=None):
 def engram_debug_staged_rows(h, rows, T, stream=None):
     return _check(load().engram_debug_staged_rows(h, _ptr(rows), int(T), _stream(stream)),
                   "engram_debug_staged_rows")
+
+
+def engram_debug_staged_mx(h, codes, scales, T, stream=None):
+    return _check(load().engram_debug_staged_mx(h, _ptr(codes), _ptr(scales), int(T),
+                                                _stream(stream)), "engram_debug_staged_mx")
 
 
 def engram_profile_enable(h, enable=1):

@@ -33,10 +33,21 @@
 //            value rows and partial records arrive by bulk copy; the hidden
 //            rows were bulk-copied while the weights streamed.
 //
+// MXFP8 wkv (T <= 128): the gather also quantises the rows (e4m3 codes and
+// E8M0 scales per 32 k), the MMAs are tcgen05 kind::mxf8f6f4 with
+// block_scale, and the scale factors sit in TMEM next to the accumulator.
+// A CTA's weight slice starts on any 16-column boundary, so instead of
+// copying scale atoms the epilogue warps write the scale words into TMEM
+// themselves (tcgen05.st): the weights' at kernel start, the tokens' after
+// the gather.  Scale cell layout (tcgen05 block scaling, scale_vec::1X):
+// the scale of A row r for k-block b sits in lane r, column sfa + r / 32,
+// byte b; that of B row n in lane n % 32, column sfb + n / 32, byte b.
+//
 // Both grid barriers reset themselves, so a captured launch replays.
 #include <cuda_bf16.h>
 
 #include "internal.h"
+#include "mxfp8.cuh"
 #include "ptx.cuh"
 
 namespace engram {
@@ -52,6 +63,7 @@ constexpr int kHidRows = 4;     // finish rows whose hidden is prefetched to sha
 struct FusedArgs {
     int T, Tn, D, H, C, E, N, K;
     int mtiles, granules, k_blocks, stages;
+    int kb128;  // K / 128: MXFP8 scale words per row
     uint32_t w_stage_bytes, x_bytes;  // per stage: weight slice region, token bytes
     int gather;                       // gather the hash rows in this launch
     const int32_t* ids;
@@ -59,14 +71,17 @@ struct FusedArgs {
     const int64_t* row_offset;
     const int64_t* rows;
     const uint16_t* table;
-    uint16_t* staged;  // [rows_alloc][K] bf16
+    uint16_t* staged;    // [rows_alloc][K] bf16
+    uint8_t* staged_q;   // MXFP8: e4m3 codes [rows_alloc][K]
+    uint8_t* staged_s;   // MXFP8: scale atoms of the codes
+    const uint8_t* wscale;  // MXFP8: E8M0 [N/32][K/32]
     const uint16_t* hidden;
     int64_t hs_t, hs_h;
     uint16_t* out;
     int64_t os_t, os_h;
     const uint8_t* mask;
     const float* qk;        // [H, D]
-    const uint16_t* wpack;  // [K/64][N][64] bf16, 8-row groups 128-byte swizzled
+    const uint8_t* wpack;   // [K bytes/128][N][128 bytes], 8-row groups 128-byte swizzled
     float* part;            // [tpitch][grid][kPartFloats]
     float* value;           // [tpitch][D]
     unsigned* bar;          // two grid barriers: {arrivals, generation} each
@@ -109,8 +124,10 @@ __device__ __forceinline__ bool grid_barrier(unsigned* bar, unsigned G) {
     return true;
 }
 
+template <bool kMx>
 __global__ void __launch_bounds__(kThreads, 1)
     decode_fused_kernel(const __grid_constant__ CUtensorMap tm_x, const FusedArgs a) {
+    constexpr int kKElems = kMx ? 128 : 64;  // k per 128-byte block
     extern __shared__ uint8_t smem_raw[];
     uint8_t* smem = reinterpret_cast<uint8_t*>(
         (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~static_cast<uintptr_t>(1023));
@@ -123,7 +140,8 @@ __global__ void __launch_bounds__(kThreads, 1)
     uint64_t* hbar = tfull + 1;
     uint64_t* fbar = hbar + 1;
     uint64_t* drain = fbar + 1;
-    uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(drain + 1);
+    uint64_t* scbar = drain + 1;  // MXFP8: every scale word is in TMEM
+    uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(scbar + 1);
     int* abort_flag = reinterpret_cast<int*>(tmem_slot + 1);
     float* gate_s = reinterpret_cast<float*>(abort_flag + 2);  // [kWarps] gates of a row batch
     const volatile int* abort_v = abort_flag;
@@ -147,6 +165,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         mbar_init(hbar, 1);
         mbar_init(fbar, 1);
         mbar_init(drain, 1);
+        mbar_init(scbar, 128);
         *abort_flag = 0;
         fence_barrier_init();
         tma_prefetch_desc(&tm_x);
@@ -161,6 +180,9 @@ __global__ void __launch_bounds__(kThreads, 1)
     __syncthreads();
     tc_fence_after();
     const uint32_t tmem_base = *tmem_slot;
+    // MXFP8 scale cells, 8 columns per k-block each (every region 8-aligned)
+    const uint32_t tm_sfa = tmem_base + kMaxFusedSlice;                     // tokens
+    const uint32_t tm_sfb = tm_sfa + 8u * static_cast<uint32_t>(a.kb128);  // weights
 
     int issued = 0;
     if (warp == 0) {
@@ -187,7 +209,7 @@ __global__ void __launch_bounds__(kThreads, 1)
             auto issue_x = [&](int s, int kb) {
                 uint8_t* sx = smem + s * stage_bytes + a.w_stage_bytes;
                 for (int m = 0; m < a.mtiles; ++m)
-                    tma_load_2d(sx + m * 16384, &tm_x, &full[s], kb * 64, m * 128);
+                    tma_load_2d(sx + m * 16384, &tm_x, &full[s], kb * kKElems, m * 128);
             };
             auto await_rows = [&]() -> bool {
                 const uint64_t t0 = globaltimer_ns();
@@ -216,7 +238,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                 }
                 mbar_arrive_expect_tx(&full[s], w_bytes + a.x_bytes);
                 bulk_load_hint(smem + s * stage_bytes,
-                               a.wpack + (static_cast<int64_t>(kb) * a.N + c_lo) * 64, w_bytes,
+                               a.wpack + (static_cast<int64_t>(kb) * a.N + c_lo) * 128, w_bytes,
                                &full[s], pol_w);
                 if (have_rows) issue_x(s, kb);
                 ++issued;
@@ -228,7 +250,11 @@ __global__ void __launch_bounds__(kThreads, 1)
         if (lane == 0) {
             const uint32_t idesc = idesc_bf16(128, width);
             bool ok = true;
-            for (int kb = 0; kb < a.k_blocks; ++kb) {
+            if constexpr (kMx) {
+                ok = mbar_wait(scbar, 0, abort_v);
+                tc_fence_after();
+            }
+            for (int kb = 0; kb < a.k_blocks && ok; ++kb) {
                 const int s = kb % a.stages;
                 if (!mbar_wait(&full[s], static_cast<uint32_t>((kb / a.stages) & 1), abort_v)) {
                     ok = false;
@@ -237,12 +263,23 @@ __global__ void __launch_bounds__(kThreads, 1)
                 tc_fence_after();
                 const uint32_t sw = smem_addr(smem + s * stage_bytes);
                 const uint64_t wdesc = smem_desc_sw128(sw);
+                if constexpr (kMx) {
+                    const uint64_t xdesc = smem_desc_sw128(sw + a.w_stage_bytes);
 #pragma unroll
-                for (int k = 0; k < 4; ++k)
-                    for (int m = 0; m < a.mtiles; ++m)
-                        mma_bf16_ss(tmem_base + static_cast<uint32_t>(m * kMaxFusedSlice),
-                                    smem_desc_sw128(sw + a.w_stage_bytes + m * 16384) + 2 * k,
-                                    wdesc + 2 * k, idesc, (kb > 0 || k > 0) ? 1u : 0u);
+                    for (int k = 0; k < 4; ++k)  // 4 x K32, scale byte k of each cell
+                        mma_mxf8_ss(tmem_base, xdesc + 2 * k, wdesc + 2 * k,
+                                    idesc_mxf8(128, width, k, k),
+                                    tm_sfa + 8u * static_cast<uint32_t>(kb),
+                                    tm_sfb + 8u * static_cast<uint32_t>(kb),
+                                    (kb > 0 || k > 0) ? 1u : 0u);
+                } else {
+#pragma unroll
+                    for (int k = 0; k < 4; ++k)
+                        for (int m = 0; m < a.mtiles; ++m)
+                            mma_bf16_ss(tmem_base + static_cast<uint32_t>(m * kMaxFusedSlice),
+                                        smem_desc_sw128(sw + a.w_stage_bytes + m * 16384) + 2 * k,
+                                        wdesc + 2 * k, idesc, (kb > 0 || k > 0) ? 1u : 0u);
+                }
                 mma_commit(&empty[s]);
             }
             if (ok) mma_commit(tfull);
@@ -250,9 +287,65 @@ __global__ void __launch_bounds__(kThreads, 1)
         }
     } else {
         const int etid = tid - 64;  // 0..127
+        const int q = warp & 3;     // TMEM lane quarter of this warp
+        const uint32_t lane_base = static_cast<uint32_t>(q * 32) << 16;
+        if constexpr (kMx) {
+            // weight scales of the slice: B row n (slice column n) in lane
+            // n % 32, column tm_sfb + 8 kb + n / 32; every lane quarter gets
+            // a copy
+            for (int kb = 0; kb < a.kb128; ++kb) {
+                uint32_t w[8];
+#pragma unroll
+                for (int jc = 0; jc < 8; ++jc) {
+                    const int n = jc * 32 + lane;
+                    w[jc] = n < width ? __ldg(reinterpret_cast<const uint32_t*>(
+                                            a.wscale + ((c_lo + n) >> 5) * (a.K >> 5) + kb * 4))
+                                      : 0x7F7F7F7Fu;
+                }
+                const uint32_t col = tm_sfb + lane_base + 8u * static_cast<uint32_t>(kb);
+                tmem_st4(col, w[0], w[1], w[2], w[3]);
+                tmem_st4(col + 4, w[4], w[5], w[6], w[7]);
+            }
+        }
         // This CTA's share of the hash rows -> the staged-rows buffer
         // (ParallelEngramEmbedding.lookup), then the first grid barrier.
-        if (a.gather) {
+        if (a.gather && kMx) {
+            // one thread per 32-k block of a hash row: the bf16 row, its
+            // e4m3 codes and its scale
+            const int bpr = a.E >> 5;
+            const int nrows = a.T * a.C;
+            const int r0 = static_cast<int>(static_cast<int64_t>(blockIdx.x) * nrows / G);
+            const int r1 = static_cast<int>(static_cast<int64_t>(blockIdx.x + 1) * nrows / G);
+            bool bad = false;
+            for (int i = etid; i < (r1 - r0) * bpr; i += 128) {
+                const int rr = r0 + i / bpr, b = i - (i / bpr) * bpr;
+                const int t = rr / a.C, c = rr - t * a.C;
+                const int64_t id = a.ids[t * a.ids_stride + c];
+                uint4 v[4];
+                if (id >= 0 && id < __ldg(a.rows + c)) {
+                    const uint16_t* src = a.table + (__ldg(a.row_offset + c) + id) * a.E + b * 32;
+#pragma unroll
+                    for (int j = 0; j < 4; ++j) v[j] = ld_stream_v4(src + j * 8);
+                } else {
+#pragma unroll
+                    for (int j = 0; j < 4; ++j) v[j] = make_uint4(0u, 0u, 0u, 0u);
+                    bad = true;
+                }
+                const int64_t k0 = static_cast<int64_t>(rr) * a.E + b * 32;  // = t*K + c*E + 32b
+#pragma unroll
+                for (int j = 0; j < 4; ++j) st_v4(a.staged + k0 + j * 8, v[j]);
+                uint4 cq[2];
+                const uint32_t sb = mx_quantize32(v, cq);
+                st_v4(a.staged_q + k0, cq[0]);
+                st_v4(a.staged_q + k0 + 16, cq[1]);
+                a.staged_s[sf_atom_offset(t, (c * a.E + b * 32) >> 5, a.kb128)] =
+                    static_cast<uint8_t>(sb);
+            }
+            if (bad) atomicOr(a.err, ENGRAM_DEVERR_BAD_HASH_ID);
+            __threadfence();
+            named_barrier_sync(1, 128);
+            if (etid == 0 && !grid_barrier(a.bar, static_cast<unsigned>(G))) fail(abort_flag, a.err);
+        } else if (a.gather) {
             const int cpr = a.E >> 3;  // 16-byte chunks per row
             const int nrows = a.T * a.C;
             const int r0 = static_cast<int>(static_cast<int64_t>(blockIdx.x) * nrows / G);
@@ -279,11 +372,23 @@ __global__ void __launch_bounds__(kThreads, 1)
             const int n = c_lo + c;
             qk_s[c] = n < a.H * a.D ? __ldg(a.qk + n) : 0.f;
         }
-        named_barrier_sync(1, 128);  // qk_s complete
+        named_barrier_sync(1, 128);  // qk_s complete; the gather barrier has passed
+        if constexpr (kMx) {
+            // token scales: A row r = token t in lane t, column
+            // tm_sfa + 8 kb + t / 32 (written to all four columns)
+            const int t = q * 32 + lane;
+            for (int kb = 0; kb < a.kb128; ++kb) {
+                const uint32_t w = __ldcg(reinterpret_cast<const unsigned*>(
+                    a.staged_s + sf_atom_offset(t, 4 * kb, a.kb128)));
+                tmem_st4(tm_sfa + lane_base + 8u * static_cast<uint32_t>(kb), w, w, w, w);
+            }
+            tmem_st_wait();
+            tc_fence_before();
+            mbar_arrive(scbar);
+        }
 
         // Epilogue: thread = one token of an accumulator (TMEM lane quarter
         // = warp % 4), columns = the slice.
-        const int q = warp & 3;
         const int h0 = c_lo / a.D;  // the slice covers hc copies h0 and possibly h0 + 1
         bool go = true;
         for (int m = 0; m < a.mtiles && go; ++m) {
@@ -491,18 +596,20 @@ __global__ void __launch_bounds__(kThreads, 1)
     }
 }
 
-// wkv [N, K] bf16 -> [K/64][N][64]: for every 64-wide k-block the rows are
-// consecutive 128-byte lines, each 8-row group 128-byte swizzled (16-byte
-// chunk j of row n at position j ^ (n % 8)), so any 8-aligned row range
-// of a k-block is a ready shared-memory operand image.
-__global__ void pack_w_kernel(const uint16_t* w, uint16_t* wp, int64_t N, int64_t K) {
+// wkv [N, row_bytes] -> [row_bytes/128][N][128 bytes]: for every 128-byte
+// k-block (64 bf16 or 128 e4m3) the rows are consecutive 128-byte lines,
+// each 8-row group 128-byte swizzled (16-byte chunk j of row n at position
+// j ^ (n % 8)), so any 8-aligned row range of a k-block is a ready
+// shared-memory operand image.
+__global__ void pack_w_kernel(const uint8_t* w, uint8_t* wp, int64_t N, int64_t row_bytes) {
     const int64_t i = static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x;  // 16-B chunk
-    if (i >= N * K / 8) return;
-    const int64_t n = i / (K / 8);
-    const int64_t k8 = i - n * (K / 8);
-    const int64_t kb = k8 / 8, j = k8 % 8;
-    const int64_t dst = (kb * N + n) * 64 + ((j ^ (n & 7)) * 8);
-    *reinterpret_cast<uint4*>(wp + dst) = *reinterpret_cast<const uint4*>(w + i * 8);
+    const int64_t cpr = row_bytes / 16;
+    if (i >= N * cpr) return;
+    const int64_t n = i / cpr;
+    const int64_t c = i - n * cpr;
+    const int64_t kb = c / 8, j = c % 8;
+    const int64_t dst = (kb * N + n) * 128 + ((j ^ (n & 7)) * 16);
+    *reinterpret_cast<uint4*>(wp + dst) = *reinterpret_cast<const uint4*>(w + i * 16);
 }
 
 }  // namespace
@@ -512,7 +619,7 @@ FusedPlan fused_plan(const engram_handle* h, int64_t T) {
     p.Tn = static_cast<int>((T + 15) / 16 * 16);
     p.mtiles = static_cast<int>((T + 127) / 128);
     p.granules = static_cast<int>(h->N / 16);
-    p.k_blocks = static_cast<int>(h->K / 64);
+    p.k_blocks = static_cast<int>(h->K * (h->cfg.wkv_format == ENGRAM_WKV_MXFP8 ? 1 : 2) / 128);
     p.grid = h->num_sms < p.granules ? h->num_sms : p.granules;
     p.max_width = (p.granules + p.grid - 1) / p.grid * 16;  // widest slice
     return p;
@@ -520,19 +627,29 @@ FusedPlan fused_plan(const engram_handle* h, int64_t T) {
 
 bool fused_supported(const engram_handle* h, int64_t T) {
     const FusedPlan p = fused_plan(h, T);
+    if (h->cfg.wkv_format == ENGRAM_WKV_MXFP8) {
+        // one accumulator of 256 columns plus 8 + 8 scale columns per k-block
+        return T >= 1 && T <= kMaxFusedTMx && p.max_width <= kMaxFusedSlice &&
+               h->cfg.head_dim % 32 == 0 && kMaxFusedSlice + 16 * (h->K / 128) <= 512;
+    }
     return T >= 1 && T <= kMaxFusedT && p.max_width <= kMaxFusedSlice && h->cfg.head_dim % 8 == 0;
 }
 
 cudaError_t pack_weights(const engram_handle* h, cudaStream_t s) {
-    const int64_t nchunks = h->N * h->K / 8;
+    const int64_t row_bytes = h->K * (h->cfg.wkv_format == ENGRAM_WKV_MXFP8 ? 1 : 2);
+    const int64_t nchunks = h->N * row_bytes / 16;
     pack_w_kernel<<<static_cast<unsigned>((nchunks + 255) / 256), 256, 0, s>>>(
-        static_cast<const uint16_t*>(h->wkv), h->ws.wpack, h->N, h->K);
+        static_cast<const uint8_t*>(h->wkv), h->ws.wpack, h->N, row_bytes);
     return cudaGetLastError();
 }
 
 cudaError_t fused_setup_attributes() {
-    return cudaFuncSetAttribute(decode_fused_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                kFusedSmemBytes);
+    cudaError_t e = cudaFuncSetAttribute(decode_fused_kernel<false>,
+                                         cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                         kFusedSmemBytes);
+    if (e != cudaSuccess) return e;
+    return cudaFuncSetAttribute(decode_fused_kernel<true>,
+                                cudaFuncAttributeMaxDynamicSharedMemorySize, kFusedSmemBytes);
 }
 
 cudaError_t launch_fused_debug_value(const engram_handle* h, float* value, int64_t T,
@@ -557,6 +674,7 @@ cudaError_t launch_decode_fused(engram_handle* h, const void* hidden, const int6
     a.mtiles = p.mtiles;
     a.granules = p.granules;
     a.k_blocks = p.k_blocks;
+    a.kb128 = static_cast<int>(h->K / 128);
     // token rows per stage: one box of Tn rows, or two of 128 rows
     a.x_bytes = static_cast<uint32_t>(p.mtiles == 1 ? p.Tn * 128 : 2 * 16384);
     a.gather = ids != nullptr ? 1 : 0;
@@ -566,6 +684,9 @@ cudaError_t launch_decode_fused(engram_handle* h, const void* hidden, const int6
     a.rows = h->d_rows;
     a.table = h->table;
     a.staged = h->ws.staged;
+    a.staged_q = h->ws.staged_q;
+    a.staged_s = h->ws.staged_s;
+    a.wscale = h->wkv_scale;
     a.hidden = static_cast<const uint16_t*>(hidden);
     a.hs_t = hs[0];
     a.hs_h = hs[1];
@@ -626,7 +747,12 @@ cudaError_t launch_decode_fused(engram_handle* h, const void* hidden, const int6
     cfg.numAttrs = 1;
     const CUtensorMap* tmx = p.mtiles == 1 ? &h->tm_act_n[p.Tn / 16 - 1] : &h->tm_act_m;
     void* args[] = {const_cast<CUtensorMap*>(tmx), &a};
-    return cudaLaunchKernelExC(&cfg, reinterpret_cast<const void*>(decode_fused_kernel), args);
+    const bool mx = h->cfg.wkv_format == ENGRAM_WKV_MXFP8;
+    return cudaLaunchKernelExC(
+        &cfg,
+        mx ? reinterpret_cast<const void*>(decode_fused_kernel<true>)
+           : reinterpret_cast<const void*>(decode_fused_kernel<false>),
+        args);
 }
 
 }  // namespace engram

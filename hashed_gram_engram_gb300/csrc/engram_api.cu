@@ -88,7 +88,7 @@ void free_handle(engram_handle* h) {
     if (h == nullptr) return;
     void* ptrs[] = {h->d_row_offset, h->d_rows,      h->ws.staged,   h->ws.staged_q,
                     h->ws.staged_s,  h->ws.partials, h->ws.value,
-                    h->ws.gate,      h->ws.qk,       h->ws.wscale_rows, h->ws.err,
+                    h->ws.gate,      h->ws.qk,       h->ws.wsf_atoms, h->ws.err,
                     h->ws.wpack,     h->ws.fpart,    h->ws.fvalue,   h->ws.grid_bar,
                     h->ws.host_hidden, h->ws.host_ids, h->ws.host_mask};
     for (void* p : ptrs)
@@ -188,10 +188,11 @@ int engram_create(const engram_config* cfg, const engram_weights* w, engram_t** 
     const int64_t K = C * c.head_dim;
     const int64_t N = c.dim * (c.hc_mult + 1);
     // What the kernels are built for.
+    const bool mx = c.wkv_format == ENGRAM_WKV_MXFP8;
     if (c.dim % kBNPrefill != 0 || c.dim > 8192 || c.hc_mult > 4 || c.head_dim % 8 != 0 ||
-        32 % (c.head_dim / 8) != 0 || K % 128 != 0 || K > (1 << 20) ||
-        (c.wkv_format == ENGRAM_WKV_MXFP8) || !aligned16(w->table) || !aligned16(w->wkv) ||
-        c.max_tokens > (1 << 24))
+        32 % (c.head_dim / 8) != 0 || K % 128 != 0 || K > (1 << 20) || !aligned16(w->table) ||
+        !aligned16(w->wkv) || c.max_tokens > (1 << 24) ||
+        (mx && (c.head_dim % 32 != 0 || !aligned16(w->wkv_scale))))
         return ENGRAM_ERR_UNSUPPORTED;
     for (int64_t i = 0; i < C; ++i)
         if (w->rows[i] <= 0 || w->row_offset[i] < 0) return ENGRAM_ERR_INVALID_ARG;
@@ -241,14 +242,21 @@ int engram_create(const engram_config* cfg, const engram_weights* w, engram_t** 
     step(dalloc(&h->d_row_offset, C * sizeof(int64_t), false));
     step(dalloc(&h->d_rows, C * sizeof(int64_t), false));
     step(dalloc(&ws.staged, ws.rows_alloc * K * 2, true));
+    if (mx) {
+        step(dalloc(&ws.staged_q, ws.rows_alloc * K, true));
+        step(dalloc(&ws.staged_s, ws.rows_alloc * K / 32, true));
+        step(dalloc(&ws.wsf_atoms, N * K / 32, false));
+    }
     // prefill path (also taken by small T when a decode column slice would
     // be too wide)
-    step(dalloc(&ws.partials, ws.rows_alloc * c.hc_mult * (c.dim / kBNPrefill) * sizeof(float2),
+    step(dalloc(&ws.partials,
+                ws.rows_alloc * c.hc_mult * (c.dim / (mx ? kBNPrefillMx : kBNPrefill)) *
+                    sizeof(float2),
                 true));
     step(dalloc(&ws.value, ws.rows_alloc * c.dim * 2, true));
     step(dalloc(&ws.gate, ws.rows_alloc * c.hc_mult * sizeof(float), true));
     // fused decode kernel workspace, sized for the largest T it serves
-    step(dalloc(&ws.wpack, N * K * 2, false));
+    step(dalloc(&ws.wpack, N * K * (mx ? 1 : 2), false));
     step(dalloc(&ws.fpart, ws.kv_tpitch * sms * 8 * sizeof(float), true));
     step(dalloc(&ws.fvalue, ws.kv_tpitch * c.dim * sizeof(float), true));
     step(dalloc(&ws.grid_bar, 4 * sizeof(unsigned), true));
@@ -260,6 +268,7 @@ int engram_create(const engram_config* cfg, const engram_weights* w, engram_t** 
         e = cudaMemcpy(h->d_rows, w->rows, C * sizeof(int64_t), cudaMemcpyHostToDevice);
     if (e == cudaSuccess) e = launch_qk(h, 0);
     if (e == cudaSuccess) e = pack_weights(h, 0);
+    if (e == cudaSuccess && mx) e = pack_scale_atoms(h, 0);
     if (e == cudaSuccess) e = gemm_setup_attributes();
     if (e == cudaSuccess) e = fused_setup_attributes();
     if (e == cudaSuccess) e = cudaDeviceSynchronize();
@@ -268,12 +277,15 @@ int engram_create(const engram_config* cfg, const engram_weights* w, engram_t** 
         return e == cudaErrorMemoryAllocation ? ENGRAM_ERR_OOM : ENGRAM_ERR_CUDA;
     }
 
-    bool ok = make_map(&h->tm_w_n, h->wkv, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, K, N, kBNPrefill) &&
-              make_map(&h->tm_act_m, ws.staged, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, K,
-                       ws.rows_alloc, kBM);
+    // token operand: bf16 rows, or their e4m3 codes for MXFP8
+    const CUtensorMapDataType dt =
+        mx ? CU_TENSOR_MAP_DATA_TYPE_UINT8 : CU_TENSOR_MAP_DATA_TYPE_BFLOAT16;
+    const int elem = mx ? 1 : 2;
+    const void* act = mx ? static_cast<const void*>(ws.staged_q) : static_cast<const void*>(ws.staged);
+    bool ok = make_map(&h->tm_w_n, h->wkv, dt, elem, K, N, mx ? kBNPrefillMx : kBNPrefill) &&
+              make_map(&h->tm_act_m, act, dt, elem, K, ws.rows_alloc, kBM);
     for (int i = 0; i < 16 && ok; ++i)
-        ok = make_map(&h->tm_act_n[i], ws.staged, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, K,
-                      ws.rows_alloc, 16 * (i + 1));
+        ok = make_map(&h->tm_act_n[i], act, dt, elem, K, ws.rows_alloc, 16 * (i + 1));
     if (!ok) {
         free_handle(h);
         return ENGRAM_ERR_CUDA;
@@ -301,8 +313,8 @@ int engram_lookup(engram_t* h, const int32_t* hash_ids, int64_t ids_row_stride, 
     }
     if (hash_ids == nullptr || ids_row_stride < h->C) return set_err(h, ENGRAM_ERR_INVALID_ARG);
     DeviceGuard guard(h->cfg.device);
-    cudaError_t e = launch_gather(h, hash_ids, ids_row_stride, T, background != 0, false, stream,
-                                  false);
+    cudaError_t e = launch_gather(h, hash_ids, ids_row_stride, T, background != 0,
+                                  h->cfg.wkv_format == ENGRAM_WKV_MXFP8, stream, false);
     if (e != cudaSuccess) return cuda_err(h, e);
     h->staged_T = T;
     return set_err(h, ENGRAM_OK);
@@ -354,7 +366,8 @@ int engram_forward(engram_t* h, const void* hidden, const int64_t hidden_strides
     h->ev_ran[1] = h->ev_ran[2] = true;
     mark(0);
     if (hash_ids != nullptr) {
-        e = launch_gather(h, hash_ids, ids_row_stride, T, false, false, stream, false);
+        e = launch_gather(h, hash_ids, ids_row_stride, T, false,
+                          h->cfg.wkv_format == ENGRAM_WKV_MXFP8, stream, false);
         if (e != cudaSuccess) return cuda_err(h, e);
         h->staged_T = T;
         first = false;
@@ -461,6 +474,19 @@ int engram_debug_staged_rows(engram_t* h, void* rows, int64_t T, cudaStream_t st
     DeviceGuard guard(h->cfg.device);
     cudaError_t e = cudaMemcpyAsync(rows, h->ws.staged, T * h->K * 2, cudaMemcpyDeviceToDevice,
                                     stream);
+    return e == cudaSuccess ? ENGRAM_OK : ENGRAM_ERR_CUDA;
+}
+
+int engram_debug_staged_mx(engram_t* h, uint8_t* codes, uint8_t* scales, int64_t T,
+                           cudaStream_t stream) {
+    if (h == nullptr || T < 0 || T > h->cfg.max_tokens) return ENGRAM_ERR_INVALID_ARG;
+    if (h->cfg.wkv_format != ENGRAM_WKV_MXFP8) return ENGRAM_ERR_INVALID_ARG;
+    if (T == 0) return ENGRAM_OK;
+    DeviceGuard guard(h->cfg.device);
+    cudaError_t e = cudaSuccess;
+    if (codes != nullptr)
+        e = cudaMemcpyAsync(codes, h->ws.staged_q, T * h->K, cudaMemcpyDeviceToDevice, stream);
+    if (e == cudaSuccess && scales != nullptr) e = launch_unpack_scales(h, scales, T, stream);
     return e == cudaSuccess ? ENGRAM_OK : ENGRAM_ERR_CUDA;
 }
 

@@ -11,7 +11,7 @@
 // once.  The per-token sums are reduced in a fixed order (shuffle tree,
 // then warps in index order) and the run is deterministic.
 //
-// The key sums come as per-256-column-tile partials (sum key^2,
+// The key sums come as per-key-tile partials (sum key^2,
 // sum hidden*q*k*key) written by the wkv epilogue, the value as bf16.
 // Hidden is read before the programmatic-launch wait, so its HBM read
 // overlaps the tail of the wkv kernel.
@@ -181,7 +181,7 @@ cudaError_t launch_gate(const engram_handle* h, const void* hidden, const int64_
     a.inv_sqrt_d = 1.0f / sqrtf(static_cast<float>(a.D));
     a.partials = h->ws.partials;
     a.value = h->ws.value;
-    a.J = a.D / kBNPrefill;
+    a.J = a.D / prefill_bn(h);
 
     int threads = a.D / 8;
     if (threads > kGateThreads) threads = kGateThreads;

@@ -9,10 +9,10 @@
 // background lookups) follows the page's note that the table dwarfs TLB
 // reach.  Optionally the same pass emits the MXFP8 form of the rows: e4m3
 // codes and one E8M0 scale per 32 consecutive k (smallest power of two that
-// keeps the block maximum within 448; round-to-nearest-even, saturating).
-#include <cuda_fp8.h>
-
+// keeps the block maximum within 448; round-to-nearest-even, saturating),
+// the scales stored as the tcgen05 scale-factor atoms the GEMM copies.
 #include "internal.h"
+#include "mxfp8.cuh"
 #include "ptx.cuh"
 
 namespace engram {
@@ -28,23 +28,12 @@ struct GatherArgs {
     const int32_t* ids;
     int64_t ids_stride;
     uint16_t* staged;  // [T, K]
-    uint8_t* codes;    // [T, K]     (quantize only)
-    uint8_t* scales;   // [T, K/32]  (quantize only)
+    uint8_t* codes;    // [T, K]                     (quantize only)
+    uint8_t* scales;   // atoms [T/128][K/128][512]  (quantize only)
     int64_t n_chunks;  // T * C * cpr
     int C, E, K, cpr_shift;
     unsigned* err;
 };
-
-// Exponent e of the E8M0 scale: the smallest integer with
-// amax <= 448 * 2^e (amax = 0 -> 0), clamped to [-127, 127].  448 = 1.75*2^8,
-// so for amax = 1.m * 2^u the answer is u - 8, plus one when 1.m > 1.75.
-__device__ __forceinline__ int mx_scale_exponent(float amax) {
-    const uint32_t b = __float_as_uint(amax);
-    const int ef = static_cast<int>((b >> 23) & 0xFFu);
-    if (ef == 0) return (b & 0x7FFFFFu) ? -127 : 0;
-    int e = ef - 127 - 8 + (((b & 0x7FFFFFu) > 0x600000u) ? 1 : 0);
-    return e < -127 ? -127 : (e > 127 ? 127 : e);
-}
 
 template <bool kQuant>
 __global__ void __launch_bounds__(kGatherThreads) gather_rows_kernel(const GatherArgs a) {
@@ -95,19 +84,13 @@ __global__ void __launch_bounds__(kGatherThreads) gather_rows_kernel(const Gathe
                 const int e = mx_scale_exponent(__uint_as_float(m << 16));
                 const float inv = __uint_as_float(static_cast<uint32_t>(127 - e) << 23);
                 if (dst[u] >= 0) {
-                    uint32_t packed[2];
-#pragma unroll
-                    for (int i = 0; i < 2; ++i) {
-                        const __nv_fp8x2_storage_t lo = __nv_cvt_float2_to_fp8x2(
-                            make_float2(bf16lo(w[2 * i]) * inv, bf16hi(w[2 * i]) * inv),
-                            __NV_SATFINITE, __NV_E4M3);
-                        const __nv_fp8x2_storage_t hi = __nv_cvt_float2_to_fp8x2(
-                            make_float2(bf16lo(w[2 * i + 1]) * inv, bf16hi(w[2 * i + 1]) * inv),
-                            __NV_SATFINITE, __NV_E4M3);
-                        packed[i] = static_cast<uint32_t>(lo) | (static_cast<uint32_t>(hi) << 16);
+                    *reinterpret_cast<uint2*>(a.codes + dst[u]) =
+                        make_uint2(mx_codes4(w[0], w[1], inv), mx_codes4(w[2], w[3], inv));
+                    if ((lane & 3) == 0) {
+                        const int64_t t = dst[u] / a.K;
+                        a.scales[sf_atom_offset(t, (dst[u] - t * a.K) >> 5, a.K >> 7)] =
+                            static_cast<uint8_t>(e + 127);
                     }
-                    *reinterpret_cast<uint2*>(a.codes + dst[u]) = make_uint2(packed[0], packed[1]);
-                    if ((lane & 3) == 0) a.scales[dst[u] >> 5] = static_cast<uint8_t>(e + 127);
                 }
             }
         }

@@ -12,38 +12,51 @@ namespace engram {
 
 // wkv GEMM tiling.
 constexpr int kBM = 128;          // MMA M: rows of the TMEM accumulator
-constexpr int kBNPrefill = 256;   // kv columns per tile when tokens are the M side
+constexpr int kBNPrefill = 256;   // kv columns per prefill tile, bf16 wkv
+constexpr int kBNPrefillMx = 128; // kv columns per prefill tile, MXFP8 wkv (TMEM holds the
+                                  // two accumulators plus a scale-factor slot per stage)
 constexpr int kKBlockBytes = 128; // bytes of K per pipeline stage (one swizzle row)
 constexpr int kGemmSmemBytes = 192 * 1024 + 2048;  // > half an SM: one CTA per SM
 constexpr int kFusedSmemBytes = 225 * 1024;       // fused decode kernel
 constexpr int kMaxFusedT = 256;                   // largest T of the fused decode kernel
 constexpr int kMaxFusedSlice = 256;               // widest column slice of one CTA (MMA N)
+constexpr int kMaxFusedTMx = 128;                 // largest T of the fused kernel, MXFP8 wkv
+
+// MXFP8 scale-factor atoms: the E8M0 scales of 128 rows x 128 k (4 scales
+// per row) as the 512-byte image tcgen05.cp .32x128b.warpx4 copies into
+// TMEM: byte 16*i + 4*j + b holds the scale of row 32*j + i, k-block b.
+// A [rows, K] operand's atoms are stored [rows/128][K/128][512].
+__host__ __device__ inline int64_t sf_atom_offset(int64_t row, int64_t k32, int64_t kblocks128) {
+    return ((row >> 7) * kblocks128 + (k32 >> 2)) * 512 + (row & 31) * 16 +
+           ((row >> 5) & 3) * 4 + (k32 & 3);
+}
 
 struct Workspace {
     // staged gather output (Engram.staged_rows): bf16 [rows_alloc, K]
     uint16_t* staged = nullptr;
     int64_t rows_alloc = 0;  // max_tokens rounded up to 256
-    // MXFP8 activations: e4m3 codes [rows_alloc, K], E8M0 scales [rows_alloc, K/32]
+    // MXFP8 activations: e4m3 codes [rows_alloc, K] and their E8M0 scales
+    // as atoms [rows_alloc/128][K/128][512]
     uint8_t* staged_q = nullptr;
     uint8_t* staged_s = nullptr;
     // tokens padded to 16 up to the fused kernel's largest T
     int64_t kv_tpitch = 0;
-    // prefill path: fp32 (sum key^2, sum hidden*q*k*key) per 256-column key
-    // tile [rows_alloc][H][D/256] and the bf16 value [rows_alloc][D]
+    // prefill path: fp32 (sum key^2, sum hidden*q*k*key) per key tile
+    // [rows_alloc][H][D/BN] and the bf16 value [rows_alloc][D]
     float2* partials = nullptr;
     uint16_t* value = nullptr;
     // fp32 gate of the last forward [rows_alloc][H]
     float* gate = nullptr;
     // fp32 q*k [H, D]
     float* qk = nullptr;
-    // MXFP8 weight scales expanded per row: [N][K/32] bytes
-    uint8_t* wscale_rows = nullptr;
+    // MXFP8 weight scales as atoms [N/128][K/128][512] (prefill B operand)
+    uint8_t* wsf_atoms = nullptr;
     // sticky device error word
     unsigned* err = nullptr;
-    // fused decode kernel: wkv packed k-block-major as swizzled shared-memory
-    // images, per-(token, CTA) gate partial sums, the fp32 value, the
-    // grid-barrier counter
-    uint16_t* wpack = nullptr;
+    // fused decode kernel: wkv packed k-block-major (128 bytes of k per row
+    // and block) as swizzled shared-memory images, per-(token, CTA) gate
+    // partial sums, the fp32 value, the grid-barrier counter
+    uint8_t* wpack = nullptr;
     float* fpart = nullptr;     // [kv_tpitch][num_sms][8]
     float* fvalue = nullptr;    // [kv_tpitch][D]
     unsigned* grid_bar = nullptr;  // two {count, generation} grid barriers of the fused kernel
@@ -73,11 +86,9 @@ struct engram_handle {
     int64_t* d_rows;
     engram::Workspace ws;
     // TMA descriptors
-    CUtensorMap tm_w_n;                 // wkv as the N-side operand (box 256 rows)
-    CUtensorMap tm_act_m;               // staged rows as the M-side operand (box 128 rows)
-    CUtensorMap tm_act_n[16];           // staged rows as the N-side operand (box 16..256 rows)
-    CUtensorMap tm_sfw;                 // MXFP8 weight scales per row
-    CUtensorMap tm_sfa_n[16];           // MXFP8 activation scales per row (N side)
+    CUtensorMap tm_w_n;        // wkv, prefill B operand (box BN rows x 128 bytes)
+    CUtensorMap tm_act_m;      // staged rows (bf16, or e4m3 codes), box 128 rows x 128 bytes
+    CUtensorMap tm_act_n[16];  // the same, box 16 * (i + 1) rows (the fused kernel's tile)
     // last lookup
     int64_t staged_T;
     int last_error;
@@ -98,6 +109,9 @@ cudaError_t launch_gather(const engram_handle* h, const int32_t* ids, int64_t id
 cudaError_t launch_wkv_tokens_m(const engram_handle* h, const void* hidden, int64_t hs_t,
                                 int64_t hs_h, int64_t T, cudaStream_t s, bool pdl);
 cudaError_t gemm_setup_attributes();
+int prefill_bn(const engram_handle* h);  // kv columns per prefill tile
+cudaError_t pack_scale_atoms(const engram_handle* h, cudaStream_t s);
+cudaError_t launch_unpack_scales(const engram_handle* h, uint8_t* out, int64_t T, cudaStream_t s);
 
 // decode_fused.cu
 FusedPlan fused_plan(const engram_handle* h, int64_t T);

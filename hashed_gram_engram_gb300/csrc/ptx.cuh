@@ -332,6 +332,24 @@ __device__ __forceinline__ void tmem_st4(uint32_t taddr, uint32_t a, uint32_t b,
                  : "memory");
 }
 
+// smem -> TMEM copy of one 512-byte scale-factor atom (32 lines of 16
+// bytes): line i goes to lanes i, 32 + i, 64 + i and 96 + i, four columns.
+__device__ __forceinline__ void tmem_cp_atom(uint32_t taddr, uint64_t sdesc) {
+    asm volatile("tcgen05.cp.cta_group::1.32x128b.warpx4 [%0], %1;" ::"r"(taddr), "l"(sdesc)
+                 : "memory");
+}
+
+// Descriptor of a plain (unswizzled) shared-memory atom for tcgen05.cp:
+// 16-byte lines, 128-byte groups of 8 lines.
+__device__ __forceinline__ uint64_t smem_desc_atom(uint32_t saddr) {
+    uint64_t d = 0;
+    d |= static_cast<uint64_t>((saddr & 0x3FFFFu) >> 4);
+    d |= static_cast<uint64_t>(16 >> 4) << 16;
+    d |= static_cast<uint64_t>(128 >> 4) << 32;
+    d |= static_cast<uint64_t>(1) << 46;
+    return d;
+}
+
 // Shared-memory matrix descriptor for a K-major operand tile written by TMA
 // with 128-byte swizzling: rows of 128 bytes, 8-row core-matrix groups 1024
 // bytes apart.  Advancing K by 32 bytes inside the 128-byte row adds 2 to

@@ -19,6 +19,14 @@
 // accumulators let the epilogue of one unit overlap the MMAs of the next.
 // The weight loads of the first pipeline stages are issued before the
 // programmatic-launch wait, overlapping the gather kernel.
+//
+// MXFP8 wkv: e4m3 codes of the rows (quantised by the gather) times e4m3
+// weights, tcgen05 kind::mxf8f6f4 block_scale, 128 x 128 tiles.  Each stage
+// also brings the two 512-byte scale-factor atoms of its k-block (tokens,
+// weights); the MMA thread copies them into that stage's TMEM scale slot
+// with tcgen05.cp right before the stage's MMAs.  A slot is rewritten only
+// after the MMAs that read it have completed (the producer reuses a stage
+// only after their commit), so one slot per stage suffices.
 #include <cuda_bf16.h>
 
 #include "internal.h"
@@ -33,7 +41,7 @@ constexpr int kStageBudget = 192 * 1024;
 constexpr uint32_t kTmemCols = 512;
 
 struct GemmArgs {
-    int m_tiles, n_tiles, k_blocks, total, T;
+    int m_tiles, n_tiles, k_blocks, total, T, kb128;
     int bn;       // MMA N: kv columns per tile
     int stages;
     uint32_t a_bytes, b_bytes;
@@ -44,6 +52,8 @@ struct GemmArgs {
     const float* qk;
     float2* partials;
     uint16_t* value;
+    const uint8_t* sfa;  // MXFP8: scale atoms of the staged codes
+    const uint8_t* sfb;  // MXFP8: scale atoms of wkv
     unsigned* err;
 };
 
@@ -71,13 +81,17 @@ __device__ __forceinline__ void fail(int* abort_flag, unsigned* err) {
     atomicOr(err, ENGRAM_DEVERR_TIMEOUT);
 }
 
+template <bool kMx>
 __global__ void __launch_bounds__(kThreads, 1)
-    wkv_gemm_bf16_kernel(const __grid_constant__ CUtensorMap tmA,
-                         const __grid_constant__ CUtensorMap tmB, const GemmArgs a) {
+    wkv_gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
+                    const GemmArgs a) {
+    constexpr int BN = kMx ? kBNPrefillMx : kBNPrefill;
+    constexpr int kKElems = kMx ? 128 : 64;  // k per 128-byte block
+    constexpr uint32_t kAtoms = kMx ? 1024u : 0u;  // scale atoms per stage
     extern __shared__ uint8_t smem_raw[];
     uint8_t* smem = reinterpret_cast<uint8_t*>(
         (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~static_cast<uintptr_t>(1023));
-    const uint32_t stage_bytes = a.a_bytes + a.b_bytes;
+    const uint32_t stage_bytes = a.a_bytes + a.b_bytes + kAtoms;
     uint64_t* full = reinterpret_cast<uint64_t*>(smem + a.stages * stage_bytes);
     uint64_t* empty = full + kMaxStages;
     uint64_t* tfull = empty + kMaxStages;
@@ -120,6 +134,15 @@ __global__ void __launch_bounds__(kThreads, 1)
             // The weight operand is independent of the gather; only the
             // token operand waits for the preceding kernel.
             const uint64_t pol_w = policy_evict_last();
+            // token tile (and, MXFP8, its scale atom) of stage s
+            auto load_x = [&](int s, int kb, int row) {
+                uint8_t* sx = smem + s * stage_bytes;
+                tma_load_2d(sx, &tmA, &full[s], kb * kKElems, row);
+                if constexpr (kMx)
+                    bulk_load(sx + a.a_bytes + a.b_bytes,
+                              a.sfa + (static_cast<int64_t>(row / kBM) * a.kb128 + kb) * 512, 512,
+                              &full[s]);
+            };
             Schedule sch(a);
             Unit u;
             bool ok = true, waited = false;
@@ -134,8 +157,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                         pdl_wait();
                         waited = true;
                         for (int i = 0; i < npro; ++i)
-                            tma_load_2d(smem + pro_s[i] * stage_bytes, &tmA, &full[pro_s[i]],
-                                        pro_kb[i] * 64, pro_row[i]);
+                            load_x(pro_s[i], pro_kb[i], pro_row[i]);
                     }
                     const int s = static_cast<int>(issued % a.stages);
                     const uint32_t par = static_cast<uint32_t>((issued / a.stages) & 1);
@@ -143,27 +165,28 @@ __global__ void __launch_bounds__(kThreads, 1)
                         ok = false;
                         break;
                     }
-                    uint8_t* sx = smem + s * stage_bytes;
-                    uint8_t* sw = sx + a.a_bytes;
+                    uint8_t* sw = smem + s * stage_bytes + a.a_bytes;
                     const int x_row = u.m * kBM;
                     mbar_arrive_expect_tx(&full[s], stage_bytes);
-                    tma_load_2d_hint(sw, &tmB, &full[s], kb * 64, u.n * a.bn, pol_w);
+                    tma_load_2d_hint(sw, &tmB, &full[s], kb * kKElems, u.n * BN, pol_w);
+                    if constexpr (kMx)
+                        bulk_load(sw + a.b_bytes + 512,
+                                  a.sfb + (static_cast<int64_t>(u.n) * a.kb128 + kb) * 512, 512,
+                                  &full[s]);
                     if (!waited) {
                         pro_kb[npro] = kb;
                         pro_row[npro] = x_row;
                         pro_s[npro] = s;
                         ++npro;
                     } else {
-                        tma_load_2d(sx, &tmA, &full[s], kb * 64, x_row);
+                        load_x(s, kb, x_row);
                     }
                     ++issued;
                 }
             }
             if (!waited) {
                 pdl_wait();
-                for (int i = 0; i < npro; ++i)
-                    tma_load_2d(smem + pro_s[i] * stage_bytes, &tmA, &full[pro_s[i]],
-                                pro_kb[i] * 64, pro_row[i]);
+                for (int i = 0; i < npro; ++i) load_x(pro_s[i], pro_kb[i], pro_row[i]);
             }
             pdl_launch_dependents();
             if (!ok) fail(abort_flag, a.err);
@@ -183,7 +206,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                     break;
                 }
                 tc_fence_after();
-                const uint32_t d_tmem = tmem_base + static_cast<uint32_t>(acc * a.bn);
+                const uint32_t d_tmem = tmem_base + static_cast<uint32_t>(acc * BN);
                 for (int kb = 0; kb < a.k_blocks; ++kb) {
                     const int s = static_cast<int>(it % a.stages);
                     const uint32_t par = static_cast<uint32_t>((it / a.stages) & 1);
@@ -195,10 +218,24 @@ __global__ void __launch_bounds__(kThreads, 1)
                     const uint32_t sa = smem_addr(smem + s * stage_bytes);
                     const uint64_t adesc = smem_desc_sw128(sa);
                     const uint64_t bdesc = smem_desc_sw128(sa + a.a_bytes);
+                    if constexpr (kMx) {
+                        // this stage's 16-column scale slot: tokens' cells at
+                        // +0, wkv's at +8
+                        const uint32_t sf = tmem_base + 2u * BN + 16u * static_cast<uint32_t>(s);
+                        const uint32_t atoms = sa + a.a_bytes + a.b_bytes;
+                        tmem_cp_atom(sf, smem_desc_atom(atoms));
+                        tmem_cp_atom(sf + 8, smem_desc_atom(atoms + 512));
 #pragma unroll
-                    for (int k = 0; k < 4; ++k)  // 4 x K16 per 64-element block
-                        mma_bf16_ss(d_tmem, adesc + 2 * k, bdesc + 2 * k, a.idesc,
-                                    (kb > 0 || k > 0) ? 1u : 0u);
+                        for (int k = 0; k < 4; ++k)  // 4 x K32, scale byte k of each cell
+                            mma_mxf8_ss(d_tmem, adesc + 2 * k, bdesc + 2 * k,
+                                        idesc_mxf8(kBM, BN, k, k), sf, sf + 8,
+                                        (kb > 0 || k > 0) ? 1u : 0u);
+                    } else {
+#pragma unroll
+                        for (int k = 0; k < 4; ++k)  // 4 x K16 per 64-element block
+                            mma_bf16_ss(d_tmem, adesc + 2 * k, bdesc + 2 * k, a.idesc,
+                                        (kb > 0 || k > 0) ? 1u : 0u);
+                    }
                     mma_commit(&empty[s]);
                     ++it;
                 }
@@ -220,22 +257,22 @@ __global__ void __launch_bounds__(kThreads, 1)
             const int acc = nu & 1;
             const uint32_t apar = static_cast<uint32_t>((nu >> 1) & 1);
             const uint32_t taddr =
-                tmem_base + (static_cast<uint32_t>(q * 32) << 16) + static_cast<uint32_t>(acc * a.bn);
+                tmem_base + (static_cast<uint32_t>(q * 32) << 16) + static_cast<uint32_t>(acc * BN);
             {
                 const int t = u.m * kBM + row;
                 const bool live = t < a.T;
-                const int col0 = u.n * kBNPrefill;
+                const int col0 = u.n * BN;
                 const int h = col0 / a.D;
                 const int d0 = col0 - h * a.D;
                 if (h < a.H) {
-                    uint4 hv[kBNPrefill / 8];
+                    uint4 hv[BN / 8];
                     if (live) {
                         const uint16_t* hp = a.hidden + t * a.hs_t + h * a.hs_h + d0;
 #pragma unroll
-                        for (int i = 0; i < kBNPrefill / 8; ++i) hv[i] = ld_nc_v4(hp + 8 * i);
+                        for (int i = 0; i < BN / 8; ++i) hv[i] = ld_nc_v4(hp + 8 * i);
                     } else {
 #pragma unroll
-                        for (int i = 0; i < kBNPrefill / 8; ++i) hv[i] = make_uint4(0, 0, 0, 0);
+                        for (int i = 0; i < BN / 8; ++i) hv[i] = make_uint4(0, 0, 0, 0);
                     }
                     if (!mbar_wait(&tfull[acc], apar, abort_v)) {
                         ok = false;
@@ -245,7 +282,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                     const float* qkp = a.qk + h * a.D + d0;
                     float skk = 0.f, shk = 0.f;
 #pragma unroll
-                    for (int c = 0; c < kBNPrefill; c += 32) {
+                    for (int c = 0; c < BN; c += 32) {
                         uint32_t r[32];
                         tmem_ld32(taddr + c, r);
                         tmem_ld_wait();
@@ -269,7 +306,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                     __syncwarp();
                     if (lane == 0) mbar_arrive(&tempty[acc]);
                     if (live)
-                        a.partials[(static_cast<int64_t>(t) * a.H + h) * a.J + d0 / kBNPrefill] =
+                        a.partials[(static_cast<int64_t>(t) * a.H + h) * a.J + d0 / BN] =
                             make_float2(skk, shk);
                 } else {
                     if (!mbar_wait(&tfull[acc], apar, abort_v)) {
@@ -279,7 +316,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                     tc_fence_after();
                     uint16_t* vp = a.value + static_cast<int64_t>(t) * a.D + d0;
 #pragma unroll
-                    for (int c = 0; c < kBNPrefill; c += 32) {
+                    for (int c = 0; c < BN; c += 32) {
                         uint32_t r[32];
                         tmem_ld32(taddr + c, r);
                         tmem_ld_wait();
@@ -326,10 +363,52 @@ __global__ void __launch_bounds__(kThreads, 1)
     if (warp == 1) tmem_dealloc(tmem_base, kTmemCols);
 }
 
+// E8M0 [N/32][K/32] block scales of wkv -> atoms [N/128][K/128][512]
+// (byte 16*i + 4*j + b of atom (g, kb) = scale of row 128g + 32j + i,
+// k-block 4kb + b).
+__global__ void pack_scale_atoms_kernel(const uint8_t* ws, uint8_t* atoms, int64_t N, int64_t K) {
+    const int64_t o = static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x;
+    const int64_t kb128 = K / 128;
+    if (o >= N * K / 32) return;
+    const int64_t w = o & 511, atom = o >> 9;
+    const int64_t g = atom / kb128, kb = atom - g * kb128;
+    const int64_t row = 128 * g + 32 * ((w >> 2) & 3) + (w >> 4);
+    const int64_t k32 = 4 * kb + (w & 3);
+    atoms[o] = ws[(row >> 5) * (K >> 5) + k32];
+}
+
+// Staged MXFP8 scale atoms -> plain [T][K/32], for validation.
+__global__ void unpack_scale_atoms_kernel(const uint8_t* atoms, uint8_t* out, int64_t T,
+                                          int64_t K) {
+    const int64_t o = static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x;
+    if (o >= T * (K / 32)) return;
+    const int64_t t = o / (K / 32), k32 = o - t * (K / 32);
+    out[o] = atoms[sf_atom_offset(t, k32, K / 128)];
+}
+
 }  // namespace
 
+cudaError_t pack_scale_atoms(const engram_handle* h, cudaStream_t s) {
+    const int64_t n = h->N * h->K / 32;
+    pack_scale_atoms_kernel<<<static_cast<unsigned>((n + 255) / 256), 256, 0, s>>>(
+        h->wkv_scale, h->ws.wsf_atoms, h->N, h->K);
+    return cudaGetLastError();
+}
+
+cudaError_t launch_unpack_scales(const engram_handle* h, uint8_t* out, int64_t T,
+                                 cudaStream_t s) {
+    const int64_t n = T * (h->K / 32);
+    unpack_scale_atoms_kernel<<<static_cast<unsigned>((n + 255) / 256), 256, 0, s>>>(
+        h->ws.staged_s, out, T, h->K);
+    return cudaGetLastError();
+}
+
 cudaError_t gemm_setup_attributes() {
-    return cudaFuncSetAttribute(wkv_gemm_bf16_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+    cudaError_t e = cudaFuncSetAttribute(wkv_gemm_kernel<false>,
+                                         cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                         kGemmSmemBytes);
+    if (e != cudaSuccess) return e;
+    return cudaFuncSetAttribute(wkv_gemm_kernel<true>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                 kGemmSmemBytes);
 }
 
@@ -350,33 +429,43 @@ static cudaError_t launch(const void* fn, int grid, const CUtensorMap& tmA, cons
     return cudaLaunchKernelExC(&cfg, fn, args);
 }
 
+int prefill_bn(const engram_handle* h) {
+    return h->cfg.wkv_format == ENGRAM_WKV_MXFP8 ? kBNPrefillMx : kBNPrefill;
+}
+
 cudaError_t launch_wkv_tokens_m(const engram_handle* h, const void* hidden, int64_t hs_t,
                                 int64_t hs_h, int64_t T, cudaStream_t s, bool pdl) {
+    const bool mx = h->cfg.wkv_format == ENGRAM_WKV_MXFP8;
+    const int bn = prefill_bn(h);
     GemmArgs a = {};
     a.m_tiles = static_cast<int>((T + kBM - 1) / kBM);
-    a.n_tiles = static_cast<int>(h->N / kBNPrefill);
-    a.k_blocks = static_cast<int>(h->K * 2 / kKBlockBytes);
+    a.n_tiles = static_cast<int>(h->N / bn);
+    a.k_blocks = static_cast<int>(h->K * (mx ? 1 : 2) / kKBlockBytes);
+    a.kb128 = static_cast<int>(h->K / 128);
     a.total = a.m_tiles * a.n_tiles;
     a.T = static_cast<int>(T);
-    a.bn = kBNPrefill;
+    a.bn = bn;
     a.a_bytes = kBM * kKBlockBytes;
-    a.b_bytes = kBNPrefill * kKBlockBytes;
-    a.stages = static_cast<int>(kStageBudget / (a.a_bytes + a.b_bytes));
+    a.b_bytes = static_cast<uint32_t>(bn) * kKBlockBytes;
+    a.stages = static_cast<int>(kStageBudget / (a.a_bytes + a.b_bytes + (mx ? 1024 : 0)));
     if (a.stages > kMaxStages) a.stages = kMaxStages;
     a.idesc = idesc_bf16(kBM, kBNPrefill);
     a.D = static_cast<int>(h->cfg.dim);
     a.H = static_cast<int>(h->cfg.hc_mult);
-    a.J = a.D / kBNPrefill;
+    a.J = a.D / bn;
     a.hidden = static_cast<const uint16_t*>(hidden);
     a.hs_t = hs_t;
     a.hs_h = hs_h;
     a.qk = h->ws.qk;
     a.partials = h->ws.partials;
     a.value = h->ws.value;
+    a.sfa = h->ws.staged_s;
+    a.sfb = h->ws.wsf_atoms;
     a.err = h->ws.err;
     const int grid = a.total < h->num_sms ? a.total : h->num_sms;
-    return launch(reinterpret_cast<const void*>(wkv_gemm_bf16_kernel), grid, h->tm_act_m,
-                  h->tm_w_n, a, s, pdl);
+    return launch(mx ? reinterpret_cast<const void*>(wkv_gemm_kernel<true>)
+                     : reinterpret_cast<const void*>(wkv_gemm_kernel<false>),
+                  grid, h->tm_act_m, h->tm_w_n, a, s, pdl);
 }
 
 }  // namespace engram

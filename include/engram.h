@@ -213,6 +213,13 @@ int engram_gate_noalloc(const void* hidden, const int64_t hidden_strides[3], con
                         int64_t T, int64_t H, int64_t D, double eps, double clamp,
                         cudaStream_t stream);
 
+/* Validation hook, MXFP8 handles only: copy the e4m3 codes [T, K] and the
+ * E8M0 scales [T, K/32] (one per 32 consecutive k, row-major) of the rows
+ * the last lookup or forward staged into device buffers, on `stream`.
+ * Either pointer may be NULL. */
+int engram_debug_staged_mx(engram_t* h, uint8_t* codes, uint8_t* scales, int64_t T,
+                           cudaStream_t stream);
+
 /* Measurement hook: with enable != 0, later engram_forward calls record a
  * CUDA event before and after each of their kernels on the call's stream
  * (this serialises the kernels, so programmatic launch overlap is lost).

@@ -71,8 +71,11 @@ class Case:
 
 
 def compare(case: Case, inp, out, ref, tokens=None, gate=None, value=None, tol=None,
-            value_rtol=1e-2, gate_rtol=1e-2):
-    """Asserts the parity bar; returns a dict of the errors seen."""
+            value_rtol=1e-2, gate_rtol=1e-2, rounding=True):
+    """Asserts the parity bar; returns a dict of the errors seen.  With
+    rounding=False the rounding-level bound is skipped (a reference that
+    differs from the kernel by more than rounding, e.g. unquantised MXFP8
+    activations)."""
     wl = case.wl
     tol = wl.tol if tol is None else tol
     got_bits = W.bits(out)
@@ -87,7 +90,8 @@ def compare(case: Case, inp, out, ref, tokens=None, gate=None, value=None, tol=N
     # projection, the bf16 value of the token-as-M path and the final RTNE
     value_ref = ref["kv"][:, wl.hc_mult * wl.dim:]
     bound = 2.0 ** -8 * np.abs(exp) + 2.0 ** -8 * np.abs(value_ref)[:, None, :] + 1e-5
-    assert np.all(np.abs(got - exp) <= bound), "output differs beyond rounding level"
+    if rounding:
+        assert np.all(np.abs(got - exp) <= bound), "output differs beyond rounding level"
     res = dict(max_abs_err=err)
     mask = inp["token_mask"]
     if mask is not None:

@@ -92,6 +92,9 @@ OFFLOAD = Workload("offload", T=256, dim=4096, hc_mult=4, max_ngram_size=3, n_he
                    head_dim=64, rows=PRIMES_2POW23, table_location="host", tol=3e-2,
                    seed=1239)
 
+# parity case only (not a benchmark configuration): the tiny shapes with MXFP8 wkv
+TINY_MXFP8 = dataclasses.replace(TINY, name="tiny_mxfp8", wkv_format="mxfp8", tol=5e-2,
+                                 seed=1240)
 ALL = {w.name: w for w in (TINY, DECODE, PREFILL, MXFP8_DECODE, MXFP8_PREFILL, OFFLOAD)}
 
 
