@@ -9,7 +9,9 @@ independently seeded layers whose weights together exceed the 129 MB L2,
 so every step reads its weights from HBM; the rotation is captured in a
 CUDA graph and timed with CUDA events on its stream.  The single-step
 latency with L2 flushed (a 512 MB write) before every step is reported
-too.
+too.  Alongside: the MXFP8 decode (T = 64, dim 7168) and prefill
+(T = 4096) steps, and the offload step (T = 256, the 17 GB table in
+pinned host memory, every gathered row crossing the host link).
 
   python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
 
@@ -44,6 +46,9 @@ def parse():
     p.add_argument("--impl", default="ours", choices=["ours", "reference"])
     p.add_argument("--no-prefill", action="store_true")
     p.add_argument("--no-cpu-baseline", action="store_true")
+    p.add_argument("--no-mxfp8", action="store_true", help="skip the MXFP8 decode and prefill")
+    p.add_argument("--no-offload", action="store_true",
+                   help="skip the offload workload (17 GB pinned host table)")
     p.add_argument("--cpu-seconds", type=float, default=10.0)
     p.add_argument("--layers", type=int, default=6)
     p.add_argument("--case", choices=["decode", "prefill"], default=None,
@@ -215,17 +220,64 @@ def stored_traffic(path, sources):
     return None
 
 
-def make_layer(W, Engram, wl, device_index, max_tokens, layer_seed):
+def make_layer(W, Engram, wl, device_index, max_tokens, layer_seed, table=None):
+    """One layer of workload wl with its own seed; a given table is shared."""
     import dataclasses
     wl_l = dataclasses.replace(wl, seed=wl.seed + 101 * layer_seed)
-    table = W.make_table(wl_l, "cuda")
+    if table is None:
+        table = W.make_table(wl_l, "cuda")
     wts = W.make_weights(wl_l, "cuda")
     layer = Engram(dim=wl.dim, hc_mult=wl.hc_mult, max_ngram_size=wl.max_ngram_size,
                    n_heads=wl.n_heads, head_dim=wl.head_dim, max_tokens=max_tokens,
                    table=table, rows=wl.rows, row_offset=W.row_offsets(wl.rows),
-                   wkv=wts["wkv"], q_weight=wts["q_weight"], k_weight=wts["k_weight"],
-                   eps=wl.eps, clamp=wl.clamp, device=device_index)
+                   wkv=wts["wkv"], wkv_scale=wts["wkv_scale"], q_weight=wts["q_weight"],
+                   k_weight=wts["k_weight"], eps=wl.eps, clamp=wl.clamp, device=device_index)
     return wl_l, layer, table, wts
+
+
+def algorithmic_bytes(wl):
+    """HBM bytes one forward of wl must move: wkv (and its scales), hidden in
+    and out, the gathered rows (from HBM unless the table is offloaded),
+    ids, q and k."""
+    mx = wl.wkv_format == "mxfp8"
+    b = (wl.N * wl.K * (1 if mx else 2) + 2 * wl.T * wl.hc_mult * wl.dim * 2
+         + wl.T * wl.n_hash_cols * 4 + 2 * wl.hc_mult * wl.dim * 2)
+    if mx:
+        b += (wl.N // 32) * (wl.K // 32)
+    if wl.table_location != "host":
+        b += wl.T * wl.K * 2
+    return b
+
+
+def time_rotation(torch, layers, stream, steps, warmup):
+    """Forwards rotating over the layers, captured in one CUDA graph and
+    replayed; returns (ms per step, steps timed, steps per graph, replays)."""
+    def step(L):
+        L["layer"].forward(L["hidden"], L["ids"], L.get("mask"), out=L["out"], stream=stream)
+
+    NL = len(layers)
+    for _ in range(max(3, warmup)):
+        for L in layers:
+            step(L)
+    torch.cuda.synchronize()
+    per_graph = NL * max(1, 24 // NL)
+    graph = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(graph, stream=stream):
+        for i in range(per_graph):
+            step(layers[i % NL])
+    for _ in range(3):
+        graph.replay()
+    torch.cuda.synchronize()
+    replays = max(1, steps // per_graph)
+    e0 = torch.cuda.Event(enable_timing=True)
+    e1 = torch.cuda.Event(enable_timing=True)
+    e0.record(stream)
+    for _ in range(replays):
+        graph.replay()
+    e1.record(stream)
+    torch.cuda.synchronize()
+    n = replays * per_graph
+    return e0.elapsed_time(e1) / n, n, per_graph, replays
 
 
 def run_case(args):
@@ -279,68 +331,49 @@ def main():
         dist.barrier()
     g.build()
     hbm_peak, bf16_peak, peak_kind = peaks()
+    fp8_peak = 2.0 * bf16_peak  # dense fp8 : bf16 = 4.5 : 2.25 nominal
     stream = torch.cuda.Stream(dev)
     torch.cuda.set_stream(stream)
 
+    def max_over_ranks(x):
+        t = torch.tensor([x], dtype=torch.float64, device=dev)
+        if world > 1:
+            dist.all_reduce(t, op=dist.ReduceOp.MAX)
+        return float(t.item())
+
+    def rotation_layers(wl, NL, max_tokens0, table=None, seed0=0):
+        out = []
+        for l in range(NL):
+            wl_l, layer, tab, wts = make_layer(W, Engram, wl, local,
+                                               max_tokens0 if l == 0 else wl.T,
+                                               seed0 + l + 1000 * rank, table=table)
+            st = W.make_step_inputs(wl_l, "cuda", step=rank)
+            out.append(dict(wl=wl_l, layer=layer, table=tab, wts=wts, hidden=st["hidden"],
+                            ids=st["hash_ids"], mask=st["token_mask"],
+                            out=torch.empty_like(st["hidden"])))
+        torch.cuda.synchronize()
+        return out
+
     # Decode: a rotation over NL independently seeded layers (each its own
-    # table, wkv, q, k, hidden and ids).  Their packed weights (NL x 40 MiB)
-    # exceed the 129 MB L2, so consecutive steps read weights from HBM and no
-    # flush is needed between them.  The rotation is captured in a CUDA graph
-    # (as a serving engine runs decode) and replayed.
+    # table, wkv, q, k, hidden and ids).  Their weights (NL x 40 MiB) exceed
+    # the 129 MB L2, so consecutive steps read weights from HBM and no flush
+    # is needed between them.  The rotation is captured in a CUDA graph (as a
+    # serving engine runs decode) and replayed.
     wl = W.DECODE
     NL = args.layers
-    layers = []
-    for l in range(NL):
-        wl_l, layer, table, wts = make_layer(W, Engram, wl, local, W.PREFILL.T if l == 0 else wl.T,
-                                             l + 1000 * rank)
-        st = W.make_step_inputs(wl_l, "cuda", step=rank)
-        layers.append(dict(wl=wl_l, layer=layer, table=table, wts=wts, hidden=st["hidden"],
-                           ids=st["hash_ids"], out=torch.empty_like(st["hidden"])))
-    torch.cuda.synchronize()
-
-    def step(L):
-        L["layer"].forward(L["hidden"], L["ids"], None, out=L["out"], stream=stream)
-
-    for _ in range(max(3, args.warmup)):
-        for L in layers:
-            step(L)
-    torch.cuda.synchronize()
-    per_graph = NL * max(1, 24 // NL)
-    graph = torch.cuda.CUDAGraph()
-    with torch.cuda.graph(graph, stream=stream):
-        for i in range(per_graph):
-            step(layers[i % NL])
-    for _ in range(3):
-        graph.replay()
-    torch.cuda.synchronize()
-    replays = max(1, args.steps // per_graph)
-    steps = replays * per_graph
-
+    layers = rotation_layers(wl, NL, W.PREFILL.T)
     clocks = Clocks(local)
     clocks.start()
     if world > 1:
         dist.barrier()
-    torch.cuda.synchronize()
-    e0 = torch.cuda.Event(enable_timing=True)
-    e1 = torch.cuda.Event(enable_timing=True)
-    e0.record(stream)
-    for _ in range(replays):
-        graph.replay()
-    e1.record(stream)
-    torch.cuda.synchronize()
+    ms_step, steps, per_graph, replays = time_rotation(torch, layers, stream, args.steps,
+                                                       args.warmup)
     if world > 1:
         dist.barrier()
     clk = clocks.stop()
-    total_ms = e0.elapsed_time(e1)
-    t = torch.tensor([total_ms], dtype=torch.float64, device=dev)
-    if world > 1:
-        dist.all_reduce(t, op=dist.ReduceOp.MAX)
-    total_ms = float(t.item())
-    ms_step = total_ms / steps
-    value = world * wl.T * steps / (total_ms / 1e3)
-
-    step_bytes = (wl.N * wl.K * 2 + 2 * wl.T * wl.hc_mult * wl.dim * 2 + wl.T * wl.K * 2
-                  + wl.T * wl.n_hash_cols * 4 + 2 * wl.hc_mult * wl.dim * 2)
+    ms_step = max_over_ranks(ms_step)
+    value = world * wl.T / (ms_step * 1e-3)
+    step_bytes = algorithmic_bytes(wl)
     # one kernel per step: its average duration is the step time (launch gaps included)
     achieved = step_bytes / (ms_step * 1e-3) / 1e9
     traffic = stored_traffic(DECODE_PROFILE, DECODE_SOURCES)
@@ -348,6 +381,10 @@ def main():
     # single-step latency with L2 flushed before the step (cold code, page
     # tables and weights), and the kernel's own event time
     L0 = layers[0]
+
+    def step0():
+        L0["layer"].forward(L0["hidden"], L0["ids"], None, out=L0["out"], stream=stream)
+
     flush = torch.empty(L2_FLUSH_BYTES, dtype=torch.uint8, device=dev)
     lat = []
     engram_profile_enable(L0["layer"].handle, 1)
@@ -357,7 +394,7 @@ def main():
         a0 = torch.cuda.Event(enable_timing=True)
         a1 = torch.cuda.Event(enable_timing=True)
         a0.record(stream)
-        step(L0)
+        step0()
         a1.record(stream)
         kern.append(engram_profile_read(L0["layer"].handle)[1])
         torch.cuda.synchronize()
@@ -381,11 +418,7 @@ def main():
         fwd_h()
     b1.record(stream)
     torch.cuda.synchronize()
-    e2e_ms = b0.elapsed_time(b1) / ne
-    th = torch.tensor([e2e_ms], dtype=torch.float64, device=dev)
-    if world > 1:
-        dist.all_reduce(th, op=dist.ReduceOp.MAX)
-    e2e_ms = float(th.item())
+    e2e_ms = max_over_ranks(b0.elapsed_time(b1) / ne)
 
     line = {
         "metric": METRIC, "value": value, "unit": "tokens/s", "n_gpus": world,
@@ -401,23 +434,23 @@ def main():
                              "the launch stream",
                    "parallelism": f"replicas x{world} (token-sharded, no collective)"},
         "roofline": {"bound": "hbm",
-                     "kernel": "decode_fused_kernel (gather4 + tcgen05 wkv + gate, one launch)",
+                     "kernel": "decode_fused_kernel (gather + tcgen05 wkv + gate, one launch)",
                      "achieved": achieved, "peak": hbm_peak, "unit": "GB/s",
                      "frac": achieved / hbm_peak, "traffic": traffic,
                      "peak_kind": peak_kind, "algorithmic_bytes": step_bytes,
                      "kernel_ms": ms_step},
         "latency_l2_flushed_us": {"step_median": 1e3 * float(np.median(lat)),
                                   "kernel_median": 1e3 * float(np.median(kern))},
-        "e2e": {"value": wl.T / (e2e_ms * 1e-3) * world, "unit": "tokens/s",
+        "e2e": {"value": world * wl.T / (e2e_ms * 1e-3), "unit": "tokens/s",
                 "h2d_bytes_per_step": int(hid_h.numel() * 2 + ids_h.numel() * 4),
                 "d2h_bytes_per_step": int(out_h.numel() * 2)},
         "gpu_launches": steps,
         "clocks": clk,
     }
+    launches = steps
 
-    if not args.no_prefill:
-        pw = W.PREFILL
-        layer = L0["layer"]
+    def prefill_block(layer, pw, kernel_name, peak, peak_name):
+        """Per-step time of a prefill forward and its kernels' event times."""
         pstep = W.make_step_inputs(pw, "cuda", step=rank)
         ph, pids, pmask = pstep["hidden"], pstep["hash_ids"], pstep["token_mask"]
         pout = torch.empty_like(ph)
@@ -433,7 +466,7 @@ def main():
             pf()
         c1.record(stream)
         torch.cuda.synchronize()
-        p_ms = c0.elapsed_time(c1) / pk
+        p_ms = max_over_ranks(c0.elapsed_time(c1) / pk)
         engram_profile_enable(layer.handle, 1)
         pprof = []
         for _ in range(10):
@@ -443,16 +476,22 @@ def main():
         pprof = np.array(pprof)
         pw_ms = float(np.median(pprof[:, 1]))
         flops = 2.0 * pw.T * pw.N * pw.K
-        line["prefill"] = {
-            "workload": "prefill", "T": pw.T, "tokens_per_s": pw.T / (p_ms * 1e-3),
-            "ms_per_step": p_ms, "l2": "inputs larger than L2 (hidden 256 MiB per step)",
+        tf = flops / (pw_ms * 1e-3) / 1e12
+        return pk * 3 + 30, {
+            "workload": pw.name, "T": pw.T, "tokens_per_s": world * pw.T / (p_ms * 1e-3),
+            "ms_per_step": p_ms, "l2": "inputs larger than L2 (hidden "
+                                      f"{pw.T * pw.hc_mult * pw.dim * 2 >> 20} MiB per step)",
             "kernel_ms": {"gather": float(np.median(pprof[:, 0])), "wkv": pw_ms,
                           "gate": float(np.median(pprof[:, 2]))},
-            "roofline": {"bound": "tensor", "kernel": "wkv_gemm_bf16 (token-as-M)",
-                         "achieved": flops / (pw_ms * 1e-3) / 1e12, "peak": bf16_peak,
-                         "unit": "TFLOP/s", "frac": flops / (pw_ms * 1e-3) / 1e12 / bf16_peak,
-                         "peak_kind": peak_kind},
+            "roofline": {"bound": "tensor", "kernel": kernel_name, "achieved": tf,
+                         "peak": peak, "unit": "TFLOP/s", "frac": tf / peak,
+                         "peak_kind": peak_name},
         }
+
+    if not args.no_prefill:
+        n, line["prefill"] = prefill_block(L0["layer"], W.PREFILL, "wkv_gemm_kernel<bf16>",
+                                           bf16_peak, peak_kind)
+        launches += n
 
     if rank == 0 and world == 1 and not args.no_cpu_baseline:
         host = dict(table=W.bits(L0["table"]), row_offset=W.row_offsets(wl.rows),
@@ -464,10 +503,75 @@ def main():
                                 "sample": f"{n} decode-step tokens ({el:.1f} s, "
                                           f"single-threaded fp64 C oracle)",
                                 "host_cores": os.cpu_count()}
-    if rank == 0:
-        print(json.dumps(line), flush=True)
     for L in layers:
         L["layer"].close()
+    del layers, L0
+
+    if not args.no_mxfp8:
+        # MXFP8 wkv: the same decode rotation (T = 64, D = 7168) and the
+        # T = 4096 prefill step on the first layer
+        mw = W.MXFP8_DECODE
+        mlayers = rotation_layers(mw, NL, W.MXFP8_PREFILL.T, seed0=50)
+        m_ms, m_steps, _, _ = time_rotation(torch, mlayers, stream, args.steps, args.warmup)
+        m_ms = max_over_ranks(m_ms)
+        mb = algorithmic_bytes(mw)
+        line["mxfp8_decode"] = {
+            "workload": mw.name, "T": mw.T, "dim": mw.dim, "tokens_per_s": world * mw.T / (m_ms * 1e-3),
+            "ms_per_step": m_ms, "steps": m_steps, "layers_rotated": NL,
+            "wkv": f"e4m3 [{mw.N}, {mw.K}] + E8M0 [{mw.N // 32}, {mw.K // 32}]",
+            "l2": f"inputs larger than L2: {NL} layers' weights ({NL * mw.N * mw.K >> 20} MiB)",
+            "roofline": {"bound": "hbm", "kernel": "decode_fused_kernel<mxfp8>",
+                         "achieved": mb / (m_ms * 1e-3) / 1e9, "peak": hbm_peak,
+                         "unit": "GB/s", "frac": mb / (m_ms * 1e-3) / 1e9 / hbm_peak,
+                         "algorithmic_bytes": mb, "peak_kind": peak_kind},
+        }
+        launches += m_steps
+        if not args.no_prefill:
+            n, line["mxfp8_prefill"] = prefill_block(
+                mlayers[0]["layer"], W.MXFP8_PREFILL, "wkv_gemm_kernel<mxfp8>", fp8_peak,
+                f"{peak_kind} bf16 x 2 (fp8:bf16 nominal ratio)")
+            launches += n
+        for L in mlayers:
+            L["layer"].close()
+        del mlayers
+
+    if not args.no_offload:
+        ow = W.OFFLOAD
+        need = ow.total_rows * ow.head_dim * 2
+        avail = W.host_memory_bytes()
+        if avail is not None and avail < need + (8 << 30):
+            line["offload"] = {"workload": ow.name, "skipped":
+                               f"{need >> 30} GiB pinned table, {avail >> 30} GiB host memory free"}
+        else:
+            # the 17 GB table in pinned host memory, shared by the rotated
+            # layers; every gathered row crosses the host link
+            otable = W.make_table(ow, "cuda")
+            olayers = rotation_layers(ow, 4, ow.T, table=otable, seed0=70)
+            o_ms, o_steps, _, _ = time_rotation(torch, olayers, stream, args.steps, args.warmup)
+            o_ms = max_over_ranks(o_ms)
+            ob = algorithmic_bytes(ow)
+            host_b = ow.T * ow.K * 2
+            line["offload"] = {
+                "workload": ow.name, "T": ow.T, "tokens_per_s": world * ow.T / (o_ms * 1e-3),
+                "ms_per_step": o_ms, "steps": o_steps, "layers_rotated": 4,
+                "table": f"{need / 1e9:.2f} GB bf16 in pinned host memory",
+                "host_link": {"bytes_per_step": host_b,
+                              "GB_per_s": host_b / (o_ms * 1e-3) / 1e9,
+                              "rows_per_step": ow.T * ow.n_hash_cols},
+                "roofline": {"bound": "hbm", "kernel": "decode_fused_kernel (host table)",
+                             "achieved": ob / (o_ms * 1e-3) / 1e9, "peak": hbm_peak,
+                             "unit": "GB/s", "frac": ob / (o_ms * 1e-3) / 1e9 / hbm_peak,
+                             "algorithmic_bytes": ob, "peak_kind": peak_kind},
+            }
+            launches += o_steps
+            for L in olayers:
+                L["layer"].close()
+            del olayers, otable
+
+    line["gpu_launches"] = steps
+    line["gpu_launches_all_timed_regions"] = launches
+    if rank == 0:
+        print(json.dumps(line), flush=True)
     if world > 1:
         dist.destroy_process_group()
 

@@ -199,3 +199,23 @@ def bits(t: torch.Tensor) -> np.ndarray:
     if t.dtype in (torch.uint8, torch.bool):
         return t.to(torch.uint8).cpu().numpy()
     return t.cpu().numpy()
+
+
+def host_memory_bytes():
+    """Memory this process may still pin on the host (cgroup limit aware)."""
+    avail = None
+    try:
+        for line in open("/proc/meminfo"):
+            if line.startswith("MemAvailable:"):
+                avail = int(line.split()[1]) * 1024
+    except OSError:
+        pass
+    try:
+        lim = open("/sys/fs/cgroup/memory.max").read().strip()
+        use = int(open("/sys/fs/cgroup/memory.current").read().strip())
+        if lim != "max":
+            cg = int(lim) - use
+            avail = cg if avail is None else min(avail, cg)
+    except (OSError, ValueError):
+        pass
+    return avail
