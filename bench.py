@@ -220,6 +220,16 @@ def stored_traffic(path, sources):
     return None
 
 
+def reduce_max(x, world, device):
+    """The largest of every rank's x (the slowest rank's time sets the job's)."""
+    import torch
+    import torch.distributed as dist
+    t = torch.tensor([float(x)], dtype=torch.float64, device=device)
+    if world > 1:
+        dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
 def make_layer(W, Engram, wl, device_index, max_tokens, layer_seed, table=None):
     """One layer of workload wl with its own seed; a given table is shared."""
     import dataclasses
@@ -336,10 +346,7 @@ def main():
     torch.cuda.set_stream(stream)
 
     def max_over_ranks(x):
-        t = torch.tensor([x], dtype=torch.float64, device=dev)
-        if world > 1:
-            dist.all_reduce(t, op=dist.ReduceOp.MAX)
-        return float(t.item())
+        return reduce_max(x, world, dev)
 
     def rotation_layers(wl, NL, max_tokens0, table=None, seed0=0):
         out = []

@@ -98,6 +98,12 @@ TINY_MXFP8 = dataclasses.replace(TINY, name="tiny_mxfp8", wkv_format="mxfp8", to
 ALL = {w.name: w for w in (TINY, DECODE, PREFILL, MXFP8_DECODE, MXFP8_PREFILL, OFFLOAD)}
 
 
+def shard_tokens(T: int, rank: int, world: int) -> tuple[int, int]:
+    """Token range [lo, hi) of one rank when T tokens are split evenly (the
+    forward has no cross-token dependence, so ranks need no exchange)."""
+    return T * rank // world, T * (rank + 1) // world
+
+
 def row_offsets(rows) -> np.ndarray:
     """Start row of every column's bucket in the concatenated table."""
     r = np.asarray(rows, np.int64)
