@@ -18,7 +18,8 @@ import numpy as np
 
 from . import _lib
 from ._lib import (EngramError, engram_config, engram_create, engram_debug_intermediates,
-                   engram_debug_staged_mx, engram_debug_staged_rows, engram_destroy, engram_device_error,
+                   engram_debug_keep_value, engram_debug_staged_mx, engram_debug_staged_rows,
+                   engram_destroy, engram_device_error,
                    engram_forward, engram_forward_host, engram_gate_noalloc,
                    engram_last_error, engram_layout,
                    engram_lookup, engram_profile_enable, engram_profile_read,
@@ -29,7 +30,7 @@ from ._lib import (EngramError, engram_config, engram_create, engram_debug_inter
 __all__ = [
     "Engram", "EngramError", "engram_config", "engram_weights", "engram_create",
     "engram_destroy", "engram_lookup", "engram_forward", "engram_forward_host",
-    "engram_gate_noalloc", "engram_debug_staged_mx",
+    "engram_gate_noalloc", "engram_debug_staged_mx", "engram_debug_keep_value",
     "engram_last_error", "engram_device_error", "engram_layout", "engram_debug_intermediates",
     "engram_debug_staged_rows", "engram_profile_enable", "engram_profile_read",
     "ENGRAM_WKV_BF16", "ENGRAM_WKV_MXFP8", "ENGRAM_TABLE_DEVICE",
@@ -51,7 +52,8 @@ class Engram:
 
     def __init__(self, *, dim, hc_mult, max_ngram_size, n_heads, head_dim, max_tokens,
                  table, rows, wkv, q_weight, k_weight, row_offset=None, wkv_scale=None,
-                 eps=1e-6, clamp=1e-6, wkv_format=None, table_location=None, device=None):
+                 eps=1e-6, clamp=1e-6, wkv_format=None, table_location=None, device=None,
+                 keep_value=False):
         import torch
         self.dim, self.hc_mult, self.head_dim = int(dim), int(hc_mult), int(head_dim)
         self.n_hash_cols = (int(max_ngram_size) - 1) * int(n_heads)
@@ -78,6 +80,8 @@ class Engram:
         self._keep = (table, wkv, wkv_scale, q_weight, k_weight, rows, row_offset)
         self.device = int(device)
         self.handle = engram_create(cfg, w)
+        if keep_value:  # validation: let intermediates() return the fused path's value
+            engram_debug_keep_value(self.handle, 1)
 
     def close(self):
         if getattr(self, "handle", None):

@@ -43,6 +43,7 @@ EXPORTED = (
     "engram_forward_host", "engram_last_error", "engram_device_error", "engram_layout",
     "engram_debug_intermediates", "engram_debug_staged_rows", "engram_profile_enable",
     "engram_profile_read", "engram_gate_noalloc", "engram_debug_staged_mx",
+    "engram_debug_keep_value",
 )
 
 
@@ -100,6 +101,7 @@ def load(path: str | None = None):
             "engram_debug_intermediates": [vp, vp, vp, i64, vp],
             "engram_debug_staged_rows": [vp, vp, i64, vp],
             "engram_debug_staged_mx": [vp, vp, vp, i64, vp],
+            "engram_debug_keep_value": [vp, ctypes.c_int],
             "engram_profile_enable": [vp, ctypes.c_int],
             "engram_profile_read": [vp, vp],
             "engram_gate_noalloc": [vp, vp, vp, i64, vp, vp, vp, vp, vp, i64, i64, i64,
@@ -208,6 +210,10 @@ def engram_debug_staged_rows(h, rows, T, stream=None):
 def engram_debug_staged_mx(h, codes, scales, T, stream=None):
     return _check(load().engram_debug_staged_mx(h, _ptr(codes), _ptr(scales), int(T),
                                                 _stream(stream)), "engram_debug_staged_mx")
+
+
+def engram_debug_keep_value(h, enable=1):
+    return _check(load().engram_debug_keep_value(h, int(enable)), "engram_debug_keep_value")
 
 
 def engram_profile_enable(h, enable=1):

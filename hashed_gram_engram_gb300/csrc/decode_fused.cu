@@ -1,49 +1,61 @@
-// The whole Engram forward of a decode step (T <= 256) in one cooperative,
-// persistent kernel (one CTA per SM).  Engram.forward
+// The whole Engram forward of a decode step (T <= 256; MXFP8 wkv T <= 128)
+// in one cooperative, persistent kernel, one CTA per SM.  Engram.forward
 // ("vllm.models.deepseek_v4_1.common.engram") defines the layer; the gate
-// arithmetic is that of _engram_gate_finish_kernel with one rank
+// arithmetic is that of _engram_gate_finish_kernel with one rank, split over
+// dim the way _engram_gate_partials_kernel splits it over ranks
 // ("vllm.models.deepseek_v41.amd.engram").
 //
-// Work split: CTA i owns a contiguous slice of the projection's N = D*(H+1)
-// columns -- 16-column granules dealt out evenly, so 128 or 144 columns at
-// the decode shapes -- over the full K.  Tokens sit on the MMA's M side
-// (128 rows per accumulator; rows past T are ignored), the slice on N.
+// Column ownership.  The N = D*(H+1) kv columns are cut into 16-column
+// granules; CTA c owns a balanced share of them, made of a few VALUE
+// granules (dims [v0, v0 + vlen) of the shared value) followed by a run of
+// KEY columns [k0, k0 + klen) (which may straddle two hc copies).  wkv is
+// packed at create time so that each CTA's rows are consecutive.  Because a
+// CTA holds the value of its dims for every token, it finishes those output
+// dims itself: the only data that crosses SMs after the projection are the
+// gate partial sums.
 //
-//   gather   every CTA copies its share (about 1/grid) of the T x C hash
-//            rows into the staged-rows buffer (an id outside its table
-//            gives a zero row and sets the device error flag), so each SM
-//            touches only a few of the table's pages; then a first grid
-//            barrier.  The weight stream has started meanwhile.  Rows
-//            staged by an earlier engram_lookup skip this step;
-//   wkv      wkv is packed at create time k-block-major with the 128-byte
-//            swizzle applied, so each stage's weight slice is one contiguous
-//            bulk copy; the staged token rows arrive by TMA (a box of T
-//            rows rounded up to 16); tcgen05 kind::f16, fp32 accumulators in
-//            TMEM;
-//   epilogue each thread owns one token's whole slice (its hidden columns
-//            are loaded while the MMAs run): for key columns it sums
-//            hidden^2, key^2 and hidden*q*k*key per hc copy (the split over
-//            dim that _engram_gate_partials_kernel uses across ranks, here
-//            across CTAs), for value columns it stores the value;
-//   finish   after a second grid barrier each CTA takes (token, hc) rows:
-//            one warp per row adds the partial sums of the CTAs covering
-//            that hc copy (a fixed order: results are run-to-run identical)
-//            and forms the signed-sqrt sigmoid gate; then all threads write
-//            hidden + gate * value (masked tokens copy hidden's bits).  The
-//            value rows and partial records arrive by bulk copy; the hidden
-//            rows were bulk-copied while the weights streamed.
+// Roles (224 threads): warp 0 streams the CTA's weight slice through a deep
+// ring of k-block stages from the first instant (bulk copies of >= 16 KB
+// keep enough bytes in flight for full HBM bandwidth); warp 1 owns TMEM and
+// issues the tcgen05 MMAs (tokens on M, the slice on N, fp32 accumulators
+// in TMEM) -- for bf16 with T <= 128 it takes the even k-blocks and warp 6
+// the odd ones into a second accumulator (one thread's issue loop cannot
+// keep the tensor pipe busy on these small MMAs), the two summed when read;
+// warps 2-5 load the token tiles, then run the epilogue and the residual
+// (TMEM lane quarter = warp % 4).  The token tiles travel on the
+// load/store path (cp.async, 16 bytes a thread, each chunk to its 128-byte-
+// swizzled place), loaded by warps 2-3 while warps 4-5 wait in a hardware
+// barrier: the scheduler that runs the MMA issuer (warp 1) then runs no
+// other busy warp.
+//
+//   gather   each CTA copies ~1/grid of the T x C hash rows into the
+//            staged buffer (MXFP8: and quantises them into e4m3 codes and
+//            scales); grid barrier 1; then every CTA loads the token tiles
+//            of every k-block from the staged rows.  Rows staged by
+//            engram_lookup skip the gather;
+//   epilogue thread = token: for the key columns it sums hidden^2, key^2
+//            and hidden*q*k*key per hc copy into a record per (copy, token,
+//            CTA); grid barrier 2;
+//   gates    CTA c reduces the records of rows (token, copy) = c, c + grid,
+//            ... (one warp per row, a fixed summation order: runs are
+//            bit-identical) and publishes the gates; grid barrier 3;
+//   residual every CTA writes hidden + gate * value for its own value dims
+//            (masked tokens keep hidden's bits), the value read straight
+//            from TMEM.
 //
 // MXFP8 wkv (T <= 128): the gather also quantises the rows (e4m3 codes and
-// E8M0 scales per 32 k), the MMAs are tcgen05 kind::mxf8f6f4 with
-// block_scale, and the scale factors sit in TMEM next to the accumulator.
-// A CTA's weight slice starts on any 16-column boundary, so instead of
-// copying scale atoms the epilogue warps write the scale words into TMEM
-// themselves (tcgen05.st): the weights' at kernel start, the tokens' after
-// the gather.  Scale cell layout (tcgen05 block scaling, scale_vec::1X):
-// the scale of A row r for k-block b sits in lane r, column sfa + r / 32,
-// byte b; that of B row n in lane n % 32, column sfb + n / 32, byte b.
+// E8M0 scales per 32 k); the MMAs are kind::mxf8f6f4 block_scale and the
+// scale factors sit in TMEM next to the accumulator.  A slice starts on any
+// 16-column boundary, so the epilogue warps write the scale words into TMEM
+// (tcgen05.st) rather than copying 128-row atoms: the weights' at kernel
+// start, the tokens' after the gather.  Scale cell layout (scale_vec::1X):
+// the scale of A row r for k-block b is byte b of lane r, column
+// sfa + r / 32; that of B row n is byte b of lane n % 32, column sfb + n / 32.
 //
-// Both grid barriers reset themselves, so a captured launch replays.
+// Grid barriers: counters that only grow.  Each launch reads its epoch e
+// from a launch counter at start (CTA 0 advances it at the very end); a
+// CTA arrives with a posted release add and waits until the counter reaches
+// e * grid.  No reset, so a captured launch replays.  Every wait is bounded.
 #include <cuda_bf16.h>
 
 #include "internal.h"
@@ -53,48 +65,50 @@
 namespace engram {
 namespace {
 
-constexpr int kThreads = 192;
+constexpr int kThreads = 224;
 constexpr int kWarps = kThreads / 32;
-constexpr int kMaxStages = 8;
-constexpr int kSliceChunks = kMaxFusedSlice / 16;  // 16-column chunks of one slice
-constexpr int kPartFloats = 8;  // per (token, CTA): 2 hc copies x (hh, kk, hk, pad)
-constexpr int kHidRows = 4;     // finish rows whose hidden is prefetched to shared memory
+constexpr int kMaxWStages = 12;
+constexpr int kXStages = 4;
+constexpr int kKeyChunks = kMaxFusedSlice / 16;  // 16-column chunks of a slice
+constexpr uint32_t kTmemCols = 512;
 
 struct FusedArgs {
     int T, Tn, D, H, C, E, N, K;
-    int mtiles, granules, k_blocks, stages;
-    int kb128;  // K / 128: MXFP8 scale words per row
-    uint32_t w_stage_bytes, x_bytes;  // per stage: weight slice region, token bytes
-    int gather;                       // gather the hash rows in this launch
+    int mtiles, NG, VG, k_blocks, kb128;
+    int w_stages;
+    int dual;  // two MMA issuers, two accumulators (bf16, one 128-token tile)
+    uint32_t w_stage_bytes, x_stage_bytes, x_bytes;
+    int gather;  // gather the hash rows in this launch
     const int32_t* ids;
     int64_t ids_stride;
     const int64_t* row_offset;
     const int64_t* rows;
     const uint16_t* table;
-    uint16_t* staged;    // [rows_alloc][K] bf16
-    uint8_t* staged_q;   // MXFP8: e4m3 codes [rows_alloc][K]
-    uint8_t* staged_s;   // MXFP8: scale atoms of the codes
+    uint16_t* staged;       // [rows_alloc][K] bf16
+    uint8_t* staged_q;      // MXFP8: e4m3 codes [rows_alloc][K]
+    uint8_t* staged_s;      // MXFP8: scale atoms of the codes
     const uint8_t* wscale;  // MXFP8: E8M0 [N/32][K/32]
     const uint16_t* hidden;
     int64_t hs_t, hs_h;
     uint16_t* out;
     int64_t os_t, os_h;
     const uint8_t* mask;
-    const float* qk;        // [H, D]
-    const uint8_t* wpack;   // [K bytes/128][N][128 bytes], 8-row groups 128-byte swizzled
-    float* part;            // [tpitch][grid][kPartFloats]
-    float* value;           // [tpitch][D]
-    unsigned* bar;          // two grid barriers: {arrivals, generation} each
+    const float* qk;       // [H, D]
+    const uint8_t* wpack;  // [K bytes/128][N][128 bytes], CTA slices consecutive
+    float4* rec;           // records (shh, skk, shk, -) per copy block [Tpitch][nh]
+    int rec_base[kMaxCopies];  // float4 offset of each copy's block
+    int cf[kMaxCopies];        // first CTA holding each copy's keys
+    int nh[kMaxCopies];        // number of CTAs holding each copy's keys
+    float* value;              // fp32 [T][D] for validation, or null
+    unsigned long long* bar;   // launch counter, then three barrier counters
     float* gate_out;
     float eps, clamp, inv_d, inv_sqrt_d;
     unsigned* err;
-    uint32_t hid_off, qk_off, bar_off, hid_rows;
+    uint32_t x_off, qk_off, bar_off;
 };
 
-// CTA that owns granule x when NG granules are dealt to G CTAs.
-__device__ __forceinline__ int owner(int x, int NG, int G) { return ((x + 1) * G - 1) / NG; }
-__device__ __forceinline__ int first_granule(int cta, int NG, int G) {
-    return static_cast<int>(static_cast<int64_t>(cta) * NG / G);
+__device__ __forceinline__ int first_granule(int cta, int n, int G) {
+    return static_cast<int>(static_cast<int64_t>(cta) * n / G);
 }
 
 __device__ __forceinline__ void fail(int* abort_flag, unsigned* err) {
@@ -102,22 +116,18 @@ __device__ __forceinline__ void fail(int* abort_flag, unsigned* err) {
     atomicOr(err, ENGRAM_DEVERR_TIMEOUT);
 }
 
-// Self-resetting grid barrier: the last CTA to arrive zeroes the count and
-// advances the generation; the others wait, bounded, for the generation
-// to change.  One thread per CTA, after the CTA's writes are fenced.
-__device__ __forceinline__ bool grid_barrier(unsigned* bar, unsigned G) {
-    const unsigned gen = ld_acquire_u32(bar + 1);
-    __threadfence();
-    if (atomicAdd(bar, 1u) == G - 1u) {
-        bar[0] = 0u;
-        __threadfence();
-        atomicAdd(bar + 1, 1u);
-        return true;
-    }
+// Grid barrier: a posted release add, then a bounded wait until all G CTAs
+// of this launch (epoch e) have arrived.  One thread per CTA.
+__device__ __forceinline__ void grid_arrive(unsigned long long* ctr) {
+    asm volatile("red.release.gpu.global.add.u64 [%0], 1;" ::"l"(ctr) : "memory");
+}
+
+__device__ __forceinline__ bool grid_wait(const unsigned long long* ctr, unsigned long long target) {
     const uint64_t t0 = globaltimer_ns();
     uint32_t spins = 0;
-    while (ld_acquire_u32(bar + 1) == gen) {
-        if ((++spins & 63u) == 0 &&
+    while (ld_acquire_u64(ctr) < target) {
+        __nanosleep(32);
+        if ((++spins & 15u) == 0 &&
             (globaltimer_ns() - t0 > kWaitLimitNs || spins > kWaitLimitIters))
             return false;
     }
@@ -126,180 +136,226 @@ __device__ __forceinline__ bool grid_barrier(unsigned* bar, unsigned G) {
 
 template <bool kMx>
 __global__ void __launch_bounds__(kThreads, 1)
-    decode_fused_kernel(const __grid_constant__ CUtensorMap tm_x, const FusedArgs a) {
-    constexpr int kKElems = kMx ? 128 : 64;  // k per 128-byte block
+    decode_fused_kernel(const FusedArgs a) {
     extern __shared__ uint8_t smem_raw[];
     uint8_t* smem = reinterpret_cast<uint8_t*>(
         (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~static_cast<uintptr_t>(1023));
-    const uint32_t stage_bytes = a.w_stage_bytes + a.mtiles * 16384u;
-    uint16_t* hid_s = reinterpret_cast<uint16_t*>(smem + a.hid_off);
-    float* qk_s = reinterpret_cast<float*>(smem + a.qk_off);  // the slice's q*k columns
-    uint64_t* full = reinterpret_cast<uint64_t*>(smem + a.bar_off);
-    uint64_t* empty = full + kMaxStages;
-    uint64_t* tfull = empty + kMaxStages;
-    uint64_t* hbar = tfull + 1;
-    uint64_t* fbar = hbar + 1;
-    uint64_t* drain = fbar + 1;
-    uint64_t* scbar = drain + 1;  // MXFP8: every scale word is in TMEM
-    uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(scbar + 1);
+    uint8_t* xring = smem + a.x_off;
+    float* qk_s = reinterpret_cast<float*>(smem + a.qk_off);  // q*k of the slice's key columns
+    uint64_t* wfull = reinterpret_cast<uint64_t*>(smem + a.bar_off);
+    uint64_t* wempty = wfull + kMaxWStages;
+    uint64_t* xfull = wempty + kMaxWStages;
+    uint64_t* xempty = xfull + kXStages;
+    uint64_t* tfull = xempty + kXStages;  // every MMA done
+    uint64_t* drain = tfull + 1;
+    uint64_t* drain2 = drain + 1;  // the second issuer's in-flight MMAs
+    uint64_t* scbar = drain2 + 1;         // MXFP8: every scale word is in TMEM
+    unsigned long long* epoch_s = reinterpret_cast<unsigned long long*>(scbar + 1);
+    uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(epoch_s + 1);
     int* abort_flag = reinterpret_cast<int*>(tmem_slot + 1);
-    float* gate_s = reinterpret_cast<float*>(abort_flag + 2);  // [kWarps] gates of a row batch
     const volatile int* abort_v = abort_flag;
 
     const int tid = threadIdx.x;
     const int warp = tid >> 5;
     const int lane = tid & 31;
     const int G = gridDim.x;
-    const int HR = a.T * a.H;  // (token, hc) rows of the output
-    const int c_lo = first_granule(blockIdx.x, a.granules, G) * 16;  // this CTA's slice
-    const int c_hi = first_granule(blockIdx.x + 1, a.granules, G) * 16;
-    const int width = c_hi - c_lo;  // a multiple of 16, at most kMaxFusedSlice
+    const int c = blockIdx.x;
+    // this CTA's columns: value dims [v0, v0 + vlen), key columns [k0, k0 + klen)
+    const int g0 = first_granule(c, a.NG, G), g1 = first_granule(c + 1, a.NG, G);
+    const int vg0 = first_granule(c, a.VG, G), vg1 = first_granule(c + 1, a.VG, G);
+    const int v0 = vg0 * 16, vlen = (vg1 - vg0) * 16;
+    const int k0 = (g0 - vg0) * 16, klen = ((g1 - vg1) - (g0 - vg0)) * 16;
+    const int width = vlen + klen;  // a multiple of 16, at most kMaxFusedSlice
+    const int c_lo = g0 * 16;       // first packed row
     const uint32_t w_bytes = static_cast<uint32_t>(width) * 128u;
 
+    // Gather item i of this CTA (a 16-byte chunk of a hash row; MXFP8: a
+    // 32-k block, four chunks): the id, then the row.  Each gathering
+    // thread fetches its first item before the CTA-wide setup below, so the
+    // dependent id -> row loads overlap it.
+    const int nrows_g = a.T * a.C;
+    const int g_r0 = static_cast<int>(static_cast<int64_t>(c) * nrows_g / G);
+    const int g_r1 = static_cast<int>(static_cast<int64_t>(c + 1) * nrows_g / G);
+    const int g_per = kMx ? (a.E >> 5) : (a.E >> 3);  // items per hash row
+    const int g_n = a.gather ? (g_r1 - g_r0) * g_per : 0;
+    auto fetch = [&](int i, uint4 (&v)[4]) -> bool {
+        const int rr = g_r0 + i / g_per, b = i - (i / g_per) * g_per;
+        const int t = rr / a.C, cc = rr - t * a.C;
+        const int64_t id = a.ids[t * a.ids_stride + cc];
+        const bool good = id >= 0 && id < __ldg(a.rows + cc);
+        const uint16_t* src = a.table + (__ldg(a.row_offset + cc) + (good ? id : 0)) * a.E +
+                              b * (kMx ? 32 : 8);
+#pragma unroll
+        for (int j = 0; j < (kMx ? 4 : 1); ++j)
+            v[j] = good ? ld_stream_v4(src + j * 8) : make_uint4(0u, 0u, 0u, 0u);
+        return good;
+    };
+    uint4 pre[4] = {};
+    bool pre_good = true;
+    if (warp >= 2 && warp < 6 && tid - 64 < g_n) pre_good = fetch(tid - 64, pre);
+
     if (tid == 0) {
-        for (int s = 0; s < a.stages; ++s) {
-            mbar_init(&full[s], 1);
-            mbar_init(&empty[s], 1);
+        for (int s = 0; s < a.w_stages; ++s) {
+            mbar_init(&wfull[s], 1);
+            mbar_init(&wempty[s], 1);
         }
-        mbar_init(tfull, 1);
-        mbar_init(hbar, 1);
-        mbar_init(fbar, 1);
+        for (int s = 0; s < kXStages; ++s) {
+            mbar_init(&xfull[s], 64);  // one cp.async arrival per loading thread
+            mbar_init(&xempty[s], 1);
+        }
+        mbar_init(tfull, a.dual ? 2 : 1);  // one commit per issuer
         mbar_init(drain, 1);
+        mbar_init(drain2, 1);
         mbar_init(scbar, 128);
         *abort_flag = 0;
+        // this launch's epoch: stable until CTA 0 advances it at the end
+        *epoch_s = *reinterpret_cast<volatile unsigned long long*>(a.bar) + 1ull;
         fence_barrier_init();
-        tma_prefetch_desc(&tm_x);
     }
-    // generation of the gather barrier, read before this CTA can arrive at it
-    const unsigned gather_gen = (a.gather && tid == 0) ? ld_acquire_u32(a.bar + 1) : 0u;
+    int w_issued = 0;
+    const uint64_t pol_w = policy_evict_first();
+    const uint8_t* w_src = a.wpack + static_cast<int64_t>(c_lo) * 128;
+    const int64_t w_kstep = static_cast<int64_t>(a.N) * 128;
+    if (tid == 0) {
+        // the first ring of weight stages needs no free slot: issue it now
+        for (; w_issued < a.w_stages && w_issued < a.k_blocks; ++w_issued) {
+            mbar_arrive_expect_tx(&wfull[w_issued], w_bytes);
+            bulk_load_hint(smem + w_issued * a.w_stage_bytes, w_src, w_bytes, &wfull[w_issued],
+                           pol_w);
+            w_src += w_kstep;
+        }
+    }
     if (warp == 1) {
-        tmem_alloc(tmem_slot, 512);
+        tmem_alloc(tmem_slot, kTmemCols);
         tmem_relinquish();
     }
     tc_fence_before();
     __syncthreads();
     tc_fence_after();
     const uint32_t tmem_base = *tmem_slot;
+    const unsigned long long target = *epoch_s * static_cast<unsigned long long>(G);
     // MXFP8 scale cells, 8 columns per k-block each (every region 8-aligned)
     const uint32_t tm_sfa = tmem_base + kMaxFusedSlice;                     // tokens
     const uint32_t tm_sfb = tm_sfa + 8u * static_cast<uint32_t>(a.kb128);  // weights
 
-    int issued = 0;
     if (warp == 0) {
         if (lane == 0) {
-            // hidden rows of this CTA's share of the finish, while weights stream
-            int nh = 0;
-            for (int r = blockIdx.x; r < HR && nh < static_cast<int>(a.hid_rows); r += G) ++nh;
-            if (nh > 0) {
-                mbar_arrive_expect_tx(hbar, static_cast<uint32_t>(nh * a.D * 2));
-                int i = 0;
-                for (int r = blockIdx.x; r < HR && i < nh; r += G, ++i) {
-                    const int t = r / a.H, h = r - t * a.H;
-                    bulk_load(hid_s + static_cast<int64_t>(i) * a.D,
-                              a.hidden + t * a.hs_t + h * a.hs_h, static_cast<uint32_t>(a.D * 2),
-                              hbar);
-                }
-            } else {
-                mbar_arrive(hbar);
-            }
-            const uint64_t pol_w = policy_evict_first();
-            // token tiles wait for the staged rows (the first grid barrier);
-            // the weight slices of the first stages go out at once
-            bool have_rows = !a.gather;
-            auto issue_x = [&](int s, int kb) {
-                uint8_t* sx = smem + s * stage_bytes + a.w_stage_bytes;
-                for (int m = 0; m < a.mtiles; ++m)
-                    tma_load_2d(sx + m * 16384, &tm_x, &full[s], kb * kKElems, m * 128);
-            };
-            auto await_rows = [&]() -> bool {
-                const uint64_t t0 = globaltimer_ns();
-                uint32_t spins = 0;
-                while (ld_acquire_u32(a.bar + 1) == gather_gen) {
-                    if ((++spins & 63u) == 0 &&
-                        (*abort_v || globaltimer_ns() - t0 > kWaitLimitNs || spins > kWaitLimitIters))
-                        return false;
-                }
-                fence_proxy_async();  // the staged rows were written by ordinary stores
-                for (int j = 0; j < issued; ++j) issue_x(j % a.stages, j);
-                have_rows = true;
-                return true;
-            };
+            // the rest of the weight slice, a stage as soon as its MMAs are done
             bool ok = true;
-            for (int kb = 0; kb < a.k_blocks && ok; ++kb) {
-                if (!have_rows && issued == a.stages && !await_rows()) {
+            int s = 0;
+            uint32_t par = 1;  // the second use of each stage
+            for (int kb = w_issued; kb < a.k_blocks; ++kb) {
+                if (!mbar_wait_sleep(&wempty[s], par ^ 1u, abort_v, 128)) {
                     ok = false;
                     break;
                 }
-                const int s = issued % a.stages;
-                const uint32_t par = static_cast<uint32_t>((issued / a.stages) & 1);
-                if (!mbar_wait(&empty[s], par ^ 1u, abort_v)) {
-                    ok = false;
-                    break;
+                mbar_arrive_expect_tx(&wfull[s], w_bytes);
+                bulk_load_hint(smem + s * a.w_stage_bytes, w_src, w_bytes, &wfull[s], pol_w);
+                w_src += w_kstep;
+                ++w_issued;
+                if (++s == a.w_stages) {
+                    s = 0;
+                    par ^= 1u;
                 }
-                mbar_arrive_expect_tx(&full[s], w_bytes + a.x_bytes);
-                bulk_load_hint(smem + s * stage_bytes,
-                               a.wpack + (static_cast<int64_t>(kb) * a.N + c_lo) * 128, w_bytes,
-                               &full[s], pol_w);
-                if (have_rows) issue_x(s, kb);
-                ++issued;
             }
-            if (ok && !have_rows && !await_rows()) ok = false;
             if (!ok) fail(abort_flag, a.err);
         }
-    } else if (warp == 1) {
+    } else if (warp == 1 || (warp == 6 && a.dual)) {
         if (lane == 0) {
+            // An issuing thread's dependent scalar work
+            // sets the pace: stage indices, phase parities and shared-memory
+            // descriptors advance incrementally (a descriptor's address field
+            // is the byte address / 16), and each k-block's MMAs are unrolled.
             const uint32_t idesc = idesc_bf16(128, width);
+            uint32_t idm[4];
+#pragma unroll
+            for (int k = 0; k < 4; ++k) idm[k] = idesc_mxf8(128, width, k, k);
+            const uint64_t wdesc0 = smem_desc_sw128(smem_addr(smem));
+            const uint64_t xdesc0 = smem_desc_sw128(smem_addr(xring));
+            const uint64_t wstep = a.w_stage_bytes >> 4, xstep = a.x_stage_bytes >> 4;
+            const bool two_tiles = a.mtiles == 2;
             bool ok = true;
             if constexpr (kMx) {
                 ok = mbar_wait(scbar, 0, abort_v);
                 tc_fence_after();
             }
-            for (int kb = 0; kb < a.k_blocks && ok; ++kb) {
-                const int s = kb % a.stages;
-                if (!mbar_wait(&full[s], static_cast<uint32_t>((kb / a.stages) & 1), abort_v)) {
+            // this issuer's k-blocks and accumulator
+            const int kstep = a.dual ? 2 : 1;
+            const int kb0 = warp == 6 ? 1 : 0;
+            const uint32_t dacc = tmem_base + (warp == 6 ? 256u : 0u);
+            int sw = 0, sx = 0;
+            uint32_t pw = 0, px = 0, acc = 0;
+            uint64_t wd = wdesc0, xd = xdesc0;
+            uint32_t sfa = tm_sfa, sfb = tm_sfb;
+            auto advance = [&]() {
+                if (++sw == a.w_stages) {
+                    sw = 0;
+                    pw ^= 1u;
+                    wd = wdesc0;
+                } else {
+                    wd += wstep;
+                }
+                if (++sx == kXStages) {
+                    sx = 0;
+                    px ^= 1u;
+                    xd = xdesc0;
+                } else {
+                    xd += xstep;
+                }
+            };
+            if (kb0 == 1) advance();
+            for (int kb = kb0; kb < a.k_blocks && ok; kb += kstep) {
+                if (!mbar_wait(&wfull[sw], pw, abort_v) || !mbar_wait(&xfull[sx], px, abort_v)) {
                     ok = false;
                     break;
                 }
+                fence_proxy_async_smem();  // token tiles were written by cp.async (generic proxy)
                 tc_fence_after();
-                const uint32_t sw = smem_addr(smem + s * stage_bytes);
-                const uint64_t wdesc = smem_desc_sw128(sw);
                 if constexpr (kMx) {
-                    const uint64_t xdesc = smem_desc_sw128(sw + a.w_stage_bytes);
-#pragma unroll
-                    for (int k = 0; k < 4; ++k)  // 4 x K32, scale byte k of each cell
-                        mma_mxf8_ss(tmem_base, xdesc + 2 * k, wdesc + 2 * k,
-                                    idesc_mxf8(128, width, k, k),
-                                    tm_sfa + 8u * static_cast<uint32_t>(kb),
-                                    tm_sfb + 8u * static_cast<uint32_t>(kb),
-                                    (kb > 0 || k > 0) ? 1u : 0u);
+                    // 4 x K32, scale byte k of each cell
+                    mma_mxf8_ss(tmem_base, xd, wd, idm[0], sfa, sfb, acc);
+                    mma_mxf8_ss(tmem_base, xd + 2, wd + 2, idm[1], sfa, sfb, 1u);
+                    mma_mxf8_ss(tmem_base, xd + 4, wd + 4, idm[2], sfa, sfb, 1u);
+                    mma_mxf8_ss(tmem_base, xd + 6, wd + 6, idm[3], sfa, sfb, 1u);
+                    sfa += 8u;
+                    sfb += 8u;
                 } else {
+                    // 4 x K16; the second 128-token tile 16 KB on
+                    mma_bf16_ss(dacc, xd, wd, idesc, acc);
+                    if (two_tiles) mma_bf16_ss(tmem_base + kMaxFusedSlice, xd + 1024, wd, idesc, acc);
 #pragma unroll
-                    for (int k = 0; k < 4; ++k)
-                        for (int m = 0; m < a.mtiles; ++m)
-                            mma_bf16_ss(tmem_base + static_cast<uint32_t>(m * kMaxFusedSlice),
-                                        smem_desc_sw128(sw + a.w_stage_bytes + m * 16384) + 2 * k,
-                                        wdesc + 2 * k, idesc, (kb > 0 || k > 0) ? 1u : 0u);
+                    for (int k = 1; k < 4; ++k) {
+                        mma_bf16_ss(dacc, xd + 2 * k, wd + 2 * k, idesc, 1u);
+                        if (two_tiles)
+                            mma_bf16_ss(tmem_base + kMaxFusedSlice, xd + 1024 + 2 * k, wd + 2 * k,
+                                        idesc, 1u);
+                    }
                 }
-                mma_commit(&empty[s]);
+                acc = 1u;
+                mma_commit(&wempty[sw]);
+                mma_commit(&xempty[sx]);
+                advance();
+                if (kstep == 2) advance();  // skip the other issuer's k-block
             }
             if (ok) mma_commit(tfull);
             if (!ok) fail(abort_flag, a.err);
         }
-    } else {
-        const int etid = tid - 64;  // 0..127
+    } else if (warp < 6) {
+        const int etid = tid - 64;  // 0..127 (warps 2-5; warp 6 idles unless it issues MMAs)
         const int q = warp & 3;     // TMEM lane quarter of this warp
         const uint32_t lane_base = static_cast<uint32_t>(q * 32) << 16;
         if constexpr (kMx) {
-            // weight scales of the slice: B row n (slice column n) in lane
-            // n % 32, column tm_sfb + 8 kb + n / 32; every lane quarter gets
+            // weight scales of the slice: B row j (slice column j) in lane
+            // j % 32, column tm_sfb + 8 kb + j / 32; every lane quarter gets
             // a copy
             for (int kb = 0; kb < a.kb128; ++kb) {
                 uint32_t w[8];
 #pragma unroll
                 for (int jc = 0; jc < 8; ++jc) {
-                    const int n = jc * 32 + lane;
-                    w[jc] = n < width ? __ldg(reinterpret_cast<const uint32_t*>(
-                                            a.wscale + ((c_lo + n) >> 5) * (a.K >> 5) + kb * 4))
+                    const int j = jc * 32 + lane;
+                    const int n = j < vlen ? a.H * a.D + v0 + j : k0 + (j - vlen);
+                    w[jc] = j < width ? __ldg(reinterpret_cast<const uint32_t*>(
+                                            a.wscale + (n >> 5) * (a.K >> 5) + kb * 4))
                                       : 0x7F7F7F7Fu;
                 }
                 const uint32_t col = tm_sfb + lane_base + 8u * static_cast<uint32_t>(kb);
@@ -308,99 +364,130 @@ __global__ void __launch_bounds__(kThreads, 1)
             }
         }
         // This CTA's share of the hash rows -> the staged-rows buffer
-        // (ParallelEngramEmbedding.lookup), then the first grid barrier.
-        if (a.gather && kMx) {
-            // one thread per 32-k block of a hash row: the bf16 row, its
-            // e4m3 codes and its scale
-            const int bpr = a.E >> 5;
-            const int nrows = a.T * a.C;
-            const int r0 = static_cast<int>(static_cast<int64_t>(blockIdx.x) * nrows / G);
-            const int r1 = static_cast<int>(static_cast<int64_t>(blockIdx.x + 1) * nrows / G);
+        // (ParallelEngramEmbedding.lookup); MXFP8: also their e4m3 codes and
+        // scales.  Every CTA's token tiles need every row: grid barrier 1.
+        if (a.gather) {
             bool bad = false;
-            for (int i = etid; i < (r1 - r0) * bpr; i += 128) {
-                const int rr = r0 + i / bpr, b = i - (i / bpr) * bpr;
-                const int t = rr / a.C, c = rr - t * a.C;
-                const int64_t id = a.ids[t * a.ids_stride + c];
+            for (int i = etid; i < g_n; i += 128) {
                 uint4 v[4];
-                if (id >= 0 && id < __ldg(a.rows + c)) {
-                    const uint16_t* src = a.table + (__ldg(a.row_offset + c) + id) * a.E + b * 32;
+                bool good;
+                if (i == etid) {
 #pragma unroll
-                    for (int j = 0; j < 4; ++j) v[j] = ld_stream_v4(src + j * 8);
+                    for (int j = 0; j < 4; ++j) v[j] = pre[j];
+                    good = pre_good;
                 } else {
-#pragma unroll
-                    for (int j = 0; j < 4; ++j) v[j] = make_uint4(0u, 0u, 0u, 0u);
-                    bad = true;
+                    good = fetch(i, v);
                 }
-                const int64_t k0 = static_cast<int64_t>(rr) * a.E + b * 32;  // = t*K + c*E + 32b
+                bad |= !good;
+                const int rr = g_r0 + i / g_per, b = i - (i / g_per) * g_per;
+                if constexpr (kMx) {
+                    const int t = rr / a.C, cc = rr - t * a.C;
+                    const int64_t k0r = static_cast<int64_t>(rr) * a.E + b * 32;  // t*K + c*E + 32b
 #pragma unroll
-                for (int j = 0; j < 4; ++j) st_v4(a.staged + k0 + j * 8, v[j]);
-                uint4 cq[2];
-                const uint32_t sb = mx_quantize32(v, cq);
-                st_v4(a.staged_q + k0, cq[0]);
-                st_v4(a.staged_q + k0 + 16, cq[1]);
-                a.staged_s[sf_atom_offset(t, (c * a.E + b * 32) >> 5, a.kb128)] =
-                    static_cast<uint8_t>(sb);
+                    for (int j = 0; j < 4; ++j) st_v4(a.staged + k0r + j * 8, v[j]);
+                    uint4 cq[2];
+                    const uint32_t sb = mx_quantize32(v, cq);
+                    st_v4(a.staged_q + k0r, cq[0]);
+                    st_v4(a.staged_q + k0r + 16, cq[1]);
+                    a.staged_s[sf_atom_offset(t, (cc * a.E + b * 32) >> 5, a.kb128)] =
+                        static_cast<uint8_t>(sb);
+                } else {
+                    st_v4(a.staged + static_cast<int64_t>(rr) * a.E + b * 8, v[0]);
+                }
             }
             if (bad) atomicOr(a.err, ENGRAM_DEVERR_BAD_HASH_ID);
-            __threadfence();
-            named_barrier_sync(1, 128);
-            if (etid == 0 && !grid_barrier(a.bar, static_cast<unsigned>(G))) fail(abort_flag, a.err);
-        } else if (a.gather) {
-            const int cpr = a.E >> 3;  // 16-byte chunks per row
-            const int nrows = a.T * a.C;
-            const int r0 = static_cast<int>(static_cast<int64_t>(blockIdx.x) * nrows / G);
-            const int r1 = static_cast<int>(static_cast<int64_t>(blockIdx.x + 1) * nrows / G);
-            bool bad = false;
-            for (int q = etid; q < (r1 - r0) * cpr; q += 128) {
-                const int rr = r0 + q / cpr, j = q - (q / cpr) * cpr;
-                const int t = rr / a.C, c = rr - t * a.C;
-                const int64_t id = a.ids[t * a.ids_stride + c];
-                uint4 v = make_uint4(0u, 0u, 0u, 0u);
-                if (id >= 0 && id < __ldg(a.rows + c))
-                    v = ld_stream_v4(a.table + (__ldg(a.row_offset + c) + id) * a.E + j * 8);
-                else
-                    bad = true;
-                st_v4(a.staged + static_cast<int64_t>(rr) * a.E + j * 8, v);
-            }
-            if (bad) atomicOr(a.err, ENGRAM_DEVERR_BAD_HASH_ID);
-            __threadfence();
-            named_barrier_sync(1, 128);
-            if (etid == 0 && !grid_barrier(a.bar, static_cast<unsigned>(G))) fail(abort_flag, a.err);
         }
-        // q*k of the slice's key columns (q*k is [H][D], i.e. columns [0, H*D))
-        for (int c = etid; c < width; c += 128) {
-            const int n = c_lo + c;
-            qk_s[c] = n < a.H * a.D ? __ldg(a.qk + n) : 0.f;
+        // grid barrier 1 (the counter advances on every launch, gather or not)
+        named_barrier_sync(1, 128);
+        if (etid == 0) {
+            grid_arrive(a.bar + 1);
+            if (a.gather && !grid_wait(a.bar + 1, target)) fail(abort_flag, a.err);
         }
-        named_barrier_sync(1, 128);  // qk_s complete; the gather barrier has passed
-        if constexpr (kMx) {
-            // token scales: A row r = token t in lane t, column
-            // tm_sfa + 8 kb + t / 32 (written to all four columns)
-            const int t = q * 32 + lane;
-            for (int kb = 0; kb < a.kb128; ++kb) {
-                const uint32_t w = __ldcg(reinterpret_cast<const unsigned*>(
-                    a.staged_s + sf_atom_offset(t, 4 * kb, a.kb128)));
-                tmem_st4(tm_sfa + lane_base + 8u * static_cast<uint32_t>(kb), w, w, w, w);
+        // q*k of the slice's key columns
+        for (int j = etid; j < klen; j += 128) qk_s[j] = __ldg(a.qk + k0 + j);
+        named_barrier_sync(1, 128);  // qk_s complete; grid barrier 1 has passed
+        // Token tiles: k-block kb of every token row into stage kb % kXStages,
+        // row r at 128 * r (second 128-row tile 16 KB on), 16-byte chunk j at
+        // position j ^ (r % 8): the 128-byte swizzle the MMA descriptors
+        // expect.  Rows past T hold whatever is staged there; their
+        // accumulator rows are never used.  (MXFP8: the token scales go to
+        // TMEM once the first tiles are on their way.)
+        {
+            // MXFP8 token scales: A row r = token t in lane t, column
+            // tm_sfa + 8 kb + t / 32 (written to all four columns); needed
+            // before the first MMA, written once the first tiles are in flight
+            constexpr int kMaxKb128 = 16;  // (TMEM budget: 256 + 16 * K/128 <= 512)
+            uint32_t sfw[kMaxKb128];
+            if constexpr (kMx) {  // loads first; the TMEM stores wait for the first tiles
+                const int t = q * 32 + lane;
+#pragma unroll
+                for (int b = 0; b < kMaxKb128; ++b)
+                    sfw[b] = b < a.kb128 ? __ldcg(reinterpret_cast<const unsigned*>(
+                                               a.staged_s + sf_atom_offset(t, 4 * b, a.kb128)))
+                                         : 0u;
             }
-            tmem_st_wait();
-            tc_fence_before();
-            mbar_arrive(scbar);
+            auto token_scales = [&]() {
+#pragma unroll
+                for (int b = 0; b < kMaxKb128; ++b)
+                    if (b < a.kb128)
+                        tmem_st4(tm_sfa + lane_base + 8u * static_cast<uint32_t>(b), sfw[b],
+                                 sfw[b], sfw[b], sfw[b]);
+                tmem_st_wait();
+                tc_fence_before();
+                mbar_arrive(scbar);
+            };
+            const int chunks = a.Tn * 8;
+            constexpr int kLoaders = 64;  // warps 2-3
+            const int kb_first = a.k_blocks < 2 ? a.k_blocks : 2;  // tiles before the scales
+            bool ok = true;
+            for (int kb = 0; kb < a.k_blocks; ++kb) {
+                // (a stage is reused only after the MMAs, which need the scales)
+                if (kb == kb_first) {
+                    if (kMx) token_scales();  // all four epilogue warps
+                    if (etid >= kLoaders) break;  // warps 4-5 are done
+                }
+                if (etid >= kLoaders) continue;
+                const int s = kb % kXStages;
+                if (!mbar_wait_sleep(&xempty[s], static_cast<uint32_t>((kb / kXStages) & 1) ^ 1u,
+                                     abort_v, 64)) {
+                    ok = false;
+                    break;
+                }
+                uint8_t* xs = xring + s * a.x_stage_bytes;
+                for (int i = etid; i < chunks; i += kLoaders) {
+                    const int r = i >> 3, j = i & 7;
+                    const uint32_t dst =
+                        smem_addr(xs + (r >> 7) * 16384 + (r & 127) * 128 + ((j ^ (r & 7)) << 4));
+                    const void* src =
+                        kMx ? static_cast<const void*>(a.staged_q + static_cast<int64_t>(r) * a.K +
+                                                       kb * 128 + j * 16)
+                            : static_cast<const void*>(a.staged + static_cast<int64_t>(r) * a.K +
+                                                       kb * 64 + j * 8);
+                    cp_async16(dst, src, 16);
+                }
+                cp_async_mbar_arrive(&xfull[s]);
+            }
+            if (kMx && a.k_blocks == kb_first) token_scales();  // (K of at most 2 blocks)
+            cp_async_wait_all();
+            if (!ok) fail(abort_flag, a.err);
+            // warps 4-5 sleep here (no polling) until the loaders are through
+            named_barrier_sync(2, 128);
         }
 
-        // Epilogue: thread = one token of an accumulator (TMEM lane quarter
-        // = warp % 4), columns = the slice.
-        const int h0 = c_lo / a.D;  // the slice covers hc copies h0 and possibly h0 + 1
+        // Epilogue: thread = one token of an accumulator, key columns of the
+        // slice -> one record per (hc copy, token).
+        const int h0 = k0 / a.D;  // the key run covers copies h0 and possibly h0 + 1
         bool go = true;
         for (int m = 0; m < a.mtiles && go; ++m) {
             const int t = m * 128 + q * 32 + lane;
             const bool live = t < a.T;
-            // this token's hidden columns of the slice, before the accumulator is ready
-            uint4 hv[2 * kSliceChunks];
+            // this token's hidden at the key columns, before the accumulator is ready
+            uint4 hv[2 * kKeyChunks];
 #pragma unroll
-            for (int ci = 0; ci < kSliceChunks; ++ci) {
-                const int n0 = c_lo + ci * 16;
+            for (int ci = 0; ci < kKeyChunks; ++ci) {
                 hv[2 * ci] = hv[2 * ci + 1] = make_uint4(0u, 0u, 0u, 0u);
-                if (live && ci * 16 < width && n0 < a.H * a.D) {
+                if (live && ci * 16 < klen) {
+                    const int n0 = k0 + ci * 16;
                     const int h = n0 / a.D, d0 = n0 - h * a.D;
                     const uint16_t* hp = a.hidden + t * a.hs_t + h * a.hs_h + d0;
                     hv[2 * ci] = ld_nc_v4(hp);
@@ -408,7 +495,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                 }
             }
             if (m == 0) {
-                const bool bad = !mbar_wait(tfull, 0, abort_v);
+                const bool bad = !mbar_wait_sleep(tfull, 0, abort_v, 128);
                 // all four epilogue warps decide together
                 if (named_barrier_or(1, 128, bad || *abort_v)) {
                     if (bad) fail(abort_flag, a.err);
@@ -418,139 +505,122 @@ __global__ void __launch_bounds__(kThreads, 1)
                 tc_fence_after();
             }
             float acc[2][3] = {{0.f, 0.f, 0.f}, {0.f, 0.f, 0.f}};
-            const uint32_t taddr = tmem_base + (static_cast<uint32_t>(q * 32) << 16) +
-                                   static_cast<uint32_t>(m * kMaxFusedSlice);
+            const uint32_t taddr =
+                tmem_base + lane_base + static_cast<uint32_t>(m * kMaxFusedSlice + vlen);
 #pragma unroll
-            for (int ci = 0; ci < kSliceChunks; ++ci) {
-                if (ci * 16 >= width) break;
+            for (int ci = 0; ci < kKeyChunks; ++ci) {
+                if (ci * 16 >= klen) break;
                 uint32_t r[16];
                 tmem_ld16(taddr + static_cast<uint32_t>(ci * 16), r);
-                tmem_ld_wait();
-                if (!live) continue;
-                const int n0 = c_lo + ci * 16;  // 16 columns never straddle an hc copy
-                const int h = n0 / a.D, d0 = n0 - h * a.D;
-                if (h < a.H) {
-                    const uint32_t w[8] = {hv[2 * ci].x,     hv[2 * ci].y,     hv[2 * ci].z,
-                                           hv[2 * ci].w,     hv[2 * ci + 1].x, hv[2 * ci + 1].y,
-                                           hv[2 * ci + 1].z, hv[2 * ci + 1].w};
-                    float shh = 0.f, skk = 0.f, shk = 0.f;
+                if (a.dual) {
+                    uint32_t r2[16];
+                    tmem_ld16(taddr + 256u + static_cast<uint32_t>(ci * 16), r2);
+                    tmem_ld_wait();
 #pragma unroll
-                    for (int e = 0; e < 16; ++e) {
-                        const float x = (e & 1) ? bf16hi(w[e >> 1]) : bf16lo(w[e >> 1]);
-                        const float key = __uint_as_float(r[e]);
-                        shh = fmaf(x, x, shh);
-                        skk = fmaf(key, key, skk);
-                        shk = fmaf(x * qk_s[ci * 16 + e], key, shk);
-                    }
-                    const int hi = h - h0;
-                    acc[hi][0] += shh;
-                    acc[hi][1] += skk;
-                    acc[hi][2] += shk;
-                } else {
-                    float4* vp =
-                        reinterpret_cast<float4*>(a.value + static_cast<int64_t>(t) * a.D + d0);
-#pragma unroll
-                    for (int e = 0; e < 4; ++e)
-                        vp[e] = make_float4(__uint_as_float(r[4 * e]), __uint_as_float(r[4 * e + 1]),
-                                            __uint_as_float(r[4 * e + 2]),
-                                            __uint_as_float(r[4 * e + 3]));
+                    for (int e = 0; e < 16; ++e)
+                        r[e] = __float_as_uint(__uint_as_float(r[e]) + __uint_as_float(r2[e]));
                 }
+                tmem_ld_wait();
+                const int n0 = k0 + ci * 16;  // 16 columns never straddle an hc copy
+                const int hi = n0 / a.D - h0;
+                const uint32_t w[8] = {hv[2 * ci].x,     hv[2 * ci].y,     hv[2 * ci].z,
+                                       hv[2 * ci].w,     hv[2 * ci + 1].x, hv[2 * ci + 1].y,
+                                       hv[2 * ci + 1].z, hv[2 * ci + 1].w};
+                float shh = 0.f, skk = 0.f, shk = 0.f;
+#pragma unroll
+                for (int e = 0; e < 16; ++e) {
+                    const float x = (e & 1) ? bf16hi(w[e >> 1]) : bf16lo(w[e >> 1]);
+                    const float key = __uint_as_float(r[e]);
+                    shh = fmaf(x, x, shh);
+                    skk = fmaf(key, key, skk);
+                    shk = fmaf(x * qk_s[ci * 16 + e], key, shk);
+                }
+                acc[hi][0] += shh;
+                acc[hi][1] += skk;
+                acc[hi][2] += shk;
             }
             if (live) {
-                float4* pp = reinterpret_cast<float4*>(
-                    a.part + (static_cast<int64_t>(t) * G + blockIdx.x) * kPartFloats);
-                pp[0] = make_float4(acc[0][0], acc[0][1], acc[0][2], 0.f);
-                pp[1] = make_float4(acc[1][0], acc[1][1], acc[1][2], 0.f);
+                // a record for every copy whose CTA range includes this CTA
+                // (zeros where it holds none of the copy's keys)
+                const int hl = klen > 0 ? (k0 + klen - 1) / a.D : -1;  // last copy of the run
+                for (int h = 0; h < a.H; ++h) {
+                    if (c < a.cf[h] || c >= a.cf[h] + a.nh[h]) continue;
+                    const bool has = h >= h0 && h <= hl;
+                    a.rec[a.rec_base[h] + t * a.nh[h] + (c - a.cf[h])] =
+                        has ? make_float4(acc[h - h0][0], acc[h - h0][1], acc[h - h0][2], 0.f)
+                            : make_float4(0.f, 0.f, 0.f, 0.f);
+                }
             }
+            if (a.value != nullptr) {
+                // validation: the fp32 value of this CTA's dims
+                for (int ci = 0; ci * 16 < vlen; ++ci) {
+                    uint32_t r[16];
+                    const uint32_t va =
+                        tmem_base + lane_base + static_cast<uint32_t>(m * kMaxFusedSlice + ci * 16);
+                    tmem_ld16(va, r);
+                    if (a.dual) {
+                        uint32_t r2[16];
+                        tmem_ld16(va + 256u, r2);
+                        tmem_ld_wait();
+#pragma unroll
+                        for (int e = 0; e < 16; ++e)
+                            r[e] = __float_as_uint(__uint_as_float(r[e]) + __uint_as_float(r2[e]));
+                    }
+                    tmem_ld_wait();
+                    if (live) {
+                        float4* vp = reinterpret_cast<float4*>(
+                            a.value + static_cast<int64_t>(t) * a.D + v0 + ci * 16);
+#pragma unroll
+                        for (int e = 0; e < 4; ++e)
+                            vp[e] = make_float4(__uint_as_float(r[4 * e]),
+                                                __uint_as_float(r[4 * e + 1]),
+                                                __uint_as_float(r[4 * e + 2]),
+                                                __uint_as_float(r[4 * e + 3]));
+                    }
+                }
+            }
+            // the residual reads hidden at the value dims: start it towards L2
+            // (plain per-line prefetches; bulk ones would queue on the TMA unit)
+            if (live && vlen > 0)
+                for (int h = 0; h < a.H; ++h) {
+                    const uint16_t* hp = a.hidden + t * a.hs_t + h * a.hs_h + v0;
+                    prefetch_line_l2(hp);
+                    prefetch_line_l2(hp + vlen - 1);
+                }
         }
-        // every partial sum and value this CTA owes is written
-        __threadfence();
+        // every record this CTA owes is written: grid barrier 2 (the release
+        // add of one thread covers the CTA's writes ordered before it by the
+        // named barrier)
         named_barrier_sync(1, 128);
-        if (etid == 0 && !grid_barrier(a.bar + 2, static_cast<unsigned>(G))) fail(abort_flag, a.err);
+        if (etid == 0) {
+            grid_arrive(a.bar + 2);
+            if (!grid_wait(a.bar + 2, target)) fail(abort_flag, a.err);
+        }
     }
 
     __syncwarp();
     tc_fence_before();
     __syncthreads();
-    if (*abort_v) {
-        // let in-flight copies and MMAs land before shared memory and TMEM go
-        if (tid == 0) {
-            const int first = issued > a.stages ? issued - a.stages : 0;
-            for (int j = first; j < issued; ++j)
-                mbar_wait(&full[j % a.stages], static_cast<uint32_t>((j / a.stages) & 1), nullptr);
-        }
-        if (tid == 32) {
-            mma_commit(drain);
-            mbar_wait(drain, 0, nullptr);
-        }
-    }
-    // the hidden rows were bulk-copied at the start; they must have landed
-    if (!mbar_wait(hbar, 0, nullptr) && lane == 0) fail(abort_flag, a.err);
-    __syncthreads();
-    tc_fence_after();
-    if (warp == 1) tmem_dealloc(tmem_base, 512);
-    if (*abort_v) return;
-
-    // Finish.  Rows of this CTA: r = blockIdx.x + i * G.  Lane i of warp 0
-    // copies row i's value row and the partial records of the CTAs covering
-    // its hc copy into the (idle) stage buffers.
-    const int nchunk = a.D >> 3;
-    float* fin = reinterpret_cast<float*>(smem);  // per row: [D value][G records]
-    const int64_t per_row = a.D + static_cast<int64_t>(G) * kPartFloats;
-    int nrows = 0;
-    for (int r = blockIdx.x; r < HR; r += G) ++nrows;
-    if (warp == 0 && nrows > 0) {
-        uint32_t bytes = 0;
-        int t = 0, h = 0, cf = 0, cl = 0;
-        const bool mine = lane < nrows;
-        if (mine) {
-            const int r = blockIdx.x + lane * G;
-            t = r / a.H;
-            h = r - t * a.H;
-            cf = owner(h * a.D / 16, a.granules, G);
-            cl = owner(((h + 1) * a.D - 1) / 16, a.granules, G);
-            bytes = static_cast<uint32_t>(a.D * 4 + (cl - cf + 1) * kPartFloats * 4);
-        }
-#pragma unroll
-        for (int off = 16; off > 0; off >>= 1) bytes += __shfl_xor_sync(0xFFFFFFFFu, bytes, off);
-        if (lane == 0) mbar_arrive_expect_tx(fbar, bytes);
-        __syncwarp();
-        if (mine) {
-            fence_proxy_async();  // written by other CTAs, read by bulk copies
-            float* dst = fin + static_cast<int64_t>(lane) * per_row;
-            bulk_load(dst, a.value + static_cast<int64_t>(t) * a.D, static_cast<uint32_t>(a.D * 4),
-                      fbar);
-            bulk_load(dst + a.D + cf * kPartFloats,
-                      a.part + (static_cast<int64_t>(t) * G + cf) * kPartFloats,
-                      static_cast<uint32_t>((cl - cf + 1) * kPartFloats * 4), fbar);
-        }
-    }
-    if (nrows > 0 && !mbar_wait(fbar, 0, nullptr)) {
-        if (lane == 0) fail(abort_flag, a.err);
-    }
-    for (int b0 = 0; b0 < nrows; b0 += kWarps) {
-        // one warp per row: the partial sums of the CTAs covering hc copy h,
-        // lane l taking CTAs cf + l, cf + l + 32, ..., then a shuffle tree
-        const int i = b0 + warp;
-        if (i < nrows) {
-            const int r = blockIdx.x + i * G;
+    if (!*abort_v) {
+        // Gates: CTA c reduces the rows (token, copy) r = c, c + G, ...; one
+        // warp per row, lane l adding the records of the copy's CTAs l,
+        // l + 32, ..., then a shuffle tree (a fixed order); grid barrier 3.
+        const int HR = a.T * a.H;
+        for (int r = c + warp * G; r < HR; r += kWarps * G) {
             const int t = r / a.H, h = r - t * a.H;
-            const float* recs = fin + static_cast<int64_t>(i) * per_row + a.D;
-            const int cf = owner(h * a.D / 16, a.granules, G);
-            const int cl = owner(((h + 1) * a.D - 1) / 16, a.granules, G);
+            const float4* rr = a.rec + a.rec_base[h] + static_cast<int64_t>(t) * a.nh[h];
             float s_hh = 0.f, s_kk = 0.f, s_hk = 0.f;
-            for (int cta = cf + lane; cta <= cl; cta += 32) {
-                const int hfirst = first_granule(cta, a.granules, G) * 16 / a.D;
-                const float* p = recs + cta * kPartFloats + (h == hfirst ? 0 : 4);
-                s_hh += p[0];
-                s_kk += p[1];
-                s_hk += p[2];
+            for (int j = lane; j < a.nh[h]; j += 32) {
+                const float4 v = __ldcg(rr + j);
+                s_hh += v.x;
+                s_kk += v.y;
+                s_hk += v.z;
             }
 #pragma unroll
-            for (int off = 16; off > 0; off >>= 1) {
-                s_hh += __shfl_xor_sync(0xFFFFFFFFu, s_hh, off);
-                s_kk += __shfl_xor_sync(0xFFFFFFFFu, s_kk, off);
-                s_hk += __shfl_xor_sync(0xFFFFFFFFu, s_hk, off);
+            for (int o = 16; o > 0; o >>= 1) {
+                s_hh += __shfl_xor_sync(0xFFFFFFFFu, s_hh, o);
+                s_kk += __shfl_xor_sync(0xFFFFFFFFu, s_kk, o);
+                s_hk += __shfl_xor_sync(0xFFFFFFFFu, s_hk, o);
             }
             if (lane == 0) {
                 const bool active = a.mask == nullptr || a.mask[t] != 0;
@@ -559,87 +629,209 @@ __global__ void __launch_bounds__(kThreads, 1)
                 const float dot = s_hk * hr * kr * a.inv_sqrt_d;
                 float gi = sqrtf(fmaxf(fabsf(dot), a.clamp));
                 if (dot < 0.0f) gi = -gi;
-                const float g = active ? 1.0f / (1.0f + expf(-gi)) : 0.0f;
-                gate_s[warp] = g;
-                a.gate_out[r] = g;
+                a.gate_out[r] = active ? 1.0f / (1.0f + expf(-gi)) : 0.0f;
             }
         }
         __syncthreads();
-        const int nb = nrows - b0 < kWarps ? nrows - b0 : kWarps;
-        for (int w = 0; w < nb; ++w) {
-            const int i2 = b0 + w;
-            const int r = blockIdx.x + i2 * G;
-            const int t = r / a.H, h = r - t * a.H;
-            const bool active = a.mask == nullptr || a.mask[t] != 0;
-            const float g = gate_s[w];
-            const uint16_t* hrow = i2 < static_cast<int>(a.hid_rows)
-                                       ? hid_s + static_cast<int64_t>(i2) * a.D
-                                       : a.hidden + t * a.hs_t + h * a.hs_h;
-            const float* vrow = fin + static_cast<int64_t>(i2) * per_row;
-            uint16_t* orow = a.out + t * a.os_t + h * a.os_h;
-            for (int c = tid; c < nchunk; c += kThreads) {
-                const int d = c * 8;
-                uint4 o = *reinterpret_cast<const uint4*>(hrow + d);
-                if (active) {
-                    const float4 v0 = *reinterpret_cast<const float4*>(vrow + d);
-                    const float4 v1 = *reinterpret_cast<const float4*>(vrow + d + 4);
-                    const uint32_t w4[4] = {o.x, o.y, o.z, o.w};
-                    o.x = pack_bf16x2(fmaf(g, v0.x, bf16lo(w4[0])), fmaf(g, v0.y, bf16hi(w4[0])));
-                    o.y = pack_bf16x2(fmaf(g, v0.z, bf16lo(w4[1])), fmaf(g, v0.w, bf16hi(w4[1])));
-                    o.z = pack_bf16x2(fmaf(g, v1.x, bf16lo(w4[2])), fmaf(g, v1.y, bf16hi(w4[2])));
-                    o.w = pack_bf16x2(fmaf(g, v1.z, bf16lo(w4[3])), fmaf(g, v1.w, bf16hi(w4[3])));
+        if (tid == 0) {
+            grid_arrive(a.bar + 3);
+            if (!grid_wait(a.bar + 3, target)) fail(abort_flag, a.err);
+        }
+        __syncthreads();
+    }
+    if (*abort_v) {
+        // let in-flight copies and MMAs land before shared memory and TMEM go
+        if (tid == 0) {
+            for (int j = w_issued > a.w_stages ? w_issued - a.w_stages : 0; j < w_issued; ++j)
+                mbar_wait(&wfull[j % a.w_stages], static_cast<uint32_t>((j / a.w_stages) & 1),
+                          nullptr);
+        }
+        if (tid == 32) {
+            mma_commit(drain);
+            mbar_wait(drain, 0, nullptr);
+        }
+        if (tid == 192 && a.dual) {
+            mma_commit(drain2);
+            mbar_wait(drain2, 0, nullptr);
+        }
+        __syncthreads();
+        tc_fence_after();
+        if (warp == 1) tmem_dealloc(tmem_base, kTmemCols);
+        return;
+    }
+    tc_fence_after();
+
+    // Residual at this CTA's value dims: thread = token (TMEM lane); the
+    // value comes straight from the accumulator.
+    const int nchunk_v = vlen >> 4;
+    if (warp >= 2 && warp < 6 && nchunk_v > 0) {
+        const int q = warp & 3;
+        const uint32_t lane_base = static_cast<uint32_t>(q * 32) << 16;
+        for (int m = 0; m < a.mtiles; ++m) {
+            if (m * 128 + q * 32 >= a.T) continue;  // warp-uniform: no live token
+            const int t = m * 128 + q * 32 + lane;
+            const bool live = t < a.T;
+            const bool active = live && (a.mask == nullptr || a.mask[t] != 0);
+            float g[kMaxCopies];
+#pragma unroll
+            for (int h = 0; h < kMaxCopies; ++h)
+                g[h] = (active && h < a.H) ? __ldcg(a.gate_out + static_cast<int64_t>(t) * a.H + h)
+                                           : 0.f;
+            for (int ci = 0; ci < nchunk_v; ++ci) {
+                uint32_t r[16];  // every lane loads (tcgen05.ld is warp-wide)
+                const uint32_t va =
+                    tmem_base + lane_base + static_cast<uint32_t>(m * kMaxFusedSlice + ci * 16);
+                tmem_ld16(va, r);
+                if (a.dual) {
+                    uint32_t r2[16];
+                    tmem_ld16(va + 256u, r2);
+                    tmem_ld_wait();
+#pragma unroll
+                    for (int e = 0; e < 16; ++e)
+                        r[e] = __float_as_uint(__uint_as_float(r[e]) + __uint_as_float(r2[e]));
                 }
-                st_v4(orow + d, o);
+                tmem_ld_wait();
+                if (!live) continue;
+                const int d = v0 + ci * 16;
+                uint4 hin[kMaxCopies][2];
+#pragma unroll
+                for (int h = 0; h < kMaxCopies; ++h) {  // all loads before any store (in place)
+                    if (h < a.H) {
+                        const uint16_t* hp = a.hidden + t * a.hs_t + h * a.hs_h + d;
+                        hin[h][0] = ld_nc_v4(hp);
+                        hin[h][1] = ld_nc_v4(hp + 8);
+                    }
+                }
+#pragma unroll
+                for (int h = 0; h < kMaxCopies; ++h) {
+                    if (h >= a.H) continue;
+                    uint4 o0 = hin[h][0], o1 = hin[h][1];
+                    if (active) {
+                        const float gh = g[h];
+                        const uint32_t w0[4] = {o0.x, o0.y, o0.z, o0.w};
+                        const uint32_t w1[4] = {o1.x, o1.y, o1.z, o1.w};
+                        uint32_t p0[4], p1[4];
+#pragma unroll
+                        for (int k = 0; k < 4; ++k) {
+                            p0[k] = pack_bf16x2(fmaf(gh, __uint_as_float(r[2 * k]), bf16lo(w0[k])),
+                                                fmaf(gh, __uint_as_float(r[2 * k + 1]), bf16hi(w0[k])));
+                            p1[k] = pack_bf16x2(
+                                fmaf(gh, __uint_as_float(r[8 + 2 * k]), bf16lo(w1[k])),
+                                fmaf(gh, __uint_as_float(r[8 + 2 * k + 1]), bf16hi(w1[k])));
+                        }
+                        o0 = make_uint4(p0[0], p0[1], p0[2], p0[3]);
+                        o1 = make_uint4(p1[0], p1[1], p1[2], p1[3]);
+                    }
+                    uint16_t* op = a.out + t * a.os_t + h * a.os_h + d;
+                    st_v4(op, o0);
+                    st_v4(op + 8, o1);
+                }
             }
         }
-        __syncthreads();  // gate_s is reused by the next batch
     }
+    // every CTA has read this launch's epoch (it passed barrier 3): advance it
+    if (c == 0 && tid == 0) atomicAdd(a.bar, 1ull);
+    tc_fence_before();
+    __syncthreads();
+    tc_fence_after();
+    if (warp == 1) tmem_dealloc(tmem_base, kTmemCols);
 }
 
-// wkv [N, row_bytes] -> [row_bytes/128][N][128 bytes]: for every 128-byte
-// k-block (64 bf16 or 128 e4m3) the rows are consecutive 128-byte lines,
-// each 8-row group 128-byte swizzled (16-byte chunk j of row n at position
-// j ^ (n % 8)), so any 8-aligned row range of a k-block is a ready
-// shared-memory operand image.
-__global__ void pack_w_kernel(const uint8_t* w, uint8_t* wp, int64_t N, int64_t row_bytes) {
+// wkv [N, row_bytes] -> [row_bytes/128][N][128 bytes] in the fused kernel's
+// column order (each CTA's value rows, then its key rows, CTA after CTA):
+// for every 128-byte k-block (64 bf16 or 128 e4m3) the rows are consecutive
+// 128-byte lines, each 8-row group 128-byte swizzled (16-byte chunk j of
+// packed row p at position j ^ (p % 8)), so a CTA's rows of a k-block are a
+// ready shared-memory operand image.
+__global__ void pack_w_kernel(const uint8_t* w, uint8_t* wp, int64_t N, int64_t row_bytes, int D,
+                              int H, int NG, int VG, int G) {
     const int64_t i = static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x;  // 16-B chunk
     const int64_t cpr = row_bytes / 16;
     if (i >= N * cpr) return;
-    const int64_t n = i / cpr;
-    const int64_t c = i - n * cpr;
-    const int64_t kb = c / 8, j = c % 8;
-    const int64_t dst = (kb * N + n) * 128 + ((j ^ (n & 7)) * 16);
-    *reinterpret_cast<uint4*>(wp + dst) = *reinterpret_cast<const uint4*>(w + i * 16);
+    const int64_t p = i / cpr;  // packed row
+    const int64_t ch = i - p * cpr;
+    const int x = static_cast<int>(p >> 4);                                        // granule
+    const int cta = static_cast<int>((static_cast<int64_t>(x + 1) * G - 1) / NG);  // its owner
+    const int g0 = first_granule(cta, NG, G), vg0 = first_granule(cta, VG, G);
+    const int vlen = (first_granule(cta + 1, VG, G) - vg0) * 16;
+    const int j = static_cast<int>(p - static_cast<int64_t>(g0) * 16);  // slice column
+    const int64_t n = j < vlen ? static_cast<int64_t>(H) * D + vg0 * 16 + j
+                               : static_cast<int64_t>(g0 - vg0) * 16 + (j - vlen);
+    const int64_t kb = ch / 8, jj = ch % 8;
+    const int64_t dst = (kb * N + p) * 128 + ((jj ^ (p & 7)) * 16);
+    *reinterpret_cast<uint4*>(wp + dst) = *reinterpret_cast<const uint4*>(w + n * row_bytes + ch * 16);
 }
 
+int host_first(int cta, int n, int G) { return static_cast<int>(static_cast<int64_t>(cta) * n / G); }
+
 }  // namespace
+
+FusedLayout fused_layout(int64_t N, int64_t D, int64_t H, int num_sms) {
+    FusedLayout L = {};
+    L.NG = static_cast<int>(N / 16);
+    L.VG = static_cast<int>(D / 16);
+    L.grid = num_sms < L.NG ? num_sms : L.NG;
+    L.ok = H >= 1 && H <= kMaxCopies && L.grid >= 1;
+    int last_cta[kMaxCopies];
+    for (int h = 0; h < kMaxCopies; ++h) {
+        L.cf[h] = L.nh[h] = 0;
+        last_cta[h] = -1;
+    }
+    for (int c = 0; c < L.grid && L.ok; ++c) {
+        const int g0 = host_first(c, L.NG, L.grid), g1 = host_first(c + 1, L.NG, L.grid);
+        const int vg0 = host_first(c, L.VG, L.grid), vg1 = host_first(c + 1, L.VG, L.grid);
+        const int kg0 = g0 - vg0, kg1 = g1 - vg1;
+        const int width = (g1 - g0) * 16;
+        if (kg1 < kg0 || width > kMaxFusedSlice) {
+            L.ok = false;
+            break;
+        }
+        if (width > L.max_width) L.max_width = width;
+        if (kg1 > kg0) {
+            const int hf = static_cast<int>(kg0 * 16 / D);
+            const int hl = static_cast<int>((kg1 * 16 - 1) / D);
+            if (hl - hf > 1) L.ok = false;  // a key run spans at most two copies
+            for (int h = hf; h <= hl && h < kMaxCopies; ++h) {
+                if (last_cta[h] < 0) L.cf[h] = c;
+                last_cta[h] = c;
+            }
+        }
+    }
+    for (int h = 0; h < H && L.ok; ++h) {
+        if (last_cta[h] < 0)
+            L.ok = false;
+        else
+            L.nh[h] = last_cta[h] - L.cf[h] + 1;
+    }
+    return L;
+}
 
 FusedPlan fused_plan(const engram_handle* h, int64_t T) {
     FusedPlan p = {};
     p.Tn = static_cast<int>((T + 15) / 16 * 16);
     p.mtiles = static_cast<int>((T + 127) / 128);
-    p.granules = static_cast<int>(h->N / 16);
     p.k_blocks = static_cast<int>(h->K * (h->cfg.wkv_format == ENGRAM_WKV_MXFP8 ? 1 : 2) / 128);
-    p.grid = h->num_sms < p.granules ? h->num_sms : p.granules;
-    p.max_width = (p.granules + p.grid - 1) / p.grid * 16;  // widest slice
     return p;
 }
 
 bool fused_supported(const engram_handle* h, int64_t T) {
-    const FusedPlan p = fused_plan(h, T);
+    if (!h->fused.ok) return false;
     if (h->cfg.wkv_format == ENGRAM_WKV_MXFP8) {
         // one accumulator of 256 columns plus 8 + 8 scale columns per k-block
-        return T >= 1 && T <= kMaxFusedTMx && p.max_width <= kMaxFusedSlice &&
-               h->cfg.head_dim % 32 == 0 && kMaxFusedSlice + 16 * (h->K / 128) <= 512;
+        return T >= 1 && T <= kMaxFusedTMx && h->cfg.head_dim % 32 == 0 &&
+               kMaxFusedSlice + 16 * (h->K / 128) <= 512;
     }
-    return T >= 1 && T <= kMaxFusedT && p.max_width <= kMaxFusedSlice && h->cfg.head_dim % 8 == 0;
+    return T >= 1 && T <= kMaxFusedT && h->cfg.head_dim % 8 == 0;
 }
 
 cudaError_t pack_weights(const engram_handle* h, cudaStream_t s) {
+    if (!h->fused.ok) return cudaSuccess;  // the fused kernel will not run
     const int64_t row_bytes = h->K * (h->cfg.wkv_format == ENGRAM_WKV_MXFP8 ? 1 : 2);
     const int64_t nchunks = h->N * row_bytes / 16;
     pack_w_kernel<<<static_cast<unsigned>((nchunks + 255) / 256), 256, 0, s>>>(
-        static_cast<const uint8_t*>(h->wkv), h->ws.wpack, h->N, row_bytes);
+        static_cast<const uint8_t*>(h->wkv), h->ws.wpack, h->N, row_bytes,
+        static_cast<int>(h->cfg.dim), static_cast<int>(h->cfg.hc_mult), h->fused.NG, h->fused.VG,
+        h->fused.grid);
     return cudaGetLastError();
 }
 
@@ -662,6 +854,8 @@ cudaError_t launch_decode_fused(engram_handle* h, const void* hidden, const int6
                                 const int32_t* ids, int64_t ids_stride, const uint8_t* mask,
                                 void* out, const int64_t* os, int64_t T, cudaStream_t s) {
     const FusedPlan p = fused_plan(h, T);
+    const FusedLayout& L = h->fused;
+    const bool mx = h->cfg.wkv_format == ENGRAM_WKV_MXFP8;
     FusedArgs a = {};
     a.T = static_cast<int>(T);
     a.Tn = p.Tn;
@@ -672,11 +866,10 @@ cudaError_t launch_decode_fused(engram_handle* h, const void* hidden, const int6
     a.N = static_cast<int>(h->N);
     a.K = static_cast<int>(h->K);
     a.mtiles = p.mtiles;
-    a.granules = p.granules;
+    a.NG = L.NG;
+    a.VG = L.VG;
     a.k_blocks = p.k_blocks;
     a.kb128 = static_cast<int>(h->K / 128);
-    // token rows per stage: one box of Tn rows, or two of 128 rows
-    a.x_bytes = static_cast<uint32_t>(p.mtiles == 1 ? p.Tn * 128 : 2 * 16384);
     a.gather = ids != nullptr ? 1 : 0;
     a.ids = ids;
     a.ids_stride = ids_stride;
@@ -696,47 +889,46 @@ cudaError_t launch_decode_fused(engram_handle* h, const void* hidden, const int6
     a.mask = mask;
     a.qk = h->ws.qk;
     a.wpack = h->ws.wpack;
-    a.part = h->ws.fpart;
-    a.value = h->ws.fvalue;
-    a.bar = h->ws.grid_bar;
+    a.rec = reinterpret_cast<float4*>(h->ws.fpart);
+    int base = 0;
+    for (int hh = 0; hh < kMaxCopies; ++hh) {
+        a.cf[hh] = L.cf[hh];
+        a.nh[hh] = L.nh[hh];
+        a.rec_base[hh] = base;
+        base += static_cast<int>(h->ws.kv_tpitch) * L.nh[hh];
+    }
+    a.value = h->keep_value ? h->ws.fvalue : nullptr;
+    a.bar = reinterpret_cast<unsigned long long*>(h->ws.grid_bar);
     a.gate_out = h->ws.gate;
     a.eps = static_cast<float>(h->cfg.eps);
     a.clamp = static_cast<float>(h->cfg.clamp);
     a.inv_d = 1.0f / static_cast<float>(a.D);
     a.inv_sqrt_d = 1.0f / sqrtf(static_cast<float>(a.D));
     a.err = h->ws.err;
-    // shared memory: stages | hidden rows | q*k slice | barriers; every stage
-    // and its token tile 1024-byte aligned
-    const int HR = a.T * a.H;
-    const int rows_per_cta = (HR + p.grid - 1) / p.grid;
-    const uint32_t row_bytes = static_cast<uint32_t>(a.D * 2);
-    const uint32_t qk_bytes = kMaxFusedSlice * 4;
-    const uint32_t bar_bytes = 512;
-    a.w_stage_bytes = static_cast<uint32_t>((p.max_width * 128 + 1023) / 1024 * 1024);
-    const uint32_t stage_bytes = a.w_stage_bytes + p.mtiles * 16384u;
-    uint32_t hid_rows = static_cast<uint32_t>(rows_per_cta < kHidRows ? rows_per_cta : kHidRows);
-    const uint32_t budget = kFusedSmemBytes - 1024;
-    int stages = 0;
-    for (;;) {
-        const uint32_t fixed = hid_rows * row_bytes + qk_bytes + bar_bytes;
-        stages = fixed < budget ? static_cast<int>((budget - fixed) / stage_bytes) : 0;
-        if (stages >= 4 || hid_rows == 0) break;
-        --hid_rows;
-    }
-    if (stages > kMaxStages) stages = kMaxStages;
-    // the finish keeps each row's value and partial records in the stage buffers
-    const int64_t fin_bytes =
-        static_cast<int64_t>(rows_per_cta) * (a.D + p.grid * kPartFloats) * 4;
-    if (stages < 2 || fin_bytes > static_cast<int64_t>(stages) * stage_bytes || rows_per_cta > 32)
-        return cudaErrorInvalidConfiguration;
-    a.stages = stages;
-    a.hid_rows = hid_rows;
-    a.hid_off = static_cast<uint32_t>(stages) * stage_bytes;
-    a.qk_off = a.hid_off + hid_rows * row_bytes;
+    // shared memory: weight ring | token ring | q*k slice | barriers
+    a.x_bytes = static_cast<uint32_t>(p.mtiles == 1 ? p.Tn * 128 : 2 * 16384);
+    a.x_stage_bytes = (a.x_bytes + 1023u) / 1024u * 1024u;
+    a.w_stage_bytes = static_cast<uint32_t>((L.max_width * 128 + 1023) / 1024 * 1024);
+    const uint32_t qk_bytes = kMaxFusedSlice * 4, bar_bytes = 1024;
+    const uint32_t budget = kFusedSmemBytes - 1024;  // after 1024-byte alignment
+    // The MMA reads all 128 rows of a token tile (M = 128) even when T is
+    // smaller; rows past T are never used, but the last stage's 16 KB read
+    // must stay inside this CTA's shared memory.
+    uint32_t x_ring = kXStages * a.x_stage_bytes;
+    if (p.mtiles == 1 && x_ring < (kXStages - 1) * a.x_stage_bytes + 16384u)
+        x_ring = (kXStages - 1) * a.x_stage_bytes + 16384u;
+    const uint32_t fixed = x_ring + qk_bytes + bar_bytes;
+    int stages = fixed < budget ? static_cast<int>((budget - fixed) / a.w_stage_bytes) : 0;
+    if (stages > kMaxWStages) stages = kMaxWStages;
+    if (stages < 2) return cudaErrorInvalidConfiguration;
+    a.w_stages = stages;
+    a.dual = (!mx && p.mtiles == 1) ? 1 : 0;
+    a.x_off = static_cast<uint32_t>(stages) * a.w_stage_bytes;
+    a.qk_off = a.x_off + x_ring;
     a.bar_off = a.qk_off + qk_bytes;
 
     cudaLaunchConfig_t cfg = {};
-    cfg.gridDim = dim3(static_cast<unsigned>(p.grid));
+    cfg.gridDim = dim3(static_cast<unsigned>(L.grid));
     cfg.blockDim = dim3(kThreads);
     cfg.dynamicSmemBytes = kFusedSmemBytes;
     cfg.stream = s;
@@ -745,9 +937,7 @@ cudaError_t launch_decode_fused(engram_handle* h, const void* hidden, const int6
     attr[0].val.cooperative = 1;
     cfg.attrs = attr;
     cfg.numAttrs = 1;
-    const CUtensorMap* tmx = p.mtiles == 1 ? &h->tm_act_n[p.Tn / 16 - 1] : &h->tm_act_m;
-    void* args[] = {const_cast<CUtensorMap*>(tmx), &a};
-    const bool mx = h->cfg.wkv_format == ENGRAM_WKV_MXFP8;
+    void* args[] = {&a};
     return cudaLaunchKernelExC(
         &cfg,
         mx ? reinterpret_cast<const void*>(decode_fused_kernel<true>)

@@ -256,10 +256,15 @@ int engram_create(const engram_config* cfg, const engram_weights* w, engram_t** 
     step(dalloc(&ws.value, ws.rows_alloc * c.dim * 2, true));
     step(dalloc(&ws.gate, ws.rows_alloc * c.hc_mult * sizeof(float), true));
     // fused decode kernel workspace, sized for the largest T it serves
-    step(dalloc(&ws.wpack, N * K * (mx ? 1 : 2), false));
-    step(dalloc(&ws.fpart, ws.kv_tpitch * sms * 8 * sizeof(float), true));
+    h->fused = fused_layout(N, c.dim, c.hc_mult, sms);
+    if (h->fused.ok) {
+        step(dalloc(&ws.wpack, N * K * (mx ? 1 : 2), false));
+        // gate-partial records: per copy [kv_tpitch][CTAs holding its keys] x 16 bytes
+        step(dalloc(&ws.fpart, ws.kv_tpitch * (h->fused.grid + kMaxCopies) * 4 * sizeof(float),
+                    true));
+    }
     step(dalloc(&ws.fvalue, ws.kv_tpitch * c.dim * sizeof(float), true));
-    step(dalloc(&ws.grid_bar, 4 * sizeof(unsigned), true));
+    step(dalloc(&ws.grid_bar, 8 * sizeof(unsigned), true));
     step(dalloc(&ws.qk, c.hc_mult * c.dim * sizeof(float), false));
     step(dalloc(&ws.err, sizeof(unsigned), true));
     if (e == cudaSuccess)
@@ -444,7 +449,7 @@ int engram_device_error(engram_t* h, uint32_t* bits, int clear) {
     if (e == cudaSuccess && (*bits & ENGRAM_DEVERR_TIMEOUT)) {
         // an unwound launch can leave the grid barrier's arrival count
         // short: start it again from zero
-        e = cudaMemset(h->ws.grid_bar, 0, 4 * sizeof(unsigned));
+        e = cudaMemset(h->ws.grid_bar, 0, 8 * sizeof(unsigned));
     }
     if (e != cudaSuccess) return ENGRAM_ERR_CUDA;
     return ENGRAM_OK;
@@ -460,7 +465,8 @@ int engram_debug_intermediates(engram_t* h, float* gate, float* value, int64_t T
         e = cudaMemcpyAsync(gate, h->ws.gate, T * h->cfg.hc_mult * sizeof(float),
                             cudaMemcpyDeviceToDevice, stream);
     if (e == cudaSuccess && value != nullptr) {
-        if (h->last_path == 0) return ENGRAM_ERR_INVALID_ARG;
+        if (h->last_path == 0 || (h->last_path == 3 && !h->keep_value))
+            return ENGRAM_ERR_INVALID_ARG;
         e = h->last_path == 3 ? launch_fused_debug_value(h, value, T, stream)
                               : launch_debug_value(h, value, T, stream);
     }
@@ -488,6 +494,12 @@ int engram_debug_staged_mx(engram_t* h, uint8_t* codes, uint8_t* scales, int64_t
         e = cudaMemcpyAsync(codes, h->ws.staged_q, T * h->K, cudaMemcpyDeviceToDevice, stream);
     if (e == cudaSuccess && scales != nullptr) e = launch_unpack_scales(h, scales, T, stream);
     return e == cudaSuccess ? ENGRAM_OK : ENGRAM_ERR_CUDA;
+}
+
+int engram_debug_keep_value(engram_t* h, int enable) {
+    if (h == nullptr) return ENGRAM_ERR_INVALID_ARG;
+    h->keep_value = enable != 0;
+    return set_err(h, ENGRAM_OK);
 }
 
 int engram_profile_enable(engram_t* h, int enable) {

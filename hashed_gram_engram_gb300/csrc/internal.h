@@ -18,6 +18,7 @@ constexpr int kBNPrefillMx = 128; // kv columns per prefill tile, MXFP8 wkv (TME
 constexpr int kKBlockBytes = 128; // bytes of K per pipeline stage (one swizzle row)
 constexpr int kGemmSmemBytes = 192 * 1024 + 2048;  // > half an SM: one CTA per SM
 constexpr int kFusedSmemBytes = 225 * 1024;       // fused decode kernel
+constexpr int kMaxCopies = 4;                     // largest hc_mult
 constexpr int kMaxFusedT = 256;                   // largest T of the fused decode kernel
 constexpr int kMaxFusedSlice = 256;               // widest column slice of one CTA (MMA N)
 constexpr int kMaxFusedTMx = 128;                 // largest T of the fused kernel, MXFP8 wkv
@@ -54,20 +55,31 @@ struct Workspace {
     // sticky device error word
     unsigned* err = nullptr;
     // fused decode kernel: wkv packed k-block-major (128 bytes of k per row
-    // and block) as swizzled shared-memory images, per-(token, CTA) gate
-    // partial sums, the fp32 value, the grid-barrier counter
+    // and block) as swizzled shared-memory images, each CTA's columns
+    // consecutive; gate-partial records; the fp32 value (validation only);
+    // two grid-barrier ticket counters
     uint8_t* wpack = nullptr;
-    float* fpart = nullptr;     // [kv_tpitch][num_sms][8]
+    float* fpart = nullptr;     // records: per hc copy [kv_tpitch][CTAs covering it][4]
     float* fvalue = nullptr;    // [kv_tpitch][D]
-    unsigned* grid_bar = nullptr;  // two {count, generation} grid barriers of the fused kernel
+    unsigned* grid_bar = nullptr;  // three 64-bit ticket counters of the fused kernel
     // host path staging (engram_forward_host)
     void* host_hidden = nullptr;
     int32_t* host_ids = nullptr;
     uint8_t* host_mask = nullptr;
 };
 
+// Column ownership of the fused decode kernel: N = D*(H+1) columns in
+// 16-column granules; CTA c owns NG-split granules [g0, g1), of which the
+// first (VG-split) ones are value columns and the rest a run of key columns
+// (first key granule = first_granule(c, NG) - first_granule(c, VG)).
+struct FusedLayout {
+    int grid, NG, VG, max_width;
+    int cf[kMaxCopies], nh[kMaxCopies];  // first CTA and CTA count holding each copy's keys
+    bool ok;
+};
+
 struct FusedPlan {
-    int Tn, mtiles, granules, k_blocks, grid, max_width;
+    int Tn, mtiles, k_blocks;
 };
 
 }  // namespace engram
@@ -89,6 +101,8 @@ struct engram_handle {
     CUtensorMap tm_w_n;        // wkv, prefill B operand (box BN rows x 128 bytes)
     CUtensorMap tm_act_m;      // staged rows (bf16, or e4m3 codes), box 128 rows x 128 bytes
     CUtensorMap tm_act_n[16];  // the same, box 16 * (i + 1) rows (the fused kernel's tile)
+    engram::FusedLayout fused;
+    int keep_value;  // validation: the fused kernel also stores the fp32 value
     // last lookup
     int64_t staged_T;
     int last_error;
@@ -114,6 +128,7 @@ cudaError_t pack_scale_atoms(const engram_handle* h, cudaStream_t s);
 cudaError_t launch_unpack_scales(const engram_handle* h, uint8_t* out, int64_t T, cudaStream_t s);
 
 // decode_fused.cu
+FusedLayout fused_layout(int64_t N, int64_t D, int64_t H, int num_sms);
 FusedPlan fused_plan(const engram_handle* h, int64_t T);
 bool fused_supported(const engram_handle* h, int64_t T);
 cudaError_t fused_setup_attributes();

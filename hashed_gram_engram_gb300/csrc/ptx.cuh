@@ -79,6 +79,24 @@ __device__ __forceinline__ bool mbar_wait(uint64_t* bar, uint32_t parity,
     return false;
 }
 
+// The same wait for threads that are not on the critical path: between
+// polls the thread sleeps ~sleep_ns, so that it does not take issue slots
+// from the warps sharing its scheduler (the MMA issuer above all).
+__device__ __forceinline__ bool mbar_wait_sleep(uint64_t* bar, uint32_t parity,
+                                                const volatile int* abort, uint32_t sleep_ns) {
+    if (mbar_try_wait(bar, parity)) return true;
+    const uint64_t t0 = globaltimer_ns();
+    for (uint32_t i = 1; i < kWaitLimitIters; ++i) {
+        __nanosleep(sleep_ns);
+        if (mbar_try_wait(bar, parity)) return true;
+        if ((i & 7u) == 0) {
+            if (abort != nullptr && *abort) return false;
+            if (globaltimer_ns() - t0 > kWaitLimitNs) return false;
+        }
+    }
+    return false;
+}
+
 // ---------------------------------------------------------------- TMA
 __device__ __forceinline__ void tma_prefetch_desc(const CUtensorMap* map) {
     asm volatile("prefetch.tensormap [%0];" ::"l"(reinterpret_cast<uint64_t>(map)) : "memory");
@@ -146,6 +164,32 @@ __device__ __forceinline__ void prefetch_l2(const void* src, uint32_t bytes) {
     asm volatile("cp.async.bulk.prefetch.L2.global [%0], %1;" ::"l"(reinterpret_cast<uint64_t>(src)),
                  "r"(bytes)
                  : "memory");
+}
+
+// 16-byte asynchronous copy global -> shared on the load/store path (not
+// the TMA unit), caching in L2 only.  src_bytes < 16 zero-fills the rest
+// (0: the whole chunk is zero and src is not read).
+__device__ __forceinline__ void cp_async16(uint32_t dst_smem, const void* src, uint32_t src_bytes) {
+    asm volatile("cp.async.cg.shared.global [%0], [%1], 16, %2;" ::"r"(dst_smem), "l"(src),
+                 "r"(src_bytes)
+                 : "memory");
+}
+
+// Arrive on `bar` once every cp.async this thread issued so far has landed
+// (the arrival counts against the barrier's expected count).
+__device__ __forceinline__ void cp_async_mbar_arrive(uint64_t* bar) {
+    asm volatile("cp.async.mbarrier.arrive.noinc.shared::cta.b64 [%0];" ::"r"(smem_addr(bar))
+                 : "memory");
+}
+
+__device__ __forceinline__ void cp_async_wait_all() {
+    asm volatile("cp.async.wait_all;" ::: "memory");
+}
+
+// Prefetch the 128-byte line holding `p` into L2 (an ordinary memory
+// instruction, not a bulk copy).
+__device__ __forceinline__ void prefetch_line_l2(const void* p) {
+    asm volatile("prefetch.global.L2 [%0];" ::"l"(p));
 }
 
 // 2-D tiled store of one box from shared memory (bulk-group completion).

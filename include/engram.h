@@ -173,6 +173,13 @@ int engram_layout(int64_t vocab_size, int32_t max_ngram_size, int32_t n_heads,
 int engram_debug_intermediates(engram_t* h, float* gate, float* value, int64_t T,
                                cudaStream_t stream);
 
+/* Validation hook: with enable != 0, later forwards on the fused decode
+ * path also store the fp32 value [T, D] (an extra T*D*4 bytes written per
+ * call) so that engram_debug_intermediates can return it; otherwise that
+ * call returns ENGRAM_ERR_INVALID_ARG for the value of a fused forward.
+ * Off by default.  The prefill path always keeps its bf16 value. */
+int engram_debug_keep_value(engram_t* h, int enable);
+
 /* Validation hook: copy the staged rows [T, K] bf16 (the gather output) of
  * the last lookup into `rows` (device), on `stream`. */
 int engram_debug_staged_rows(engram_t* h, void* rows, int64_t T, cudaStream_t stream);

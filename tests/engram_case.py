@@ -39,7 +39,7 @@ class Case:
                             max_tokens=max_tokens or wl.T, table=self.table, rows=self.rows,
                             row_offset=self.row_offset, wkv=self.wkv, wkv_scale=self.wkv_scale,
                             q_weight=self.q, k_weight=self.k, eps=wl.eps, clamp=wl.clamp,
-                            device=0)
+                            device=0, keep_value=True)
         self._host = None
 
     def host(self):
