@@ -43,6 +43,10 @@
 //            (masked tokens keep hidden's bits), the value read straight
 //            from TMEM.
 //
+// The launch is programmatic-dependent: the next launch may start once every
+// CTA has begun; before griddepcontrol.wait a CTA only sets up and starts the
+// weight stream (wkv is never written by a kernel).
+//
 // MXFP8 wkv (T <= 128): the gather also quantises the rows (e4m3 codes and
 // E8M0 scales per 32 k); the MMAs are kind::mxf8f6f4 block_scale and the
 // scale factors sit in TMEM next to the accumulator.  A slice starts on any
@@ -190,10 +194,6 @@ __global__ void __launch_bounds__(kThreads, 1)
             v[j] = good ? ld_stream_v4(src + j * 8) : make_uint4(0u, 0u, 0u, 0u);
         return good;
     };
-    uint4 pre[4] = {};
-    bool pre_good = true;
-    if (warp >= 2 && warp < 6 && tid - 64 < g_n) pre_good = fetch(tid - 64, pre);
-
     if (tid == 0) {
         for (int s = 0; s < a.w_stages; ++s) {
             mbar_init(&wfull[s], 1);
@@ -208,9 +208,8 @@ __global__ void __launch_bounds__(kThreads, 1)
         mbar_init(drain2, 1);
         mbar_init(scbar, 128);
         *abort_flag = 0;
-        // this launch's epoch: stable until CTA 0 advances it at the end
-        *epoch_s = *reinterpret_cast<volatile unsigned long long*>(a.bar) + 1ull;
         fence_barrier_init();
+        pdl_launch_dependents();
     }
     int w_issued = 0;
     const uint64_t pol_w = policy_evict_first();
@@ -225,6 +224,15 @@ __global__ void __launch_bounds__(kThreads, 1)
             w_src += w_kstep;
         }
     }
+    // everything below may read what the preceding launch wrote
+    pdl_wait();
+    if (tid == 0) {
+        // this launch's epoch: stable until CTA 0 advances it at the end
+        *epoch_s = *reinterpret_cast<volatile unsigned long long*>(a.bar) + 1ull;
+    }
+    uint4 pre[4] = {};
+    bool pre_good = true;
+    if (warp >= 2 && warp < 6 && tid - 64 < g_n) pre_good = fetch(tid - 64, pre);
     if (warp == 1) {
         tmem_alloc(tmem_slot, kTmemCols);
         tmem_relinquish();
@@ -852,7 +860,8 @@ cudaError_t launch_fused_debug_value(const engram_handle* h, float* value, int64
 
 cudaError_t launch_decode_fused(engram_handle* h, const void* hidden, const int64_t* hs,
                                 const int32_t* ids, int64_t ids_stride, const uint8_t* mask,
-                                void* out, const int64_t* os, int64_t T, cudaStream_t s) {
+                                void* out, const int64_t* os, int64_t T, cudaStream_t s,
+                                bool pdl) {
     const FusedPlan p = fused_plan(h, T);
     const FusedLayout& L = h->fused;
     const bool mx = h->cfg.wkv_format == ENGRAM_WKV_MXFP8;
@@ -932,11 +941,13 @@ cudaError_t launch_decode_fused(engram_handle* h, const void* hidden, const int6
     cfg.blockDim = dim3(kThreads);
     cfg.dynamicSmemBytes = kFusedSmemBytes;
     cfg.stream = s;
-    cudaLaunchAttribute attr[1];
+    cudaLaunchAttribute attr[2];
     attr[0].id = cudaLaunchAttributeCooperative;
     attr[0].val.cooperative = 1;
+    attr[1].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[1].val.programmaticStreamSerializationAllowed = 1;
     cfg.attrs = attr;
-    cfg.numAttrs = 1;
+    cfg.numAttrs = pdl ? 2 : 1;
     void* args[] = {&a};
     return cudaLaunchKernelExC(
         &cfg,

@@ -360,7 +360,7 @@ int engram_forward(engram_t* h, const void* hidden, const int64_t hidden_strides
         mark(0);
         mark(1);
         e = launch_decode_fused(h, hidden, hidden_strides, hash_ids, ids_row_stride, token_mask,
-                                out, out_strides, T, stream);
+                                out, out_strides, T, stream, !prof);
         if (hash_ids != nullptr) h->staged_T = T;  // the kernel staged the rows
         mark(2);
         mark(3);

@@ -61,7 +61,7 @@ struct Workspace {
     uint8_t* wpack = nullptr;
     float* fpart = nullptr;     // records: per hc copy [kv_tpitch][CTAs covering it][4]
     float* fvalue = nullptr;    // [kv_tpitch][D]
-    unsigned* grid_bar = nullptr;  // three 64-bit ticket counters of the fused kernel
+    unsigned* grid_bar = nullptr;  // launch counter + barrier counters of the fused kernel
     // host path staging (engram_forward_host)
     void* host_hidden = nullptr;
     int32_t* host_ids = nullptr;
@@ -138,7 +138,8 @@ cudaError_t launch_fused_debug_value(const engram_handle* h, float* value, int64
 // ids == nullptr: the rows were staged by engram_lookup
 cudaError_t launch_decode_fused(engram_handle* h, const void* hidden, const int64_t* hs,
                                 const int32_t* ids, int64_t ids_stride, const uint8_t* mask,
-                                void* out, const int64_t* os, int64_t T, cudaStream_t s);
+                                void* out, const int64_t* os, int64_t T, cudaStream_t s,
+                                bool pdl);
 
 // gate.cu
 cudaError_t launch_gate_from_partials(const engram_handle* h, const void* hidden,
