@@ -51,7 +51,8 @@ def parse():
                    help="skip the offload workload (17 GB pinned host table)")
     p.add_argument("--cpu-seconds", type=float, default=10.0)
     p.add_argument("--layers", type=int, default=6)
-    p.add_argument("--case", choices=["decode", "prefill"], default=None,
+    p.add_argument("--case", choices=["decode", "prefill", "mxfp8_decode", "mxfp8_prefill"],
+                   default=None,
                    help="only run W + K plain forwards of one layer of that workload (the "
                         "small case profilers capture) and print a one-line summary")
     return p.parse_args()
@@ -300,7 +301,7 @@ def run_case(args):
     torch.cuda.set_device(0)
     stream = torch.cuda.Stream()
     torch.cuda.set_stream(stream)
-    wl = W.DECODE if args.case == "decode" else W.PREFILL
+    wl = W.ALL[args.case]
     wl_l, layer, _, _ = make_layer(W, Engram, wl, 0, wl.T, 0)
     st = W.make_step_inputs(wl_l, "cuda")
     out = torch.empty_like(st["hidden"])

@@ -21,12 +21,11 @@
 // in TMEM) -- for bf16 with T <= 128 it takes the even k-blocks and warp 6
 // the odd ones into a second accumulator (one thread's issue loop cannot
 // keep the tensor pipe busy on these small MMAs), the two summed when read;
-// warps 2-5 load the token tiles, then run the epilogue and the residual
-// (TMEM lane quarter = warp % 4).  The token tiles travel on the
-// load/store path (cp.async, 16 bytes a thread, each chunk to its 128-byte-
-// swizzled place), loaded by warps 2-3 while warps 4-5 wait in a hardware
-// barrier: the scheduler that runs the MMA issuer (warp 1) then runs no
-// other busy warp.
+// warps 2-5 gather, then run the epilogue and the residual (TMEM lane
+// quarter = warp % 4).  The token tiles come through their own ring of TMA
+// tensor copies (one box of the staged rows per k-block, 128-byte swizzled
+// by the copy engine), issued by one thread of warp 2: per-thread cp.async
+// from a few warps could not keep enough bytes in flight.
 //
 //   gather   each CTA copies ~1/grid of the T x C hash rows into the
 //            staged buffer (MXFP8: and quantises them into e4m3 codes and
@@ -72,14 +71,15 @@ namespace {
 constexpr int kThreads = 224;
 constexpr int kWarps = kThreads / 32;
 constexpr int kMaxWStages = 12;
-constexpr int kXStages = 4;
+constexpr int kMaxXStages = 12;
+constexpr uint32_t kXRingTarget = 96 * 1024;  // bytes of token stages
 constexpr int kKeyChunks = kMaxFusedSlice / 16;  // 16-column chunks of a slice
 constexpr uint32_t kTmemCols = 512;
 
 struct FusedArgs {
     int T, Tn, D, H, C, E, N, K;
     int mtiles, NG, VG, k_blocks, kb128;
-    int w_stages;
+    int w_stages, x_stages;
     int dual;  // two MMA issuers, two accumulators (bf16, one 128-token tile)
     uint32_t w_stage_bytes, x_stage_bytes, x_bytes;
     int gather;  // gather the hash rows in this launch
@@ -140,7 +140,7 @@ __device__ __forceinline__ bool grid_wait(const unsigned long long* ctr, unsigne
 
 template <bool kMx>
 __global__ void __launch_bounds__(kThreads, 1)
-    decode_fused_kernel(const FusedArgs a) {
+    decode_fused_kernel(const __grid_constant__ CUtensorMap tm_x, const FusedArgs a) {
     extern __shared__ uint8_t smem_raw[];
     uint8_t* smem = reinterpret_cast<uint8_t*>(
         (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~static_cast<uintptr_t>(1023));
@@ -149,8 +149,8 @@ __global__ void __launch_bounds__(kThreads, 1)
     uint64_t* wfull = reinterpret_cast<uint64_t*>(smem + a.bar_off);
     uint64_t* wempty = wfull + kMaxWStages;
     uint64_t* xfull = wempty + kMaxWStages;
-    uint64_t* xempty = xfull + kXStages;
-    uint64_t* tfull = xempty + kXStages;  // every MMA done
+    uint64_t* xempty = xfull + kMaxXStages;
+    uint64_t* tfull = xempty + kMaxXStages;  // every MMA done
     uint64_t* drain = tfull + 1;
     uint64_t* drain2 = drain + 1;  // the second issuer's in-flight MMAs
     uint64_t* scbar = drain2 + 1;         // MXFP8: every scale word is in TMEM
@@ -199,8 +199,8 @@ __global__ void __launch_bounds__(kThreads, 1)
             mbar_init(&wfull[s], 1);
             mbar_init(&wempty[s], 1);
         }
-        for (int s = 0; s < kXStages; ++s) {
-            mbar_init(&xfull[s], 64);  // one cp.async arrival per loading thread
+        for (int s = 0; s < a.x_stages; ++s) {
+            mbar_init(&xfull[s], 1);  // the loading thread's expect_tx
             mbar_init(&xempty[s], 1);
         }
         mbar_init(tfull, a.dual ? 2 : 1);  // one commit per issuer
@@ -209,9 +209,11 @@ __global__ void __launch_bounds__(kThreads, 1)
         mbar_init(scbar, 128);
         *abort_flag = 0;
         fence_barrier_init();
+        tma_prefetch_desc(&tm_x);
         pdl_launch_dependents();
     }
     int w_issued = 0;
+    int x_issued = 0;  // token-tile copies issued (thread 64)
     const uint64_t pol_w = policy_evict_first();
     const uint8_t* w_src = a.wpack + static_cast<int64_t>(c_lo) * 128;
     const int64_t w_kstep = static_cast<int64_t>(a.N) * 128;
@@ -303,7 +305,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                 } else {
                     wd += wstep;
                 }
-                if (++sx == kXStages) {
+                if (++sx == a.x_stages) {
                     sx = 0;
                     px ^= 1u;
                     xd = xdesc0;
@@ -317,7 +319,6 @@ __global__ void __launch_bounds__(kThreads, 1)
                     ok = false;
                     break;
                 }
-                fence_proxy_async_smem();  // token tiles were written by cp.async (generic proxy)
                 tc_fence_after();
                 if constexpr (kMx) {
                     // 4 x K32, scale byte k of each cell
@@ -404,6 +405,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                 }
             }
             if (bad) atomicOr(a.err, ENGRAM_DEVERR_BAD_HASH_ID);
+            fence_proxy_async();  // other CTAs read these rows with TMA copies
         }
         // grid barrier 1 (the counter advances on every launch, gather or not)
         named_barrier_sync(1, 128);
@@ -414,12 +416,12 @@ __global__ void __launch_bounds__(kThreads, 1)
         // q*k of the slice's key columns
         for (int j = etid; j < klen; j += 128) qk_s[j] = __ldg(a.qk + k0 + j);
         named_barrier_sync(1, 128);  // qk_s complete; grid barrier 1 has passed
-        // Token tiles: k-block kb of every token row into stage kb % kXStages,
-        // row r at 128 * r (second 128-row tile 16 KB on), 16-byte chunk j at
-        // position j ^ (r % 8): the 128-byte swizzle the MMA descriptors
-        // expect.  Rows past T hold whatever is staged there; their
-        // accumulator rows are never used.  (MXFP8: the token scales go to
-        // TMEM once the first tiles are on their way.)
+        // Token tiles: k-block kb of the first Tn staged rows into stage
+        // kb % x_stages by one TMA box (128-row boxes for a second tile), row
+        // r at 128 * r, 16-byte chunk j at position j ^ (r % 8): the 128-byte
+        // swizzle the MMA descriptors expect.  Rows past T hold whatever is
+        // staged there; their accumulator rows are never used.  (MXFP8: the
+        // token scales go to TMEM once the first tiles are on their way.)
         {
             // MXFP8 token scales: A row r = token t in lane t, column
             // tm_sfa + 8 kb + t / 32 (written to all four columns); needed
@@ -444,42 +446,38 @@ __global__ void __launch_bounds__(kThreads, 1)
                 tc_fence_before();
                 mbar_arrive(scbar);
             };
-            const int chunks = a.Tn * 8;
-            constexpr int kLoaders = 64;  // warps 2-3
-            const int kb_first = a.k_blocks < 2 ? a.k_blocks : 2;  // tiles before the scales
+            constexpr int kKElems = kMx ? 128 : 64;  // elements per 128-byte row of a k-block
             bool ok = true;
-            for (int kb = 0; kb < a.k_blocks; ++kb) {
-                // (a stage is reused only after the MMAs, which need the scales)
-                if (kb == kb_first) {
-                    if (kMx) token_scales();  // all four epilogue warps
-                    if (etid >= kLoaders) break;  // warps 4-5 are done
-                }
-                if (etid >= kLoaders) continue;
-                const int s = kb % kXStages;
-                if (!mbar_wait_sleep(&xempty[s], static_cast<uint32_t>((kb / kXStages) & 1) ^ 1u,
-                                     abort_v, 64)) {
-                    ok = false;
-                    break;
-                }
+            auto load_x = [&](int kb) {  // thread 64 only
+                const int s = kb % a.x_stages;
                 uint8_t* xs = xring + s * a.x_stage_bytes;
-                for (int i = etid; i < chunks; i += kLoaders) {
-                    const int r = i >> 3, j = i & 7;
-                    const uint32_t dst =
-                        smem_addr(xs + (r >> 7) * 16384 + (r & 127) * 128 + ((j ^ (r & 7)) << 4));
-                    const void* src =
-                        kMx ? static_cast<const void*>(a.staged_q + static_cast<int64_t>(r) * a.K +
-                                                       kb * 128 + j * 16)
-                            : static_cast<const void*>(a.staged + static_cast<int64_t>(r) * a.K +
-                                                       kb * 64 + j * 8);
-                    cp_async16(dst, src, 16);
-                }
-                cp_async_mbar_arrive(&xfull[s]);
+                mbar_arrive_expect_tx(&xfull[s], a.x_bytes);
+                tma_load_2d(xs, &tm_x, &xfull[s], kb * kKElems, 0);
+                if (a.mtiles == 2) tma_load_2d(xs + 16384, &tm_x, &xfull[s], kb * kKElems, 128);
+                ++x_issued;
+            };
+            const int first = a.k_blocks < a.x_stages ? a.k_blocks : a.x_stages;
+            if (etid == 0) {
+                fence_proxy_async();  // the staged rows were written by ordinary stores
+                for (int kb = 0; kb < first; ++kb) load_x(kb);
             }
-            if (kMx && a.k_blocks == kb_first) token_scales();  // (K of at most 2 blocks)
-            cp_async_wait_all();
-            if (!ok) fail(abort_flag, a.err);
-            // warps 4-5 sleep here (no polling) until the loaders are through
-            named_barrier_sync(2, 128);
+            __syncwarp();
+            if (kMx) token_scales();  // (the first MMAs wait for the scales)
+            if (etid == 0) {
+                // the rest, each as soon as its stage's MMAs are done
+                for (int kb = first; kb < a.k_blocks; ++kb) {
+                    const int s = kb % a.x_stages;
+                    if (!mbar_wait_sleep(&xempty[s],
+                                         static_cast<uint32_t>((kb / a.x_stages) & 1) ^ 1u, abort_v,
+                                         64)) {
+                        ok = false;
+                        break;
+                    }
+                    load_x(kb);
+                }
+                if (!ok) fail(abort_flag, a.err);
+            }
+            __syncwarp();
         }
 
         // Epilogue: thread = one token of an accumulator, key columns of the
@@ -652,6 +650,11 @@ __global__ void __launch_bounds__(kThreads, 1)
         if (tid == 0) {
             for (int j = w_issued > a.w_stages ? w_issued - a.w_stages : 0; j < w_issued; ++j)
                 mbar_wait(&wfull[j % a.w_stages], static_cast<uint32_t>((j / a.w_stages) & 1),
+                          nullptr);
+        }
+        if (tid == 64) {
+            for (int j = x_issued > a.x_stages ? x_issued - a.x_stages : 0; j < x_issued; ++j)
+                mbar_wait(&xfull[j % a.x_stages], static_cast<uint32_t>((j / a.x_stages) & 1),
                           nullptr);
         }
         if (tid == 32) {
@@ -923,9 +926,14 @@ cudaError_t launch_decode_fused(engram_handle* h, const void* hidden, const int6
     // The MMA reads all 128 rows of a token tile (M = 128) even when T is
     // smaller; rows past T are never used, but the last stage's 16 KB read
     // must stay inside this CTA's shared memory.
-    uint32_t x_ring = kXStages * a.x_stage_bytes;
-    if (p.mtiles == 1 && x_ring < (kXStages - 1) * a.x_stage_bytes + 16384u)
-        x_ring = (kXStages - 1) * a.x_stage_bytes + 16384u;
+    // Token stages: about kXRingTarget bytes of them (at least 4), so that
+    // the tiles in flight cover the L2 round trip of the refills.
+    int xs = static_cast<int>(kXRingTarget / a.x_stage_bytes);
+    xs = xs < 4 ? 4 : (xs > kMaxXStages ? kMaxXStages : xs);
+    a.x_stages = xs;
+    uint32_t x_ring = static_cast<uint32_t>(xs) * a.x_stage_bytes;
+    if (p.mtiles == 1 && x_ring < static_cast<uint32_t>(xs - 1) * a.x_stage_bytes + 16384u)
+        x_ring = static_cast<uint32_t>(xs - 1) * a.x_stage_bytes + 16384u;
     const uint32_t fixed = x_ring + qk_bytes + bar_bytes;
     int stages = fixed < budget ? static_cast<int>((budget - fixed) / a.w_stage_bytes) : 0;
     if (stages > kMaxWStages) stages = kMaxWStages;
@@ -948,7 +956,9 @@ cudaError_t launch_decode_fused(engram_handle* h, const void* hidden, const int6
     attr[1].val.programmaticStreamSerializationAllowed = 1;
     cfg.attrs = attr;
     cfg.numAttrs = pdl ? 2 : 1;
-    void* args[] = {&a};
+    // token tiles: a box of Tn rows, or two of 128
+    CUtensorMap tm_x = p.mtiles == 1 ? h->tm_act_n[p.Tn / 16 - 1] : h->tm_act_m;
+    void* args[] = {&tm_x, &a};
     return cudaLaunchKernelExC(
         &cfg,
         mx ? reinterpret_cast<const void*>(decode_fused_kernel<true>)
