@@ -372,6 +372,8 @@ __global__ void __launch_bounds__(kThreads, 1)
                 tmem_st4(col + 4, w[4], w[5], w[6], w[7]);
             }
         }
+        // q*k of the slice's key columns (fixed at create)
+        for (int j = etid; j < klen; j += 128) qk_s[j] = __ldg(a.qk + k0 + j);
         // This CTA's share of the hash rows -> the staged-rows buffer
         // (ParallelEngramEmbedding.lookup); MXFP8: also their e4m3 codes and
         // scales.  Every CTA's token tiles need every row: grid barrier 1.
@@ -413,8 +415,6 @@ __global__ void __launch_bounds__(kThreads, 1)
             grid_arrive(a.bar + 1);
             if (a.gather && !grid_wait(a.bar + 1, target)) fail(abort_flag, a.err);
         }
-        // q*k of the slice's key columns
-        for (int j = etid; j < klen; j += 128) qk_s[j] = __ldg(a.qk + k0 + j);
         named_barrier_sync(1, 128);  // qk_s complete; grid barrier 1 has passed
         // Token tiles: k-block kb of the first Tn staged rows into stage
         // kb % x_stages by one TMA box (128-row boxes for a second tile), row

@@ -251,7 +251,7 @@ int engram_create(const engram_config* cfg, const engram_weights* w, engram_t** 
     // be too wide)
     step(dalloc(&ws.partials,
                 ws.rows_alloc * c.hc_mult * (c.dim / (mx ? kBNPrefillMx : kBNPrefill)) *
-                    sizeof(float2),
+                    sizeof(float4),
                 true));
     step(dalloc(&ws.value, ws.rows_alloc * c.dim * 2, true));
     step(dalloc(&ws.gate, ws.rows_alloc * c.hc_mult * sizeof(float), true));
@@ -276,6 +276,7 @@ int engram_create(const engram_config* cfg, const engram_weights* w, engram_t** 
     if (e == cudaSuccess && mx) e = pack_scale_atoms(h, 0);
     if (e == cudaSuccess) e = gemm_setup_attributes();
     if (e == cudaSuccess) e = fused_setup_attributes();
+    if (e == cudaSuccess) e = gate_setup_attributes();
     if (e == cudaSuccess) e = cudaDeviceSynchronize();
     if (e != cudaSuccess) {
         free_handle(h);

@@ -44,7 +44,7 @@ struct Workspace {
     int64_t kv_tpitch = 0;
     // prefill path: fp32 (sum key^2, sum hidden*q*k*key) per key tile
     // [rows_alloc][H][D/BN] and the bf16 value [rows_alloc][D]
-    float2* partials = nullptr;
+    float4* partials = nullptr;  // prefill: (sum hidden^2, sum key^2, sum h*q*k*key, -)
     uint16_t* value = nullptr;
     // fp32 gate of the last forward [rows_alloc][H]
     float* gate = nullptr;
@@ -132,6 +132,7 @@ FusedLayout fused_layout(int64_t N, int64_t D, int64_t H, int num_sms);
 FusedPlan fused_plan(const engram_handle* h, int64_t T);
 bool fused_supported(const engram_handle* h, int64_t T);
 cudaError_t fused_setup_attributes();
+cudaError_t gate_setup_attributes();
 cudaError_t pack_weights(const engram_handle* h, cudaStream_t s);
 cudaError_t launch_fused_debug_value(const engram_handle* h, float* value, int64_t T,
                                      cudaStream_t s);

@@ -202,6 +202,15 @@ __device__ __forceinline__ void tma_store_2d(const CUtensorMap* map, const void*
         : "memory");
 }
 
+// Contiguous shared -> global copy (both 16-byte aligned, size a multiple
+// of 16) in the thread's current bulk group.
+__device__ __forceinline__ void bulk_store(void* dst, const void* src, uint32_t bytes) {
+    asm volatile("cp.async.bulk.global.shared::cta.bulk_group [%0], [%1], %2;" ::"l"(
+                     reinterpret_cast<uint64_t>(dst)),
+                 "r"(smem_addr(src)), "r"(bytes)
+                 : "memory");
+}
+
 __device__ __forceinline__ void bulk_commit() {
     asm volatile("cp.async.bulk.commit_group;" ::: "memory");
 }

@@ -9,7 +9,7 @@
 // This is the prefill schedule (T > 256; decode runs in decode_fused.cu):
 // 128 tokens x 256 kv columns per tile, persistent CTAs stride over tiles.
 // The epilogue never writes keys: for a key tile it reduces
-// (sum key^2, sum hidden*q*k*key) over the tile's 256 dims -- the
+// (sum hidden^2, sum key^2, sum hidden*q*k*key) over the tile's dims -- the
 // split-dim gate partials of _engram_gate_partials_kernel
 // ("vllm.models.deepseek_v41.amd.engram"), here per N tile instead of per
 // TP rank -- and for a value tile it stores the value in bf16.
@@ -50,7 +50,7 @@ struct GemmArgs {
     const uint16_t* hidden;
     int64_t hs_t, hs_h;
     const float* qk;
-    float2* partials;
+    float4* partials;
     uint16_t* value;
     const uint8_t* sfa;  // MXFP8: scale atoms of the staged codes
     const uint8_t* sfb;  // MXFP8: scale atoms of wkv
@@ -280,7 +280,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                     }
                     tc_fence_after();
                     const float* qkp = a.qk + h * a.D + d0;
-                    float skk = 0.f, shk = 0.f;
+                    float shh = 0.f, skk = 0.f, shk = 0.f;
 #pragma unroll
                     for (int c = 0; c < BN; c += 32) {
                         uint32_t r[32];
@@ -297,6 +297,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                             for (int i = 0; i < 8; ++i) {
                                 const float key = __uint_as_float(r[j + i]);
                                 const float x = (i & 1) ? bf16hi(w[i >> 1]) : bf16lo(w[i >> 1]);
+                                shh = fmaf(x, x, shh);
                                 skk = fmaf(key, key, skk);
                                 shk = fmaf(x * qk[i], key, shk);
                             }
@@ -307,7 +308,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                     if (lane == 0) mbar_arrive(&tempty[acc]);
                     if (live)
                         a.partials[(static_cast<int64_t>(t) * a.H + h) * a.J + d0 / BN] =
-                            make_float2(skk, shk);
+                            make_float4(shh, skk, shk, 0.f);
                 } else {
                     if (!mbar_wait(&tfull[acc], apar, abort_v)) {
                         ok = false;
