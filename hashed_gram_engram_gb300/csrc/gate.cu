@@ -112,9 +112,12 @@ __global__ void __launch_bounds__(kRingThreads, 1) gate_ring_kernel(const RingAr
                 const int s = i % a.stages, t = token(i);
                 uint8_t* st = smem + s * a.stage_bytes;
                 mbar_arrive_expect_tx(&full[s], in_bytes);
-                for (int h = 0; h < a.H; ++h)
-                    bulk_load(st + h * a.row_bytes, a.hidden + t * a.hs_t + h * a.hs_h, a.row_bytes,
-                              &full[s]);
+                if (a.hs_h == a.D)  // the token's rows are one block
+                    bulk_load(st, a.hidden + t * a.hs_t, a.H * a.row_bytes, &full[s]);
+                else
+                    for (int h = 0; h < a.H; ++h)
+                        bulk_load(st + h * a.row_bytes, a.hidden + t * a.hs_t + h * a.hs_h,
+                                  a.row_bytes, &full[s]);
             };
             auto load_rest = [&](int i) {  // written by the wkv kernel
                 const int s = i % a.stages, t = token(i);
@@ -138,12 +141,24 @@ __global__ void __launch_bounds__(kRingThreads, 1) gate_ring_kernel(const RingAr
                     break;
                 }
                 const uint8_t* st = smem + s * a.stage_bytes;
-                for (int h = 0; h < a.H; ++h)
-                    bulk_store(a.out + t * a.os_t + h * a.os_h, st + h * a.row_bytes, a.row_bytes);
+                if (a.os_h == a.D)
+                    bulk_store(a.out + t * a.os_t, st, a.H * a.row_bytes);
+                else
+                    for (int h = 0; h < a.H; ++h)
+                        bulk_store(a.out + t * a.os_t + h * a.os_h, st + h * a.row_bytes,
+                                   a.row_bytes);
                 bulk_commit();
                 // the stage takes token j + stages once the store has read it
                 // (the compute warps go on with the tokens already in place)
-                if (j + a.stages < n) {
+                if (a.stages >= 4) {
+                    const int next = j - 1 + a.stages;
+                    if (j >= 1 && next < n) {
+                        bulk_wait_read<1>();
+                        load_hidden(next);
+                        load_rest(next);
+                        ++issued;
+                    }
+                } else if (j + a.stages < n) {
                     bulk_wait_read<0>();
                     load_hidden(j + a.stages);
                     load_rest(j + a.stages);
