@@ -245,12 +245,14 @@ int engram_create(const engram_config* cfg, const engram_weights* w, engram_t** 
     if (mx) {
         step(dalloc(&ws.staged_q, ws.rows_alloc * K, true));
         step(dalloc(&ws.staged_s, ws.rows_alloc * K / 32, true));
-        step(dalloc(&ws.wsf_atoms, N * K / 32, false));
+        // one 512-byte atom per 128 rows of each prefill tile and 128-byte k-block
+        step(dalloc(&ws.wsf_atoms,
+                    (N / prefill_bn(h)) * ((prefill_bn(h) + 127) / 128) * (K / 128) * 512, false));
     }
     // prefill path (also taken by small T when a decode column slice would
     // be too wide)
     step(dalloc(&ws.partials,
-                ws.rows_alloc * c.hc_mult * (c.dim / (mx ? kBNPrefillMx : kBNPrefill)) *
+                ws.rows_alloc * c.hc_mult * (c.dim / prefill_bn(h)) *
                     sizeof(float4),
                 true));
     step(dalloc(&ws.value, ws.rows_alloc * c.dim * 2, true));
@@ -288,7 +290,7 @@ int engram_create(const engram_config* cfg, const engram_weights* w, engram_t** 
         mx ? CU_TENSOR_MAP_DATA_TYPE_UINT8 : CU_TENSOR_MAP_DATA_TYPE_BFLOAT16;
     const int elem = mx ? 1 : 2;
     const void* act = mx ? static_cast<const void*>(ws.staged_q) : static_cast<const void*>(ws.staged);
-    bool ok = make_map(&h->tm_w_n, h->wkv, dt, elem, K, N, mx ? kBNPrefillMx : kBNPrefill) &&
+    bool ok = make_map(&h->tm_w_n, h->wkv, dt, elem, K, N, prefill_bn(h)) &&
               make_map(&h->tm_act_m, act, dt, elem, K, ws.rows_alloc, kBM);
     for (int i = 0; i < 16 && ok; ++i)
         ok = make_map(&h->tm_act_n[i], act, dt, elem, K, ws.rows_alloc, 16 * (i + 1));

@@ -15,6 +15,7 @@ constexpr int kBM = 128;          // MMA M: rows of the TMEM accumulator
 constexpr int kBNPrefill = 256;   // kv columns per prefill tile, bf16 wkv
 constexpr int kBNPrefillMx = 128; // kv columns per prefill tile, MXFP8 wkv (TMEM holds the
                                   // two accumulators plus a scale-factor slot per stage)
+constexpr int kBNPrefillMxWide = 224;  // the same when it divides dim (2 x 224 + 4 x 16 = 512)
 constexpr int kKBlockBytes = 128; // bytes of K per pipeline stage (one swizzle row)
 constexpr int kGemmSmemBytes = 192 * 1024 + 2048;  // > half an SM: one CTA per SM
 constexpr int kFusedSmemBytes = 225 * 1024;       // fused decode kernel

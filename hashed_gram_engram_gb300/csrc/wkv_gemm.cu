@@ -21,9 +21,12 @@
 // programmatic-launch wait, overlapping the gather kernel.
 //
 // MXFP8 wkv: e4m3 codes of the rows (quantised by the gather) times e4m3
-// weights, tcgen05 kind::mxf8f6f4 block_scale, 128 x 128 tiles.  Each stage
-// also brings the two 512-byte scale-factor atoms of its k-block (tokens,
-// weights); the MMA thread copies them into that stage's TMEM scale slot
+// weights, tcgen05 kind::mxf8f6f4 block_scale, 128 x 224 tiles when 224
+// divides dim (two accumulators of 224 columns and four 16-column scale
+// slots fill the 512 TMEM columns), else 128 x 128.  Each stage also brings
+// the 512-byte scale-factor atoms of its k-block (the tokens', and one per
+// 128 tile rows of the weights', packed per tile at create); the MMA
+// thread copies them into that stage's TMEM scale slot
 // with tcgen05.cp right before the stage's MMAs.  A slot is rewritten only
 // after the MMAs that read it have completed (the producer reuses a stage
 // only after their commit), so one slot per stage suffices.
@@ -81,17 +84,18 @@ __device__ __forceinline__ void fail(int* abort_flag, unsigned* err) {
     atomicOr(err, ENGRAM_DEVERR_TIMEOUT);
 }
 
-template <bool kMx>
+template <bool kMx, int BN>
 __global__ void __launch_bounds__(kThreads, 1)
     wkv_gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
                     const GemmArgs a) {
-    constexpr int BN = kMx ? kBNPrefillMx : kBNPrefill;
     constexpr int kKElems = kMx ? 128 : 64;  // k per 128-byte block
-    constexpr uint32_t kAtoms = kMx ? 1024u : 0u;  // scale atoms per stage
+    constexpr uint32_t kBAtoms = (BN + 127) / 128;  // weight scale atoms per k-block
+    constexpr uint32_t kAtoms = kMx ? 512u * (1u + kBAtoms) : 0u;  // scale atoms per stage
     extern __shared__ uint8_t smem_raw[];
     uint8_t* smem = reinterpret_cast<uint8_t*>(
         (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~static_cast<uintptr_t>(1023));
-    const uint32_t stage_bytes = a.a_bytes + a.b_bytes + kAtoms;
+    const uint32_t tx_bytes = a.a_bytes + a.b_bytes + kAtoms;  // copied per stage
+    const uint32_t stage_bytes = (tx_bytes + 1023u) & ~1023u;   // stride: swizzle atoms stay aligned
     uint64_t* full = reinterpret_cast<uint64_t*>(smem + a.stages * stage_bytes);
     uint64_t* empty = full + kMaxStages;
     uint64_t* tfull = empty + kMaxStages;
@@ -167,12 +171,12 @@ __global__ void __launch_bounds__(kThreads, 1)
                     }
                     uint8_t* sw = smem + s * stage_bytes + a.a_bytes;
                     const int x_row = u.m * kBM;
-                    mbar_arrive_expect_tx(&full[s], stage_bytes);
+                    mbar_arrive_expect_tx(&full[s], tx_bytes);
                     tma_load_2d_hint(sw, &tmB, &full[s], kb * kKElems, u.n * BN, pol_w);
                     if constexpr (kMx)
                         bulk_load(sw + a.b_bytes + 512,
-                                  a.sfb + (static_cast<int64_t>(u.n) * a.kb128 + kb) * 512, 512,
-                                  &full[s]);
+                                  a.sfb + (static_cast<int64_t>(u.n) * a.kb128 + kb) * (512 * kBAtoms),
+                                  512 * kBAtoms, &full[s]);
                     if (!waited) {
                         pro_kb[npro] = kb;
                         pro_row[npro] = x_row;
@@ -220,11 +224,13 @@ __global__ void __launch_bounds__(kThreads, 1)
                     const uint64_t bdesc = smem_desc_sw128(sa + a.a_bytes);
                     if constexpr (kMx) {
                         // this stage's 16-column scale slot: tokens' cells at
-                        // +0, wkv's at +8
+                        // +0, wkv's at +8 (4 columns per 128 tile rows)
                         const uint32_t sf = tmem_base + 2u * BN + 16u * static_cast<uint32_t>(s);
                         const uint32_t atoms = sa + a.a_bytes + a.b_bytes;
                         tmem_cp_atom(sf, smem_desc_atom(atoms));
-                        tmem_cp_atom(sf + 8, smem_desc_atom(atoms + 512));
+#pragma unroll
+                        for (uint32_t b = 0; b < kBAtoms; ++b)
+                            tmem_cp_atom(sf + 8 + 4 * b, smem_desc_atom(atoms + 512 * (1 + b)));
 #pragma unroll
                         for (int k = 0; k < 4; ++k)  // 4 x K32, scale byte k of each cell
                             mma_mxf8_ss(d_tmem, adesc + 2 * k, bdesc + 2 * k,
@@ -364,18 +370,21 @@ __global__ void __launch_bounds__(kThreads, 1)
     if (warp == 1) tmem_dealloc(tmem_base, kTmemCols);
 }
 
-// E8M0 [N/32][K/32] block scales of wkv -> atoms [N/128][K/128][512]
-// (byte 16*i + 4*j + b of atom (g, kb) = scale of row 128g + 32j + i,
-// k-block 4kb + b).
-__global__ void pack_scale_atoms_kernel(const uint8_t* ws, uint8_t* atoms, int64_t N, int64_t K) {
+// E8M0 [N/32][K/32] block scales of wkv -> atoms [N/bn][K/128][ceil(bn/128)][512]
+// per prefill tile of bn rows (byte 16*i + 4*j + b of atom (tile, kb, a) =
+// scale of tile row 128a + 32j + i, k-block 4kb + b; rows past the tile,
+// which no MMA reads, get 2^0).
+__global__ void pack_scale_atoms_kernel(const uint8_t* ws, uint8_t* atoms, int64_t N, int64_t K,
+                                        int64_t bn) {
     const int64_t o = static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x;
-    const int64_t kb128 = K / 128;
-    if (o >= N * K / 32) return;
+    const int64_t kb128 = K / 128, nb = (bn + 127) / 128;
+    if (o >= (N / bn) * kb128 * nb * 512) return;
     const int64_t w = o & 511, atom = o >> 9;
-    const int64_t g = atom / kb128, kb = atom - g * kb128;
-    const int64_t row = 128 * g + 32 * ((w >> 2) & 3) + (w >> 4);
+    const int64_t a = atom % nb, tk = atom / nb;
+    const int64_t tile = tk / kb128, kb = tk - tile * kb128;
+    const int64_t r = 128 * a + 32 * ((w >> 2) & 3) + (w >> 4);
     const int64_t k32 = 4 * kb + (w & 3);
-    atoms[o] = ws[(row >> 5) * (K >> 5) + k32];
+    atoms[o] = r < bn ? ws[((tile * bn + r) >> 5) * (K >> 5) + k32] : static_cast<uint8_t>(127);
 }
 
 // Staged MXFP8 scale atoms -> plain [T][K/32], for validation.
@@ -390,9 +399,10 @@ __global__ void unpack_scale_atoms_kernel(const uint8_t* atoms, uint8_t* out, in
 }  // namespace
 
 cudaError_t pack_scale_atoms(const engram_handle* h, cudaStream_t s) {
-    const int64_t n = h->N * h->K / 32;
+    const int64_t bn = prefill_bn(h);
+    const int64_t n = (h->N / bn) * ((bn + 127) / 128) * (h->K / 128) * 512;
     pack_scale_atoms_kernel<<<static_cast<unsigned>((n + 255) / 256), 256, 0, s>>>(
-        h->wkv_scale, h->ws.wsf_atoms, h->N, h->K);
+        h->wkv_scale, h->ws.wsf_atoms, h->N, h->K, bn);
     return cudaGetLastError();
 }
 
@@ -405,12 +415,15 @@ cudaError_t launch_unpack_scales(const engram_handle* h, uint8_t* out, int64_t T
 }
 
 cudaError_t gemm_setup_attributes() {
-    cudaError_t e = cudaFuncSetAttribute(wkv_gemm_kernel<false>,
-                                         cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                         kGemmSmemBytes);
-    if (e != cudaSuccess) return e;
-    return cudaFuncSetAttribute(wkv_gemm_kernel<true>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                kGemmSmemBytes);
+    const void* fns[] = {reinterpret_cast<const void*>(wkv_gemm_kernel<false, kBNPrefill>),
+                         reinterpret_cast<const void*>(wkv_gemm_kernel<true, kBNPrefillMx>),
+                         reinterpret_cast<const void*>(wkv_gemm_kernel<true, kBNPrefillMxWide>)};
+    for (const void* fn : fns) {
+        const cudaError_t e =
+            cudaFuncSetAttribute(fn, cudaFuncAttributeMaxDynamicSharedMemorySize, kGemmSmemBytes);
+        if (e != cudaSuccess) return e;
+    }
+    return cudaSuccess;
 }
 
 static cudaError_t launch(const void* fn, int grid, const CUtensorMap& tmA, const CUtensorMap& tmB,
@@ -431,7 +444,10 @@ static cudaError_t launch(const void* fn, int grid, const CUtensorMap& tmA, cons
 }
 
 int prefill_bn(const engram_handle* h) {
-    return h->cfg.wkv_format == ENGRAM_WKV_MXFP8 ? kBNPrefillMx : kBNPrefill;
+    if (h->cfg.wkv_format != ENGRAM_WKV_MXFP8) return kBNPrefill;
+    // The widest MXFP8 tile whose two accumulators and the stages' scale
+    // slots fit TMEM, when it divides dim (then it divides N too).
+    return h->cfg.dim % kBNPrefillMxWide == 0 ? kBNPrefillMxWide : kBNPrefillMx;
 }
 
 cudaError_t launch_wkv_tokens_m(const engram_handle* h, const void* hidden, int64_t hs_t,
@@ -448,8 +464,12 @@ cudaError_t launch_wkv_tokens_m(const engram_handle* h, const void* hidden, int6
     a.bn = bn;
     a.a_bytes = kBM * kKBlockBytes;
     a.b_bytes = static_cast<uint32_t>(bn) * kKBlockBytes;
-    a.stages = static_cast<int>(kStageBudget / (a.a_bytes + a.b_bytes + (mx ? 1024 : 0)));
+    const uint32_t atoms = mx ? 512u * (1u + static_cast<uint32_t>((bn + 127) / 128)) : 0u;
+    const uint32_t stride = (a.a_bytes + a.b_bytes + atoms + 1023u) & ~1023u;
+    a.stages = static_cast<int>(kStageBudget / stride);
     if (a.stages > kMaxStages) a.stages = kMaxStages;
+    // MXFP8: two accumulators plus a 16-column scale slot per stage in TMEM
+    if (mx && a.stages > (512 - 2 * bn) / 16) a.stages = (512 - 2 * bn) / 16;
     a.idesc = idesc_bf16(kBM, kBNPrefill);
     a.D = static_cast<int>(h->cfg.dim);
     a.H = static_cast<int>(h->cfg.hc_mult);
@@ -464,8 +484,12 @@ cudaError_t launch_wkv_tokens_m(const engram_handle* h, const void* hidden, int6
     a.sfb = h->ws.wsf_atoms;
     a.err = h->ws.err;
     const int grid = a.total < h->num_sms ? a.total : h->num_sms;
-    return launch(mx ? reinterpret_cast<const void*>(wkv_gemm_kernel<true>)
-                     : reinterpret_cast<const void*>(wkv_gemm_kernel<false>),
+    const void* fn =
+        !mx ? reinterpret_cast<const void*>(wkv_gemm_kernel<false, kBNPrefill>)
+            : (bn == kBNPrefillMxWide
+                   ? reinterpret_cast<const void*>(wkv_gemm_kernel<true, kBNPrefillMxWide>)
+                   : reinterpret_cast<const void*>(wkv_gemm_kernel<true, kBNPrefillMx>));
+    return launch(fn,
                   grid, h->tm_act_m, h->tm_w_n, a, s, pdl);
 }
 
