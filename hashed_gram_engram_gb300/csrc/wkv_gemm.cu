@@ -152,6 +152,8 @@ __global__ void __launch_bounds__(kThreads, 1)
             bool ok = true, waited = false;
             int pro_kb[kMaxStages], pro_row[kMaxStages], pro_s[kMaxStages];
             int npro = 0;
+            int s = 0;         // stage of the next iteration
+            uint32_t par = 0;  // its phase parity
             while (ok && sch.next(u)) {
                 for (int kb = 0; kb < a.k_blocks; ++kb) {
                     if (!waited && issued == a.stages) {
@@ -163,8 +165,6 @@ __global__ void __launch_bounds__(kThreads, 1)
                         for (int i = 0; i < npro; ++i)
                             load_x(pro_s[i], pro_kb[i], pro_row[i]);
                     }
-                    const int s = static_cast<int>(issued % a.stages);
-                    const uint32_t par = static_cast<uint32_t>((issued / a.stages) & 1);
                     if (!mbar_wait(&empty[s], par ^ 1u, abort_v)) {
                         ok = false;
                         break;
@@ -186,6 +186,10 @@ __global__ void __launch_bounds__(kThreads, 1)
                         load_x(s, kb, x_row);
                     }
                     ++issued;
+                    if (++s == a.stages) {
+                        s = 0;
+                        par ^= 1u;
+                    }
                 }
             }
             if (!waited) {
@@ -200,8 +204,19 @@ __global__ void __launch_bounds__(kThreads, 1)
             Schedule sch(a);
             Unit u;
             bool ok = true;
-            int64_t it = 0;
             int nu = 0;
+            // The issuing thread's scalar latency sets the pace: the stage,
+            // its parity, descriptors and scale slot advance incrementally
+            // (a descriptor's address field is the byte address / 16).
+            int s = 0;
+            uint32_t par = 0;
+            const uint32_t sa0 = smem_addr(smem);
+            const uint64_t adesc0 = smem_desc_sw128(sa0);
+            const uint64_t bdesc0 = smem_desc_sw128(sa0 + a.a_bytes);
+            const uint64_t dstep = stage_bytes >> 4;
+            uint32_t sa = sa0;
+            uint64_t adesc = adesc0, bdesc = bdesc0;
+            uint32_t sf = tmem_base + 2u * BN;  // MXFP8: this stage's scale slot
             while (ok && sch.next(u)) {
                 const int acc = nu & 1;
                 const uint32_t apar = static_cast<uint32_t>((nu >> 1) & 1);
@@ -212,20 +227,14 @@ __global__ void __launch_bounds__(kThreads, 1)
                 tc_fence_after();
                 const uint32_t d_tmem = tmem_base + static_cast<uint32_t>(acc * BN);
                 for (int kb = 0; kb < a.k_blocks; ++kb) {
-                    const int s = static_cast<int>(it % a.stages);
-                    const uint32_t par = static_cast<uint32_t>((it / a.stages) & 1);
                     if (!mbar_wait(&full[s], par, abort_v)) {
                         ok = false;
                         break;
                     }
                     tc_fence_after();
-                    const uint32_t sa = smem_addr(smem + s * stage_bytes);
-                    const uint64_t adesc = smem_desc_sw128(sa);
-                    const uint64_t bdesc = smem_desc_sw128(sa + a.a_bytes);
                     if constexpr (kMx) {
                         // this stage's 16-column scale slot: tokens' cells at
                         // +0, wkv's at +8 (4 columns per 128 tile rows)
-                        const uint32_t sf = tmem_base + 2u * BN + 16u * static_cast<uint32_t>(s);
                         const uint32_t atoms = sa + a.a_bytes + a.b_bytes;
                         tmem_cp_atom(sf, smem_desc_atom(atoms));
 #pragma unroll
@@ -243,7 +252,19 @@ __global__ void __launch_bounds__(kThreads, 1)
                                         (kb > 0 || k > 0) ? 1u : 0u);
                     }
                     mma_commit(&empty[s]);
-                    ++it;
+                    if (++s == a.stages) {
+                        s = 0;
+                        par ^= 1u;
+                        sa = sa0;
+                        adesc = adesc0;
+                        bdesc = bdesc0;
+                        sf = tmem_base + 2u * BN;
+                    } else {
+                        sa += stage_bytes;
+                        adesc += dstep;
+                        bdesc += dstep;
+                        sf += 16u;
+                    }
                 }
                 if (!ok) break;
                 mma_commit(&tfull[acc]);
