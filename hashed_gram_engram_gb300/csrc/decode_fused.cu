@@ -115,6 +115,37 @@ __device__ __forceinline__ int first_granule(int cta, int n, int G) {
     return static_cast<int>(static_cast<int64_t>(cta) * n / G);
 }
 
+// out = hidden + g * value at 16 dims of every hc copy of one token, rounded
+// to bf16; a masked token keeps hidden's bits.  hin: hidden there, v: the
+// value (fp32).
+__device__ __forceinline__ void residual16(uint16_t* out, int64_t os_t, int64_t os_h, int t, int d,
+                                           int H, const uint4 (&hin)[kMaxCopies][2],
+                                           const float* v, const float* g, bool active) {
+#pragma unroll
+    for (int h = 0; h < kMaxCopies; ++h) {
+        if (h >= H) continue;
+        uint4 o0 = hin[h][0], o1 = hin[h][1];
+        if (active) {
+            const float gh = g[h];
+            const uint32_t w0[4] = {o0.x, o0.y, o0.z, o0.w};
+            const uint32_t w1[4] = {o1.x, o1.y, o1.z, o1.w};
+            uint32_t p0[4], p1[4];
+#pragma unroll
+            for (int k = 0; k < 4; ++k) {
+                p0[k] = pack_bf16x2(fmaf(gh, v[2 * k], bf16lo(w0[k])),
+                                    fmaf(gh, v[2 * k + 1], bf16hi(w0[k])));
+                p1[k] = pack_bf16x2(fmaf(gh, v[8 + 2 * k], bf16lo(w1[k])),
+                                    fmaf(gh, v[8 + 2 * k + 1], bf16hi(w1[k])));
+            }
+            o0 = make_uint4(p0[0], p0[1], p0[2], p0[3]);
+            o1 = make_uint4(p1[0], p1[1], p1[2], p1[3]);
+        }
+        uint16_t* op = out + t * os_t + h * os_h + d;
+        st_v4(op, o0);
+        st_v4(op + 8, o1);
+    }
+}
+
 __device__ __forceinline__ void fail(int* abort_flag, unsigned* err) {
     *reinterpret_cast<volatile int*>(abort_flag) = 1;
     atomicOr(err, ENGRAM_DEVERR_TIMEOUT);
@@ -247,6 +278,15 @@ __global__ void __launch_bounds__(kThreads, 1)
     // MXFP8 scale cells, 8 columns per k-block each (every region 8-aligned)
     const uint32_t tm_sfa = tmem_base + kMaxFusedSlice;                     // tokens
     const uint32_t tm_sfb = tm_sfa + 8u * static_cast<uint32_t>(a.kb128);  // weights
+
+    // One token tile and at most kEarlyChunks 16-dim value chunks: the
+    // epilogue warps load the residual's operands (the value from TMEM, hidden
+    // at the CTA's value dims, which no other CTA touches) before grid
+    // barrier 2, so after barrier 3 only the gates are waited for.
+    constexpr int kEarlyChunks = 3;
+    const bool early = a.mtiles == 1 && (vlen >> 4) <= kEarlyChunks;
+    float ev[kEarlyChunks][16];
+    uint4 eh[kEarlyChunks][kMaxCopies][2];
 
     if (warp == 0) {
         if (lane == 0) {
@@ -428,14 +468,6 @@ __global__ void __launch_bounds__(kThreads, 1)
             // before the first MMA, written once the first tiles are in flight
             constexpr int kMaxKb128 = 16;  // (TMEM budget: 256 + 16 * K/128 <= 512)
             uint32_t sfw[kMaxKb128];
-            if constexpr (kMx) {  // loads first; the TMEM stores wait for the first tiles
-                const int t = q * 32 + lane;
-#pragma unroll
-                for (int b = 0; b < kMaxKb128; ++b)
-                    sfw[b] = b < a.kb128 ? __ldcg(reinterpret_cast<const unsigned*>(
-                                               a.staged_s + sf_atom_offset(t, 4 * b, a.kb128)))
-                                         : 0u;
-            }
             auto token_scales = [&]() {
 #pragma unroll
                 for (int b = 0; b < kMaxKb128; ++b)
@@ -462,6 +494,15 @@ __global__ void __launch_bounds__(kThreads, 1)
                 for (int kb = 0; kb < first; ++kb) load_x(kb);
             }
             __syncwarp();
+            // (after the first tiles: the proxy fence would wait for these loads)
+            if constexpr (kMx) {
+                const int t = q * 32 + lane;
+#pragma unroll
+                for (int b = 0; b < kMaxKb128; ++b)
+                    sfw[b] = b < a.kb128 ? __ldcg(reinterpret_cast<const unsigned*>(
+                                               a.staged_s + sf_atom_offset(t, 4 * b, a.kb128)))
+                                         : 0u;
+            }
             if (kMx) token_scales();  // (the first MMAs wait for the scales)
             if (etid == 0) {
                 // the rest, each as soon as its stage's MMAs are done
@@ -587,12 +628,42 @@ __global__ void __launch_bounds__(kThreads, 1)
             }
             // the residual reads hidden at the value dims: start it towards L2
             // (plain per-line prefetches; bulk ones would queue on the TMA unit)
-            if (live && vlen > 0)
+            if (live && vlen > 0 && !early)
                 for (int h = 0; h < a.H; ++h) {
                     const uint16_t* hp = a.hidden + t * a.hs_t + h * a.hs_h + v0;
                     prefetch_line_l2(hp);
                     prefetch_line_l2(hp + vlen - 1);
                 }
+        }
+        if (early && go) {
+            const int t = q * 32 + lane;
+            const bool live = t < a.T;
+#pragma unroll
+            for (int ci = 0; ci < kEarlyChunks; ++ci) {
+                if (ci >= (vlen >> 4)) break;
+                uint32_t r[16];  // every lane loads (tcgen05.ld is warp-wide)
+                const uint32_t va = tmem_base + lane_base + static_cast<uint32_t>(ci * 16);
+                tmem_ld16(va, r);
+                if (a.dual) {
+                    uint32_t r2[16];
+                    tmem_ld16(va + 256u, r2);
+                    tmem_ld_wait();
+#pragma unroll
+                    for (int e = 0; e < 16; ++e)
+                        r[e] = __float_as_uint(__uint_as_float(r[e]) + __uint_as_float(r2[e]));
+                }
+                tmem_ld_wait();
+#pragma unroll
+                for (int e = 0; e < 16; ++e) ev[ci][e] = __uint_as_float(r[e]);
+#pragma unroll
+                for (int h = 0; h < kMaxCopies; ++h) {
+                    if (live && h < a.H) {
+                        const uint16_t* hp = a.hidden + t * a.hs_t + h * a.hs_h + v0 + ci * 16;
+                        eh[ci][h][0] = ld_nc_v4(hp);
+                        eh[ci][h][1] = ld_nc_v4(hp + 8);
+                    }
+                }
+            }
         }
         // every record this CTA owes is written: grid barrier 2 (the release
         // add of one thread covers the CTA's writes ordered before it by the
@@ -675,7 +746,23 @@ __global__ void __launch_bounds__(kThreads, 1)
     // Residual at this CTA's value dims: thread = token (TMEM lane); the
     // value comes straight from the accumulator.
     const int nchunk_v = vlen >> 4;
-    if (warp >= 2 && warp < 6 && nchunk_v > 0) {
+    if (warp >= 2 && warp < 6 && nchunk_v > 0 && early) {
+        const int q = warp & 3;
+        const int t = q * 32 + lane;
+        if (t < a.T) {
+            const bool active = a.mask == nullptr || a.mask[t] != 0;
+            float g[kMaxCopies];
+#pragma unroll
+            for (int h = 0; h < kMaxCopies; ++h)
+                g[h] = (active && h < a.H) ? __ldcg(a.gate_out + static_cast<int64_t>(t) * a.H + h)
+                                           : 0.f;
+#pragma unroll
+            for (int ci = 0; ci < kEarlyChunks; ++ci)
+                if (ci < nchunk_v)
+                    residual16(a.out, a.os_t, a.os_h, t, v0 + ci * 16, a.H, eh[ci], ev[ci], g,
+                               active);
+        }
+    } else if (warp >= 2 && warp < 6 && nchunk_v > 0) {
         const int q = warp & 3;
         const uint32_t lane_base = static_cast<uint32_t>(q * 32) << 16;
         for (int m = 0; m < a.mtiles; ++m) {
@@ -713,30 +800,10 @@ __global__ void __launch_bounds__(kThreads, 1)
                         hin[h][1] = ld_nc_v4(hp + 8);
                     }
                 }
+                float v[16];
 #pragma unroll
-                for (int h = 0; h < kMaxCopies; ++h) {
-                    if (h >= a.H) continue;
-                    uint4 o0 = hin[h][0], o1 = hin[h][1];
-                    if (active) {
-                        const float gh = g[h];
-                        const uint32_t w0[4] = {o0.x, o0.y, o0.z, o0.w};
-                        const uint32_t w1[4] = {o1.x, o1.y, o1.z, o1.w};
-                        uint32_t p0[4], p1[4];
-#pragma unroll
-                        for (int k = 0; k < 4; ++k) {
-                            p0[k] = pack_bf16x2(fmaf(gh, __uint_as_float(r[2 * k]), bf16lo(w0[k])),
-                                                fmaf(gh, __uint_as_float(r[2 * k + 1]), bf16hi(w0[k])));
-                            p1[k] = pack_bf16x2(
-                                fmaf(gh, __uint_as_float(r[8 + 2 * k]), bf16lo(w1[k])),
-                                fmaf(gh, __uint_as_float(r[8 + 2 * k + 1]), bf16hi(w1[k])));
-                        }
-                        o0 = make_uint4(p0[0], p0[1], p0[2], p0[3]);
-                        o1 = make_uint4(p1[0], p1[1], p1[2], p1[3]);
-                    }
-                    uint16_t* op = a.out + t * a.os_t + h * a.os_h + d;
-                    st_v4(op, o0);
-                    st_v4(op + 8, o1);
-                }
+                for (int e = 0; e < 16; ++e) v[e] = __uint_as_float(r[e]);
+                residual16(a.out, a.os_t, a.os_h, t, d, a.H, hin, v, g, active);
             }
         }
     }
