@@ -20,7 +20,8 @@
  *
  * Pins (tests marked "not gpu"): layout primes against sympy.nextprime;
  * bf16/e4m3/E8M0 decoding against torch's dtype conversions and ldexp;
- * e4m3 and bf16 rounding against torch casts and constructed ties; the
+ * e4m3 and bf16 rounding against torch casts and constructed ties; the fp8
+ * table gather against torch's e4m3 decode with exact power-of-two scaling; the
  * contraction against numpy's float64 matmul; the gate against closed
  * forms (identity projection, q = 0, sign symmetry, all-False mask).
  */
@@ -185,6 +186,37 @@ void oracle_gather(const uint16_t* table, const int64_t* row_offset,
             }
             const uint16_t* src = table + (row_offset[c] + id) * E;
             for (int64_t j = 0; j < E; ++j) dst[j] = src[j];
+        }
+    }
+    if (n_bad) *n_bad = bad;
+}
+
+/* The same gather from an fp8 table (class ParallelEngramEmbedding: rows
+ * stored as e4m3 with one ue8m0 scale per 32 consecutive elements,
+ * dequantized on lookup into bf16): element j of a row is
+ * e4m3(codes[row, j]) * 2^(scales[row, j / 32] - 127), rounded to bf16
+ * (nearest, ties to even).  codes: [total_rows, E] bytes; scales:
+ * [total_rows, E / 32] bytes; E a multiple of 32.  Bad ids as above. */
+void oracle_gather_e4m3(const uint8_t* codes, const uint8_t* scales,
+                        const int64_t* row_offset, const int64_t* rows, int64_t C,
+                        int64_t E, const int32_t* ids, int64_t ids_stride, int64_t T,
+                        uint16_t* out, int64_t* n_bad) {
+    int64_t bad = 0;
+    for (int64_t t = 0; t < T; ++t) {
+        for (int64_t c = 0; c < C; ++c) {
+            int64_t id = ids[t * ids_stride + c];
+            uint16_t* dst = out + (t * C + c) * E;
+            if (id < 0 || id >= rows[c]) {
+                ++bad;
+                for (int64_t j = 0; j < E; ++j) dst[j] = 0;
+                continue;
+            }
+            int64_t row = row_offset[c] + id;
+            for (int64_t j = 0; j < E; ++j) {
+                double v = oracle_e4m3_to_f64(codes[row * E + j]) *
+                           oracle_e8m0_to_f64(scales[row * (E / 32) + j / 32]);
+                dst[j] = oracle_f64_to_bf16(v);
+            }
         }
     }
     if (n_bad) *n_bad = bad;

@@ -15,7 +15,7 @@ import numpy as np
 
 __all__ = [
     "build_oracle", "lib", "bf16_to_f64", "e4m3_to_f64", "e8m0_to_f64",
-    "f64_to_e4m3", "f64_to_bf16", "layout", "gather", "wkv_bf16", "wkv_mxfp8",
+    "f64_to_e4m3", "f64_to_bf16", "layout", "gather", "gather_e4m3", "wkv_bf16", "wkv_mxfp8",
     "mx_quantize", "wkv_mxfp8_qact", "gate", "forward",
 ]
 
@@ -63,6 +63,8 @@ def lib():
             L.oracle_layout.restype = ctypes.c_int
             L.oracle_gather.argtypes = [vp, vp, vp, i64, i64, vp, i64, i64, vp, vp]
             L.oracle_gather.restype = None
+            L.oracle_gather_e4m3.argtypes = [vp, vp, vp, vp, i64, i64, vp, i64, i64, vp, vp]
+            L.oracle_gather_e4m3.restype = None
             L.oracle_wkv_bf16.argtypes = [vp, i64, i64, vp, i64, vp]
             L.oracle_wkv_bf16.restype = None
             L.oracle_wkv_mxfp8.argtypes = [vp, i64, i64, vp, vp, i64, vp]
@@ -153,6 +155,26 @@ def gather(table_bits, row_offset, rows, ids, E):
     return out, int(nbad[0])
 
 
+def gather_e4m3(codes, scales, row_offset, rows, ids, E):
+    """gather() from an fp8 table: e4m3 codes [total_rows, E] with one ue8m0
+    scale byte per 32 elements [total_rows, E / 32], dequantized to bf16 bits
+    (class ParallelEngramEmbedding).  Returns (rows uint16 [T, C, E], bad ids)."""
+    codes = _c(codes, np.uint8)
+    scales = _c(scales, np.uint8)
+    assert E % 32 == 0 and codes.shape[-1] == E and scales.shape[-1] == E // 32
+    row_offset = _c(np.asarray(row_offset, np.int64), np.int64)
+    rows = _c(np.asarray(rows, np.int64), np.int64)
+    ids = np.asarray(ids)
+    assert ids.dtype == np.int32 and ids.ndim == 2 and ids.strides[1] == 4
+    T, C = ids.shape
+    stride = ids.strides[0] // 4 if T > 0 else C
+    out = np.zeros((T, C, E), np.uint16)
+    nbad = np.zeros(1, np.int64)
+    lib().oracle_gather_e4m3(_p(codes), _p(scales), _p(row_offset), _p(rows), C, E,
+                             ctypes.c_void_p(ids.ctypes.data), stride, T, _p(out), _p(nbad))
+    return out, int(nbad[0])
+
+
 def wkv_bf16(A_bits, W_bits):
     """kv = A . W^T in fp64 (Engram.forward's wkv on the flattened rows)."""
     A_bits = _c(A_bits, np.uint16)
@@ -225,13 +247,17 @@ def gate(hidden_bits, kv, q_bits, k_bits, mask, eps=1e-6, clamp=1e-6):
 
 
 def forward(table_bits, row_offset, rows, ids, E, W, hidden_bits, q_bits, k_bits,
-            mask=None, Ws=None, eps=1e-6, clamp=1e-6, quantize_act=False):
+            mask=None, Ws=None, eps=1e-6, clamp=1e-6, quantize_act=False, table_scale=None):
     """The whole layer: gather -> wkv -> gate/residual.
 
-    W is bf16 bits [N, K] (Ws None) or e4m3 codes with E8M0 scales Ws.
-    With quantize_act the MXFP8 path quantises the rows first.
-    Returns the gate() dict plus rows, kv and the bad-id count."""
-    rws, nbad = gather(table_bits, row_offset, rows, ids, E)
+    The table is bf16 bits, or (table_scale given) e4m3 codes with one ue8m0
+    scale per 32 elements.  W is bf16 bits [N, K] (Ws None) or e4m3 codes
+    with E8M0 scales Ws.  With quantize_act the MXFP8 path quantises the
+    rows first.  Returns the gate() dict plus rows, kv and the bad-id count."""
+    if table_scale is None:
+        rws, nbad = gather(table_bits, row_offset, rows, ids, E)
+    else:
+        rws, nbad = gather_e4m3(table_bits, table_scale, row_offset, rows, ids, E)
     T, C, _ = rws.shape
     A = rws.reshape(T, C * E)
     if Ws is None:

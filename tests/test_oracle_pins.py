@@ -314,3 +314,52 @@ def test_forward_tiny_end_to_end_composition():
     mask = W.bits(d["token_mask"]).astype(bool)
     assert 0 < mask.sum() < T
     assert np.array_equal(r["out_bf16"][~mask], W.bits(d["hidden"])[~mask])
+
+
+def test_gather_e4m3_table_matches_torch_dequant_and_indexing():
+    """fp8 table rows (class ParallelEngramEmbedding: e4m3 with one ue8m0 scale
+    per 32 elements, dequantized to bf16 on lookup) against torch's own
+    float8_e4m3fn -> float64 decode, an exact power-of-two scaling, and its
+    RTNE cast to bfloat16; plus direct row indexing and bad ids."""
+    E = 64
+    scale_bytes = [0, 1, 9, 60, 113, 118, 121, 127, 128, 140, 200, 253, 254]
+    # every code appears in each block position, under every scale byte
+    codes = np.tile(np.arange(256, dtype=np.uint8).reshape(4, 64), (len(scale_bytes), 1))
+    scales = np.repeat(np.array(scale_bytes, np.uint8), 4)[:, None].repeat(2, axis=1).copy()
+    scales[::2, 1] = 127  # a second block with another scale in half of the rows
+    n = codes.shape[0]
+    rows = np.array([n], np.int64)
+    ids = np.arange(n, dtype=np.int32).reshape(-1, 1)
+    got, bad = oracle.gather_e4m3(codes, scales, [0], rows, ids, E)
+    assert bad == 0
+    dq = torch.from_numpy(codes).view(torch.float8_e4m3fn).to(torch.float64)
+    mult = torch.from_numpy(np.ldexp(1.0, scales.astype(np.int64) - 127))  # exact
+    ref = (dq * mult.repeat_interleave(32, dim=1)).to(torch.bfloat16).view(torch.int16)
+    ref = ref.numpy().view(np.uint16)
+    g = got[:, 0, :]
+    refnan = ((ref & 0x7F80) == 0x7F80) & ((ref & 0x7F) != 0)
+    gotnan = ((g & 0x7F80) == 0x7F80) & ((g & 0x7F) != 0)
+    assert np.array_equal(refnan, gotnan)          # the NaN codes S.1111.111
+    assert refnan.sum() == 2 * len(scale_bytes)    # (0x7F and 0xFF once per scale byte)
+    assert np.array_equal(g[~refnan], ref[~refnan])
+
+    # rows by direct indexing: strided ids, per-column offsets, bad ids
+    rng = np.random.default_rng(5)
+    rws = np.array([7, 11, 13], np.int64)
+    off = W.row_offsets(rws)
+    tc = rng.integers(0, 256, (rws.sum(), E), dtype=np.uint8)
+    ts = rng.integers(110, 130, (rws.sum(), E // 32), dtype=np.uint8)
+    full = np.stack([rng.integers(0, r, 6) for r in rws], 1).astype(np.int32)
+    full = np.concatenate([full, np.full((6, 2), -9, np.int32)], 1)
+    idv = full[:, :3]                               # row stride 5 > C
+    out, bad = oracle.gather_e4m3(tc, ts, off, rws, idv, E)
+    assert bad == 0
+    one, _ = oracle.gather_e4m3(tc, ts, [0], [rws.sum()], (off[None, :] + idv).reshape(-1, 1)
+                                .astype(np.int32), E)
+    assert np.array_equal(out.reshape(-1, E), one[:, 0, :])
+    idv2 = idv.copy()
+    idv2[1, 2] = 13      # == rows[2]
+    idv2[4, 0] = -1
+    out2, bad2 = oracle.gather_e4m3(tc, ts, off, rws, idv2, E)
+    assert bad2 == 2 and not out2[1, 2].any() and not out2[4, 0].any()
+    assert np.array_equal(out2[0], out[0])
