@@ -10,8 +10,10 @@ so every step reads its weights from HBM; the rotation is captured in a
 CUDA graph and timed with CUDA events on its stream.  The single-step
 latency with L2 flushed (a 512 MB write) before every step is reported
 too.  Alongside: the MXFP8 decode (T = 64, dim 7168) and prefill
-(T = 4096) steps, and the offload step (T = 256, the 17 GB table in
-pinned host memory, every gathered row crossing the host link).
+(T = 4096) steps, the offload step (T = 256, the 17 GB table in
+pinned host memory, every gathered row crossing the host link), and the
+decode and offload steps again with an fp8 table (e4m3 rows with ue8m0
+scales per 32 elements, dequantized by the gather: half the row bytes).
 
   python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
 
@@ -48,7 +50,9 @@ def parse():
     p.add_argument("--no-cpu-baseline", action="store_true")
     p.add_argument("--no-mxfp8", action="store_true", help="skip the MXFP8 decode and prefill")
     p.add_argument("--no-offload", action="store_true",
-                   help="skip the offload workload (17 GB pinned host table)")
+                   help="skip the offload workloads (17 GB / 8.9 GB pinned host tables)")
+    p.add_argument("--no-e4m3-table", action="store_true",
+                   help="skip the workloads whose hash table is fp8 (e4m3 + ue8m0 per 32)")
     p.add_argument("--cpu-seconds", type=float, default=10.0)
     p.add_argument("--layers", type=int, default=6)
     p.add_argument("--case", choices=["decode", "prefill", "mxfp8_decode", "mxfp8_prefill"],
@@ -232,17 +236,23 @@ def reduce_max(x, world, device):
 
 
 def make_layer(W, Engram, wl, device_index, max_tokens, layer_seed, table=None):
-    """One layer of workload wl with its own seed; a given table is shared."""
+    """One layer of workload wl with its own seed; a given table is shared
+    (for an e4m3 table, the pair (codes, scales))."""
     import dataclasses
     wl_l = dataclasses.replace(wl, seed=wl.seed + 101 * layer_seed)
     if table is None:
-        table = W.make_table(wl_l, "cuda")
+        table = (W.make_table(wl_l, "cuda"), W.make_table_scale(wl_l, "cuda"))
+    elif not isinstance(table, tuple):
+        table = (table, None)
+    table, table_scale = table
     wts = W.make_weights(wl_l, "cuda")
+    wts["table_scale"] = table_scale
     layer = Engram(dim=wl.dim, hc_mult=wl.hc_mult, max_ngram_size=wl.max_ngram_size,
                    n_heads=wl.n_heads, head_dim=wl.head_dim, max_tokens=max_tokens,
                    table=table, rows=wl.rows, row_offset=W.row_offsets(wl.rows),
                    wkv=wts["wkv"], wkv_scale=wts["wkv_scale"], q_weight=wts["q_weight"],
-                   k_weight=wts["k_weight"], eps=wl.eps, clamp=wl.clamp, device=device_index)
+                   k_weight=wts["k_weight"], eps=wl.eps, clamp=wl.clamp, device=device_index,
+                   table_scale=table_scale)
     return wl_l, layer, table, wts
 
 
@@ -256,8 +266,16 @@ def algorithmic_bytes(wl):
     if mx:
         b += (wl.N // 32) * (wl.K // 32)
     if wl.table_location != "host":
-        b += wl.T * wl.K * 2
+        b += row_bytes(wl)
     return b
+
+
+def row_bytes(wl):
+    """Bytes of the T x C gathered rows: bf16, or e4m3 codes plus one scale
+    byte per 32 elements."""
+    if wl.table_format == "e4m3":
+        return wl.T * wl.K + wl.T * wl.K // 32
+    return wl.T * wl.K * 2
 
 
 def time_rotation(torch, layers, stream, steps, warmup):
@@ -543,38 +561,68 @@ def main():
             L["layer"].close()
         del mlayers
 
-    if not args.no_offload:
-        ow = W.OFFLOAD
-        need = ow.total_rows * ow.head_dim * 2
+    def offload_line(ow, seed0):
+        """The offload step: the table in pinned host memory, shared by the
+        rotated layers; every gathered row crosses the host link."""
+        fp8 = ow.table_format == "e4m3"
+        need = ow.total_rows * ow.head_dim * (1 + 1 / 32 if fp8 else 2)
         avail = W.host_memory_bytes()
         if avail is not None and avail < need + (8 << 30):
-            line["offload"] = {"workload": ow.name, "skipped":
-                               f"{need >> 30} GiB pinned table, {avail >> 30} GiB host memory free"}
-        else:
-            # the 17 GB table in pinned host memory, shared by the rotated
-            # layers; every gathered row crosses the host link
-            otable = W.make_table(ow, "cuda")
-            olayers = rotation_layers(ow, 4, ow.T, table=otable, seed0=70)
-            o_ms, o_steps, _, _ = time_rotation(torch, olayers, stream, args.steps, args.warmup)
-            o_ms = max_over_ranks(o_ms)
-            ob = algorithmic_bytes(ow)
-            host_b = ow.T * ow.K * 2
-            line["offload"] = {
-                "workload": ow.name, "T": ow.T, "tokens_per_s": world * ow.T / (o_ms * 1e-3),
-                "ms_per_step": o_ms, "steps": o_steps, "layers_rotated": 4,
-                "table": f"{need / 1e9:.2f} GB bf16 in pinned host memory",
-                "host_link": {"bytes_per_step": host_b,
-                              "GB_per_s": host_b / (o_ms * 1e-3) / 1e9,
-                              "rows_per_step": ow.T * ow.n_hash_cols},
-                "roofline": {"bound": "hbm", "kernel": "decode_fused_kernel (host table)",
-                             "achieved": ob / (o_ms * 1e-3) / 1e9, "peak": hbm_peak,
-                             "unit": "GB/s", "frac": ob / (o_ms * 1e-3) / 1e9 / hbm_peak,
-                             "algorithmic_bytes": ob, "peak_kind": peak_kind},
-            }
-            launches += o_steps
-            for L in olayers:
-                L["layer"].close()
-            del olayers, otable
+            return {"workload": ow.name, "skipped":
+                    f"{int(need) >> 30} GiB pinned table, {avail >> 30} GiB host memory free"}, 0
+        otable = (W.make_table(ow, "cuda"), W.make_table_scale(ow, "cuda"))
+        olayers = rotation_layers(ow, 4, ow.T, table=otable, seed0=seed0)
+        o_ms, o_steps, _, _ = time_rotation(torch, olayers, stream, args.steps, args.warmup)
+        o_ms = max_over_ranks(o_ms)
+        ob = algorithmic_bytes(ow)
+        host_b = row_bytes(ow)
+        kind = "e4m3 codes + ue8m0 scales per 32" if fp8 else "bf16"
+        res = {
+            "workload": ow.name, "T": ow.T, "tokens_per_s": world * ow.T / (o_ms * 1e-3),
+            "ms_per_step": o_ms, "steps": o_steps, "layers_rotated": 4,
+            "table": f"{need / 1e9:.2f} GB {kind} in pinned host memory",
+            "host_link": {"bytes_per_step": host_b,
+                          "GB_per_s": host_b / (o_ms * 1e-3) / 1e9,
+                          "rows_per_step": ow.T * ow.n_hash_cols},
+            "roofline": {"bound": "hbm", "kernel": "decode_fused_kernel (host table)",
+                         "achieved": ob / (o_ms * 1e-3) / 1e9, "peak": hbm_peak,
+                         "unit": "GB/s", "frac": ob / (o_ms * 1e-3) / 1e9 / hbm_peak,
+                         "algorithmic_bytes": ob, "peak_kind": peak_kind},
+        }
+        for L in olayers:
+            L["layer"].close()
+        del olayers, otable
+        return res, o_steps
+
+    if not args.no_offload:
+        line["offload"], n = offload_line(W.OFFLOAD, 70)
+        launches += n
+
+    if not args.no_e4m3_table:
+        # fp8 tables (the pages' storage): the decode rotation and the
+        # offload step with e4m3 rows and ue8m0 scales, dequantized by the gather
+        ew = W.DECODE_E4M3
+        elayers = rotation_layers(ew, NL, ew.T, seed0=90)
+        e_ms, e_steps, _, _ = time_rotation(torch, elayers, stream, args.steps, args.warmup)
+        e_ms = max_over_ranks(e_ms)
+        eb = algorithmic_bytes(ew)
+        line["decode_e4m3_table"] = {
+            "workload": ew.name, "T": ew.T, "tokens_per_s": world * ew.T / (e_ms * 1e-3),
+            "ms_per_step": e_ms, "steps": e_steps, "layers_rotated": NL,
+            "table": f"{ew.total_rows * ew.head_dim * (1 + 1 / 32) / 1e9:.2f} GB e4m3 + ue8m0 "
+                     f"per layer in HBM",
+            "roofline": {"bound": "hbm", "kernel": "decode_fused_kernel (e4m3 table)",
+                         "achieved": eb / (e_ms * 1e-3) / 1e9, "peak": hbm_peak,
+                         "unit": "GB/s", "frac": eb / (e_ms * 1e-3) / 1e9 / hbm_peak,
+                         "algorithmic_bytes": eb, "peak_kind": peak_kind},
+        }
+        launches += e_steps
+        for L in elayers:
+            L["layer"].close()
+        del elayers
+        if not args.no_offload:
+            line["offload_e4m3_table"], n = offload_line(W.OFFLOAD_E4M3, 110)
+            launches += n
 
     line["gpu_launches"] = steps
     line["gpu_launches_all_timed_regions"] = launches

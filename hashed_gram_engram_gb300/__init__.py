@@ -24,8 +24,8 @@ from ._lib import (EngramError, engram_config, engram_create, engram_debug_inter
                    engram_last_error, engram_layout,
                    engram_lookup, engram_profile_enable, engram_profile_read,
                    engram_weights, ENGRAM_WKV_BF16, ENGRAM_WKV_MXFP8,
-                   ENGRAM_TABLE_DEVICE, ENGRAM_TABLE_HOST_PINNED, ENGRAM_DEVERR_BAD_HASH_ID,
-                   ENGRAM_DEVERR_TIMEOUT)
+                   ENGRAM_TABLE_DEVICE, ENGRAM_TABLE_HOST_PINNED, ENGRAM_TABLE_FORMAT_BF16,
+                   ENGRAM_TABLE_FORMAT_E4M3, ENGRAM_DEVERR_BAD_HASH_ID, ENGRAM_DEVERR_TIMEOUT)
 
 __all__ = [
     "Engram", "EngramError", "engram_config", "engram_weights", "engram_create",
@@ -34,7 +34,8 @@ __all__ = [
     "engram_last_error", "engram_device_error", "engram_layout", "engram_debug_intermediates",
     "engram_debug_staged_rows", "engram_profile_enable", "engram_profile_read",
     "ENGRAM_WKV_BF16", "ENGRAM_WKV_MXFP8", "ENGRAM_TABLE_DEVICE",
-    "ENGRAM_TABLE_HOST_PINNED", "ENGRAM_DEVERR_BAD_HASH_ID", "ENGRAM_DEVERR_TIMEOUT",
+    "ENGRAM_TABLE_HOST_PINNED", "ENGRAM_TABLE_FORMAT_BF16", "ENGRAM_TABLE_FORMAT_E4M3",
+    "ENGRAM_DEVERR_BAD_HASH_ID", "ENGRAM_DEVERR_TIMEOUT",
 ]
 
 
@@ -47,13 +48,15 @@ class Engram:
 
     Tensors are torch tensors on the handle's device (the table may be a
     pinned host tensor with ``table_location=ENGRAM_TABLE_HOST_PINNED``).
+    An fp8 table is its e4m3 codes (uint8 [rows, head_dim]) as ``table`` and
+    its ue8m0 scales (uint8 [rows, head_dim / 32]) as ``table_scale``.
     The object keeps references to them so they outlive the handle.
     """
 
     def __init__(self, *, dim, hc_mult, max_ngram_size, n_heads, head_dim, max_tokens,
                  table, rows, wkv, q_weight, k_weight, row_offset=None, wkv_scale=None,
                  eps=1e-6, clamp=1e-6, wkv_format=None, table_location=None, device=None,
-                 keep_value=False):
+                 keep_value=False, table_scale=None):
         import torch
         self.dim, self.hc_mult, self.head_dim = int(dim), int(hc_mult), int(head_dim)
         self.n_hash_cols = (int(max_ngram_size) - 1) * int(n_heads)
@@ -72,12 +75,15 @@ class Engram:
                             max_ngram_size=int(max_ngram_size), n_heads=int(n_heads),
                             head_dim=self.head_dim, eps=float(eps), clamp=float(clamp),
                             max_tokens=self.max_tokens, wkv_format=int(wkv_format),
-                            table_location=int(table_location), device=int(device), reserved=0)
+                            table_location=int(table_location), device=int(device),
+                            table_format=ENGRAM_TABLE_FORMAT_BF16 if table_scale is None
+                            else ENGRAM_TABLE_FORMAT_E4M3)
         w = engram_weights(table=table.data_ptr(), row_offset=row_offset.ctypes.data,
                            rows=rows.ctypes.data, wkv=wkv.data_ptr(),
                            wkv_scale=None if wkv_scale is None else wkv_scale.data_ptr(),
-                           q_weight=q_weight.data_ptr(), k_weight=k_weight.data_ptr())
-        self._keep = (table, wkv, wkv_scale, q_weight, k_weight, rows, row_offset)
+                           q_weight=q_weight.data_ptr(), k_weight=k_weight.data_ptr(),
+                           table_scale=None if table_scale is None else table_scale.data_ptr())
+        self._keep = (table, table_scale, wkv, wkv_scale, q_weight, k_weight, rows, row_offset)
         self.device = int(device)
         self.handle = engram_create(cfg, w)
         if keep_value:  # validation: let intermediates() return the fused path's value

@@ -36,6 +36,8 @@ ENGRAM_WKV_BF16 = 0
 ENGRAM_WKV_MXFP8 = 1
 ENGRAM_TABLE_DEVICE = 0
 ENGRAM_TABLE_HOST_PINNED = 1
+ENGRAM_TABLE_FORMAT_BF16 = 0
+ENGRAM_TABLE_FORMAT_E4M3 = 1
 
 # Every symbol include/engram.h declares.
 EXPORTED = (
@@ -60,7 +62,7 @@ class engram_config(ctypes.Structure):
         ("head_dim", ctypes.c_int64), ("eps", ctypes.c_double), ("clamp", ctypes.c_double),
         ("max_tokens", ctypes.c_int64), ("wkv_format", ctypes.c_int32),
         ("table_location", ctypes.c_int32), ("device", ctypes.c_int32),
-        ("reserved", ctypes.c_int32),
+        ("table_format", ctypes.c_int32),
     ]
 
 
@@ -69,6 +71,7 @@ class engram_weights(ctypes.Structure):
         ("table", ctypes.c_void_p), ("row_offset", ctypes.c_void_p), ("rows", ctypes.c_void_p),
         ("wkv", ctypes.c_void_p), ("wkv_scale", ctypes.c_void_p),
         ("q_weight", ctypes.c_void_p), ("k_weight", ctypes.c_void_p),
+        ("table_scale", ctypes.c_void_p),
     ]
 
 

@@ -87,7 +87,8 @@ struct FusedArgs {
     int64_t ids_stride;
     const int64_t* row_offset;
     const int64_t* rows;
-    const uint16_t* table;
+    const uint16_t* table;   // bf16 rows, or e4m3 codes of an fp8 table
+    const uint8_t* tscale;   // fp8 table: ue8m0 [rows][E/32]; else null
     uint16_t* staged;       // [rows_alloc][K] bf16
     uint8_t* staged_q;      // MXFP8: e4m3 codes [rows_alloc][K]
     uint8_t* staged_s;      // MXFP8: scale atoms of the codes
@@ -218,8 +219,17 @@ __global__ void __launch_bounds__(kThreads, 1)
         const int t = rr / a.C, cc = rr - t * a.C;
         const int64_t id = a.ids[t * a.ids_stride + cc];
         const bool good = id >= 0 && id < __ldg(a.rows + cc);
-        const uint16_t* src = a.table + (__ldg(a.row_offset + cc) + (good ? id : 0)) * a.E +
-                              b * (kMx ? 32 : 8);
+        const int64_t row = __ldg(a.row_offset + cc) + (good ? id : 0);
+        if (a.tscale != nullptr) {  // fp8 table: dequantize on the way
+            const uint8_t* cp = reinterpret_cast<const uint8_t*>(a.table) + row * a.E + b * (kMx ? 32 : 8);
+            const uint32_t sb = good ? __ldg(a.tscale + row * (a.E >> 5) + (kMx ? b : (b >> 2))) : 0u;
+#pragma unroll
+            for (int j = 0; j < (kMx ? 4 : 1); ++j)
+                v[j] = good ? dequant8(__ldg(reinterpret_cast<const uint2*>(cp + j * 8)), sb)
+                            : make_uint4(0u, 0u, 0u, 0u);
+            return good;
+        }
+        const uint16_t* src = a.table + row * a.E + b * (kMx ? 32 : 8);
 #pragma unroll
         for (int j = 0; j < (kMx ? 4 : 1); ++j)
             v[j] = good ? ld_stream_v4(src + j * 8) : make_uint4(0u, 0u, 0u, 0u);
@@ -955,6 +965,7 @@ cudaError_t launch_decode_fused(engram_handle* h, const void* hidden, const int6
     a.row_offset = h->d_row_offset;
     a.rows = h->d_rows;
     a.table = h->table;
+    a.tscale = h->table_scale;
     a.staged = h->ws.staged;
     a.staged_q = h->ws.staged_q;
     a.staged_s = h->ws.staged_s;

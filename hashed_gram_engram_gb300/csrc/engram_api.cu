@@ -177,13 +177,16 @@ int engram_create(const engram_config* cfg, const engram_weights* w, engram_t** 
     const engram_config c = *cfg;
     if (c.dim <= 0 || c.hc_mult <= 0 || c.max_ngram_size < 2 || c.n_heads < 1 ||
         c.head_dim <= 0 || c.max_tokens <= 0 || !(c.eps >= 0.0) || !(c.clamp >= 0.0) ||
-        c.reserved != 0 || (c.wkv_format != ENGRAM_WKV_BF16 && c.wkv_format != ENGRAM_WKV_MXFP8) ||
+        (c.table_format != ENGRAM_TABLE_FORMAT_BF16 && c.table_format != ENGRAM_TABLE_FORMAT_E4M3) ||
+        (c.wkv_format != ENGRAM_WKV_BF16 && c.wkv_format != ENGRAM_WKV_MXFP8) ||
         (c.table_location != ENGRAM_TABLE_DEVICE && c.table_location != ENGRAM_TABLE_HOST_PINNED))
         return ENGRAM_ERR_INVALID_ARG;
     if (w->table == nullptr || w->row_offset == nullptr || w->rows == nullptr ||
         w->wkv == nullptr || w->q_weight == nullptr || w->k_weight == nullptr)
         return ENGRAM_ERR_INVALID_ARG;
     if (c.wkv_format == ENGRAM_WKV_MXFP8 && w->wkv_scale == nullptr) return ENGRAM_ERR_INVALID_ARG;
+    const bool tfp8 = c.table_format == ENGRAM_TABLE_FORMAT_E4M3;
+    if (tfp8 && w->table_scale == nullptr) return ENGRAM_ERR_INVALID_ARG;
     const int64_t C = (c.max_ngram_size - 1) * c.n_heads;
     const int64_t K = C * c.head_dim;
     const int64_t N = c.dim * (c.hc_mult + 1);
@@ -192,7 +195,8 @@ int engram_create(const engram_config* cfg, const engram_weights* w, engram_t** 
     if (c.dim % kBNPrefill != 0 || c.dim > 8192 || c.hc_mult > 4 || c.head_dim % 8 != 0 ||
         32 % (c.head_dim / 8) != 0 || K % 128 != 0 || K > (1 << 20) || !aligned16(w->table) ||
         !aligned16(w->wkv) || c.max_tokens > (1 << 24) ||
-        (mx && (c.head_dim % 32 != 0 || !aligned16(w->wkv_scale))))
+        (mx && (c.head_dim % 32 != 0 || !aligned16(w->wkv_scale))) ||
+        (tfp8 && c.head_dim % 32 != 0))
         return ENGRAM_ERR_UNSUPPORTED;
     for (int64_t i = 0; i < C; ++i)
         if (w->rows[i] <= 0 || w->row_offset[i] < 0) return ENGRAM_ERR_INVALID_ARG;
@@ -205,15 +209,21 @@ int engram_create(const engram_config* cfg, const engram_weights* w, engram_t** 
         return ENGRAM_ERR_CUDA;
 
     const void* table = w->table;
+    const void* table_scale = tfp8 ? static_cast<const void*>(w->table_scale) : nullptr;
     if (c.table_location == ENGRAM_TABLE_HOST_PINNED) {
-        cudaPointerAttributes pa;
         if (!uva) return ENGRAM_ERR_NO_UVA;
-        if (cudaPointerGetAttributes(&pa, w->table) != cudaSuccess) {
-            cudaGetLastError();
-            return ENGRAM_ERR_NO_UVA;
+        // the device aliases of the pinned table (and of its scales)
+        for (const void** p : {&table, &table_scale}) {
+            if (*p == nullptr) continue;
+            cudaPointerAttributes pa;
+            if (cudaPointerGetAttributes(&pa, *p) != cudaSuccess) {
+                cudaGetLastError();
+                return ENGRAM_ERR_NO_UVA;
+            }
+            if (pa.type != cudaMemoryTypeHost || pa.devicePointer == nullptr)
+                return ENGRAM_ERR_NO_UVA;
+            *p = pa.devicePointer;
         }
-        if (pa.type != cudaMemoryTypeHost || pa.devicePointer == nullptr) return ENGRAM_ERR_NO_UVA;
-        table = pa.devicePointer;
     }
 
     engram_handle* h = new (std::nothrow) engram_handle();
@@ -225,6 +235,7 @@ int engram_create(const engram_config* cfg, const engram_weights* w, engram_t** 
     h->N = N;
     h->num_sms = sms;
     h->table = static_cast<const uint16_t*>(table);
+    h->table_scale = static_cast<const uint8_t*>(table_scale);
     h->wkv = w->wkv;
     h->wkv_scale = w->wkv_scale;
     h->q = static_cast<const uint16_t*>(w->q_weight);

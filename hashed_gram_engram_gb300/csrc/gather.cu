@@ -11,6 +11,9 @@
 // codes and one E8M0 scale per 32 consecutive k (smallest power of two that
 // keeps the block maximum within 448; round-to-nearest-even, saturating),
 // the scales stored as the tcgen05 scale-factor atoms the GEMM copies.
+// An fp8 table (e4m3 rows, one ue8m0 scale per 32 elements, class
+// ParallelEngramEmbedding) is dequantized to bf16 on the way: a thread reads
+// 8 code bytes and the row's scale byte for its 16-byte chunk.
 #include "internal.h"
 #include "mxfp8.cuh"
 #include "ptx.cuh"
@@ -22,7 +25,8 @@ constexpr int kGatherThreads = 256;
 constexpr int kUnroll = 4;
 
 struct GatherArgs {
-    const uint16_t* table;
+    const uint16_t* table;     // bf16 rows, or (fp8) e4m3 codes [rows][E]
+    const uint8_t* tscale;     // fp8 table: ue8m0 [rows][E/32]; else null
     const int64_t* row_offset;
     const int64_t* rows;
     const int32_t* ids;
@@ -60,8 +64,14 @@ __global__ void __launch_bounds__(kGatherThreads) gather_rows_kernel(const Gathe
                 const int64_t id = a.ids[t * a.ids_stride + c];
                 dst[u] = r * a.E + j * 8;
                 if (id >= 0 && id < __ldg(a.rows + c)) {
-                    const uint16_t* src = a.table + (__ldg(a.row_offset + c) + id) * a.E + j * 8;
-                    v[u] = ld_stream_v4(src);
+                    const int64_t row = __ldg(a.row_offset + c) + id;
+                    if (a.tscale == nullptr) {
+                        v[u] = ld_stream_v4(a.table + row * a.E + j * 8);
+                    } else {
+                        const uint8_t* cp = reinterpret_cast<const uint8_t*>(a.table) + row * a.E + j * 8;
+                        v[u] = dequant8(__ldg(reinterpret_cast<const uint2*>(cp)),
+                                        __ldg(a.tscale + row * (a.E >> 5) + (j >> 2)));
+                    }
                 } else {
                     bad = 1;
                 }
@@ -105,6 +115,7 @@ cudaError_t launch_gather(const engram_handle* h, const int32_t* ids, int64_t id
                           int64_t T, bool background, bool quantize, cudaStream_t s, bool pdl) {
     GatherArgs a;
     a.table = h->table;
+    a.tscale = h->table_scale;
     a.row_offset = h->d_row_offset;
     a.rows = h->d_rows;
     a.ids = ids;

@@ -90,7 +90,8 @@ struct engram_handle {
     int64_t C, K, N;
     int num_sms;
     // borrowed weights
-    const uint16_t* table;
+    const uint16_t* table;        // bf16 rows, or e4m3 codes of an fp8 table
+    const uint8_t* table_scale;   // fp8 table: ue8m0 [rows][E/32]; null for bf16
     const void* wkv;
     const uint8_t* wkv_scale;
     const uint16_t* q;

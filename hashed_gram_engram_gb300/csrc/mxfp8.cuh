@@ -55,4 +55,46 @@ __device__ __forceinline__ uint32_t mx_quantize32(const uint4 (&v)[4], uint4 (&c
     return static_cast<uint32_t>(e + 127);
 }
 
+// ---------------------------------------------------------------- fp8 tables
+// Rows of an fp8 table (class ParallelEngramEmbedding): e4m3 codes with one
+// E8M0 scale byte per 32 elements, dequantized to bf16 on lookup:
+// e4m3(code) * 2^(scale - 127), rounded to bf16 (nearest, ties to even).
+
+// OCP e4m3 ("fn"): sign, 4-bit exponent with bias 7, 3-bit mantissa;
+// exponent 0 holds the subnormals m * 2^-9; S.1111.111 is NaN (no inf).
+__device__ __forceinline__ float e4m3_value(uint32_t b) {
+    const uint32_t e = (b >> 3) & 15u, m = b & 7u;
+    float v;
+    if (e == 0u)
+        v = static_cast<float>(m) * 0x1p-9f;
+    else if (e == 15u && m == 7u)
+        v = __uint_as_float(0x7FC00000u);
+    else
+        v = __uint_as_float(((e + 120u) << 23) | (m << 20));  // (1 + m/8) * 2^(e-7)
+    return (b & 0x80u) ? -v : v;
+}
+
+// E8M0 byte s -> 2^(s - 127) as fp32 (s = 0: the subnormal 2^-127; 255: NaN).
+__device__ __forceinline__ float e8m0_value(uint32_t s) {
+    if (s == 0u) return __uint_as_float(0x00400000u);
+    if (s == 255u) return __uint_as_float(0x7FC00000u);
+    return __uint_as_float(s << 23);
+}
+
+// Eight e4m3 codes (a 64-bit word, lowest byte first) times one block
+// scale -> eight bf16 in a 16-byte chunk.  Each product is exact in fp32
+// (four significant bits times a power of two), so the one rounding is the
+// bf16 conversion.
+__device__ __forceinline__ uint4 dequant8(uint2 codes, uint32_t scale_byte) {
+    const float sc = e8m0_value(scale_byte);
+    const uint32_t c[2] = {codes.x, codes.y};
+    uint32_t w[4];
+#pragma unroll
+    for (int i = 0; i < 4; ++i) {
+        const uint32_t q = c[i >> 1] >> (16 * (i & 1));
+        w[i] = pack_bf16x2(e4m3_value(q & 0xFFu) * sc, e4m3_value((q >> 8) & 0xFFu) * sc);
+    }
+    return make_uint4(w[0], w[1], w[2], w[3]);
+}
+
 }  // namespace engram

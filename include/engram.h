@@ -55,6 +55,13 @@ extern "C" {
 #define ENGRAM_WKV_BF16 0   /* wkv bf16 [N, K] */
 #define ENGRAM_WKV_MXFP8 1  /* wkv e4m3 [N, K] with E8M0 scales [N/32, K/32] */
 
+/* Storage of the hash table's rows (class ParallelEngramEmbedding). */
+#define ENGRAM_TABLE_FORMAT_BF16 0  /* bf16 [sum(rows), E] */
+#define ENGRAM_TABLE_FORMAT_E4M3 1  /* e4m3 codes [sum(rows), E] with one ue8m0 scale per 32
+                                       elements [sum(rows), E/32]; dequantized to bf16 on
+                                       lookup: e4m3(code) * 2^(scale - 127), rounded to
+                                       nearest even (E a multiple of 32) */
+
 #define ENGRAM_TABLE_DEVICE 0       /* table rows in HBM */
 #define ENGRAM_TABLE_HOST_PINNED 1  /* table rows in pinned host memory, read over the
                                        host link by the GPU (zero copy) */
@@ -74,12 +81,13 @@ typedef struct engram_config {
     int32_t wkv_format;     /* ENGRAM_WKV_* */
     int32_t table_location; /* ENGRAM_TABLE_* */
     int32_t device;         /* CUDA device ordinal the handle lives on */
-    int32_t reserved;       /* must be 0 */
+    int32_t table_format;   /* ENGRAM_TABLE_FORMAT_* (0: bf16) */
 } engram_config;
 
 /* Weights, all borrowed.  Device pointers unless stated. */
 typedef struct engram_weights {
-    const void* table;          /* bf16 [sum(rows), E] row-major: every hash column's
+    const void* table;          /* bf16 [sum(rows), E] row-major (or e4m3 codes for
+                                   ENGRAM_TABLE_FORMAT_E4M3): every hash column's
                                    bucket concatenated (class ParallelEngramEmbedding);
                                    pinned host memory when table_location is HOST_PINNED;
                                    16-byte aligned */
@@ -92,6 +100,9 @@ typedef struct engram_weights {
                                    per 32x32 weight block; NULL for bf16 */
     const void* q_weight;       /* bf16 [H, D] */
     const void* k_weight;       /* bf16 [H, D] */
+    const uint8_t* table_scale; /* ENGRAM_TABLE_FORMAT_E4M3 only: ue8m0 [sum(rows), E/32]
+                                   row-major, in the same memory as the table; NULL for
+                                   bf16 */
 } engram_weights;
 
 typedef struct engram_handle engram_t;

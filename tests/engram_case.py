@@ -23,8 +23,11 @@ class Case:
         small = wl.total_rows * wl.head_dim < (1 << 24)
         gen = gen_device or ("cpu" if small else "cuda")
         table = W.make_table(wl, gen)
+        tscale = W.make_table_scale(wl, gen)
         if wl.table_location == "device":
             table = table.to(dev)
+            tscale = None if tscale is None else tscale.to(dev)
+        self.table_scale = tscale
         wts = W.make_weights(wl, gen)
         self.table = table
         self.wkv = wts["wkv"].to(dev)
@@ -39,13 +42,14 @@ class Case:
                             max_tokens=max_tokens or wl.T, table=self.table, rows=self.rows,
                             row_offset=self.row_offset, wkv=self.wkv, wkv_scale=self.wkv_scale,
                             q_weight=self.q, k_weight=self.k, eps=wl.eps, clamp=wl.clamp,
-                            device=0, keep_value=True)
+                            device=0, keep_value=True, table_scale=self.table_scale)
         self._host = None
 
     def host(self):
         if self._host is None:
             self._host = dict(
                 table=W.bits(self.table),
+                table_scale=None if self.table_scale is None else W.bits(self.table_scale),
                 wkv=W.bits(self.wkv),
                 wkv_scale=None if self.wkv_scale is None else W.bits(self.wkv_scale),
                 q=W.bits(self.q), k=W.bits(self.k))
@@ -67,7 +71,8 @@ class Case:
             mask = None if mask is None else mask[tokens]
         return oracle.forward(hs["table"], self.row_offset, self.rows, ids, self.wl.head_dim,
                               hs["wkv"], hidden, hs["q"], hs["k"], mask, Ws=hs["wkv_scale"],
-                              eps=self.wl.eps, clamp=self.wl.clamp, quantize_act=quantize_act)
+                              eps=self.wl.eps, clamp=self.wl.clamp, quantize_act=quantize_act,
+                              table_scale=hs["table_scale"])
 
 
 def compare(case: Case, inp, out, ref, tokens=None, gate=None, value=None, tol=None,

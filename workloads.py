@@ -10,6 +10,9 @@ an MXFP8 wkv, and host-offloaded tables):
 * hidden: bf16 N(0, 1), [T, hc_mult, dim], contiguous
 * MXFP8 wkv: e4m3 codes of N(0, 1) (torch's float8_e4m3fn cast) with E8M0
   scale bytes uniform in {119..127} (block exponents -8..0)
+* fp8 tables (e4m3 rows, one ue8m0 scale per 32 elements, the storage of
+  class ParallelEngramEmbedding): codes of N(0, 1) the same way, scale bytes
+  uniform in {113..121} (exponents -14..-6, magnitudes near the bf16 tables')
 * hash ids: per column local ids, uniform over [0, rows[c]), or Zipf(1.1)
   ranks scattered over the rows by a per-column bijection r -> (a r + b) mod p
 * token_mask: Bernoulli(p) bytes, or None
@@ -51,6 +54,7 @@ class Workload:
     ids: str = "uniform"            # "uniform" | "zipf"
     mask_p: float | None = None     # Bernoulli(p) token mask, None = no mask
     table_location: str = "device"  # "device" | "host"
+    table_format: str = "bf16"      # "bf16" | "e4m3" (with ue8m0 scales per 32)
     tol: float = 3e-2               # max abs error on the output
     seed: int = 1234
     eps: float = 1e-6
@@ -95,7 +99,15 @@ OFFLOAD = Workload("offload", T=256, dim=4096, hc_mult=4, max_ngram_size=3, n_he
 # parity case only (not a benchmark configuration): the tiny shapes with MXFP8 wkv
 TINY_MXFP8 = dataclasses.replace(TINY, name="tiny_mxfp8", wkv_format="mxfp8", tol=5e-2,
                                  seed=1240)
-ALL = {w.name: w for w in (TINY, DECODE, PREFILL, MXFP8_DECODE, MXFP8_PREFILL, OFFLOAD)}
+# fp8 (e4m3 + ue8m0 per 32) tables, the storage the pages' ParallelEngramEmbedding
+# keeps: the decode and offload shapes, and a tiny parity case
+DECODE_E4M3 = dataclasses.replace(DECODE, name="decode_e4m3_table", table_format="e4m3",
+                                  seed=1241)
+OFFLOAD_E4M3 = dataclasses.replace(OFFLOAD, name="offload_e4m3_table", table_format="e4m3",
+                                   seed=1242)
+TINY_E4M3 = dataclasses.replace(TINY, name="tiny_e4m3_table", table_format="e4m3", seed=1243)
+ALL = {w.name: w for w in (TINY, DECODE, PREFILL, MXFP8_DECODE, MXFP8_PREFILL, OFFLOAD,
+                           DECODE_E4M3, OFFLOAD_E4M3)}
 
 
 def shard_tokens(T: int, rank: int, world: int) -> tuple[int, int]:
@@ -121,22 +133,48 @@ def _normal_bf16(shape, std, g, device):
             * std).to(torch.bfloat16)
 
 
+def _e4m3_codes(shape, g, device):
+    return torch.randn(shape, generator=g, device=device).to(torch.float8_e4m3fn).view(
+        torch.uint8)
+
+
 def make_table(wl: Workload, device="cpu", chunk_rows=1 << 22):
-    """bf16 [total_rows, head_dim] N(0, 0.02).  For table_location "host" the
-    rows are drawn on ``device`` in chunks and stored in pinned host memory."""
+    """bf16 [total_rows, head_dim] N(0, 0.02), or for an e4m3 table its codes
+    (uint8, same shape).  For table_location "host" the rows are drawn on
+    ``device`` in chunks and stored in pinned host memory."""
     g = _gen(device, wl.seed * 7 + 1)
     n, E = wl.total_rows, wl.head_dim
+    fp8 = wl.table_format == "e4m3"
+    dt = torch.uint8 if fp8 else torch.bfloat16
+    draw = (lambda m: _e4m3_codes((m, E), g, device)) if fp8 else (
+        lambda m: _normal_bf16((m, E), 0.02, g, device))
     if wl.table_location == "host":
-        out = torch.empty((n, E), dtype=torch.bfloat16, pin_memory=True)
+        out = torch.empty((n, E), dtype=dt, pin_memory=True)
         for s in range(0, n, chunk_rows):
             e = min(n, s + chunk_rows)
-            out[s:e].copy_(_normal_bf16((e - s, E), 0.02, g, device))
+            out[s:e].copy_(draw(e - s))
         return out
-    out = torch.empty((n, E), dtype=torch.bfloat16, device=device)
+    out = torch.empty((n, E), dtype=dt, device=device)
     for s in range(0, n, chunk_rows):
         e = min(n, s + chunk_rows)
-        out[s:e] = _normal_bf16((e - s, E), 0.02, g, device)
+        out[s:e] = draw(e - s)
     return out
+
+
+def make_table_scale(wl: Workload, device="cpu"):
+    """ue8m0 scale bytes [total_rows, head_dim / 32] of an e4m3 table, uniform
+    in {113..121} (in pinned host memory for table_location "host"); None for
+    a bf16 table."""
+    if wl.table_format != "e4m3":
+        return None
+    g = _gen(device, wl.seed * 7 + 5)
+    sc = torch.randint(113, 122, (wl.total_rows, wl.head_dim // 32), generator=g,
+                       device=device, dtype=torch.int32).to(torch.uint8)
+    if wl.table_location == "host":
+        out = torch.empty(sc.shape, dtype=torch.uint8, pin_memory=True)
+        out.copy_(sc)
+        return out
+    return sc
 
 
 def make_weights(wl: Workload, device="cpu"):
@@ -189,7 +227,7 @@ def make_step_inputs(wl: Workload, device="cpu", T: int | None = None, step: int
 
 
 def make_all(wl: Workload, device="cpu", T: int | None = None):
-    d = dict(table=make_table(wl, device))
+    d = dict(table=make_table(wl, device), table_scale=make_table_scale(wl, device))
     d.update(make_weights(wl, device))
     d.update(make_step_inputs(wl, device, T))
     d["row_offset"] = row_offsets(wl.rows)
