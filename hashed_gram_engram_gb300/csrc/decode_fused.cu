@@ -207,8 +207,8 @@ __global__ void __launch_bounds__(kThreads, 1)
 
     // Gather item i of this CTA (a 16-byte chunk of a hash row; MXFP8: a
     // 32-k block, four chunks): the id, then the row.  Each gathering
-    // thread fetches its first item before the CTA-wide setup below, so the
-    // dependent id -> row loads overlap it.
+    // thread fetches its first two items before the CTA-wide setup below, so
+    // the dependent id -> row loads overlap it and each other.
     const int nrows_g = a.T * a.C;
     const int g_r0 = static_cast<int>(static_cast<int64_t>(c) * nrows_g / G);
     const int g_r1 = static_cast<int>(static_cast<int64_t>(c + 1) * nrows_g / G);
@@ -273,9 +273,12 @@ __global__ void __launch_bounds__(kThreads, 1)
         // this launch's epoch: stable until CTA 0 advances it at the end
         *epoch_s = *reinterpret_cast<volatile unsigned long long*>(a.bar) + 1ull;
     }
-    uint4 pre[4] = {};
-    bool pre_good = true;
+    // (a thread's second item too, so that two id -> row chains overlap when
+    // rows cross the host link)
+    uint4 pre[4] = {}, pre2[4] = {};
+    bool pre_good = true, pre2_good = true;
     if (warp >= 2 && warp < 6 && tid - 64 < g_n) pre_good = fetch(tid - 64, pre);
+    if (warp >= 2 && warp < 6 && tid - 64 + 128 < g_n) pre2_good = fetch(tid - 64 + 128, pre2);
     if (warp == 1) {
         tmem_alloc(tmem_slot, kTmemCols);
         tmem_relinquish();
@@ -436,6 +439,10 @@ __global__ void __launch_bounds__(kThreads, 1)
 #pragma unroll
                     for (int j = 0; j < 4; ++j) v[j] = pre[j];
                     good = pre_good;
+                } else if (i == etid + 128) {
+#pragma unroll
+                    for (int j = 0; j < 4; ++j) v[j] = pre2[j];
+                    good = pre2_good;
                 } else {
                     good = fetch(i, v);
                 }
