@@ -170,7 +170,7 @@ __device__ __forceinline__ bool grid_wait(const unsigned long long* ctr, unsigne
     return true;
 }
 
-template <bool kMx>
+template <bool kMx, bool kF8T>
 __global__ void __launch_bounds__(kThreads, 1)
     decode_fused_kernel(const __grid_constant__ CUtensorMap tm_x, const FusedArgs a) {
     extern __shared__ uint8_t smem_raw[];
@@ -220,7 +220,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         const int64_t id = a.ids[t * a.ids_stride + cc];
         const bool good = id >= 0 && id < __ldg(a.rows + cc);
         const int64_t row = __ldg(a.row_offset + cc) + (good ? id : 0);
-        if (a.tscale != nullptr) {  // fp8 table: dequantize on the way
+        if constexpr (kF8T) {  // fp8 table: dequantize on the way
             const uint8_t* cp = reinterpret_cast<const uint8_t*>(a.table) + row * a.E + b * (kMx ? 32 : 8);
             const uint32_t sb = good ? __ldg(a.tscale + row * (a.E >> 5) + (kMx ? b : (b >> 2))) : 0u;
 #pragma unroll
@@ -278,7 +278,8 @@ __global__ void __launch_bounds__(kThreads, 1)
     uint4 pre[4] = {}, pre2[4] = {};
     bool pre_good = true, pre2_good = true;
     if (warp >= 2 && warp < 6 && tid - 64 < g_n) pre_good = fetch(tid - 64, pre);
-    if (warp >= 2 && warp < 6 && tid - 64 + 128 < g_n) pre2_good = fetch(tid - 64 + 128, pre2);
+    if constexpr (!kMx)  // (MXFP8 items are 32 k: a CTA never has more than 128)
+        if (warp >= 2 && warp < 6 && tid - 64 + 128 < g_n) pre2_good = fetch(tid - 64 + 128, pre2);
     if (warp == 1) {
         tmem_alloc(tmem_slot, kTmemCols);
         tmem_relinquish();
@@ -439,7 +440,7 @@ __global__ void __launch_bounds__(kThreads, 1)
 #pragma unroll
                     for (int j = 0; j < 4; ++j) v[j] = pre[j];
                     good = pre_good;
-                } else if (i == etid + 128) {
+                } else if (!kMx && i == etid + 128) {
 #pragma unroll
                     for (int j = 0; j < 4; ++j) v[j] = pre2[j];
                     good = pre2_good;
@@ -931,12 +932,16 @@ cudaError_t pack_weights(const engram_handle* h, cudaStream_t s) {
 }
 
 cudaError_t fused_setup_attributes() {
-    cudaError_t e = cudaFuncSetAttribute(decode_fused_kernel<false>,
-                                         cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                         kFusedSmemBytes);
-    if (e != cudaSuccess) return e;
-    return cudaFuncSetAttribute(decode_fused_kernel<true>,
-                                cudaFuncAttributeMaxDynamicSharedMemorySize, kFusedSmemBytes);
+    const void* fns[] = {reinterpret_cast<const void*>(decode_fused_kernel<false, false>),
+                         reinterpret_cast<const void*>(decode_fused_kernel<false, true>),
+                         reinterpret_cast<const void*>(decode_fused_kernel<true, false>),
+                         reinterpret_cast<const void*>(decode_fused_kernel<true, true>)};
+    for (const void* fn : fns) {
+        const cudaError_t e =
+            cudaFuncSetAttribute(fn, cudaFuncAttributeMaxDynamicSharedMemorySize, kFusedSmemBytes);
+        if (e != cudaSuccess) return e;
+    }
+    return cudaSuccess;
 }
 
 cudaError_t launch_fused_debug_value(const engram_handle* h, float* value, int64_t T,
@@ -952,6 +957,7 @@ cudaError_t launch_decode_fused(engram_handle* h, const void* hidden, const int6
     const FusedPlan p = fused_plan(h, T);
     const FusedLayout& L = h->fused;
     const bool mx = h->cfg.wkv_format == ENGRAM_WKV_MXFP8;
+    const bool f8t = h->table_scale != nullptr;
     FusedArgs a = {};
     a.T = static_cast<int>(T);
     a.Tn = p.Tn;
@@ -1046,8 +1052,10 @@ cudaError_t launch_decode_fused(engram_handle* h, const void* hidden, const int6
     void* args[] = {&tm_x, &a};
     return cudaLaunchKernelExC(
         &cfg,
-        mx ? reinterpret_cast<const void*>(decode_fused_kernel<true>)
-           : reinterpret_cast<const void*>(decode_fused_kernel<false>),
+        mx ? (f8t ? reinterpret_cast<const void*>(decode_fused_kernel<true, true>)
+                  : reinterpret_cast<const void*>(decode_fused_kernel<true, false>))
+           : (f8t ? reinterpret_cast<const void*>(decode_fused_kernel<false, true>)
+                  : reinterpret_cast<const void*>(decode_fused_kernel<false, false>)),
         args);
 }
 
