@@ -13,7 +13,8 @@
 // the key columns anyway; the value comes as bf16.  What is left is a
 // stream: per token, H hidden rows and the value row in, H rows out.
 //
-// gate_ring_kernel: one persistent CTA per SM takes tokens c, c + grid, ...
+// gate_ring_kernel: persistent CTAs (two per SM when two token stages fit
+// in half of the SM's shared memory, else one) take tokens c, c + grid, ...
 // One thread (warp 8) keeps a ring of token stages full with bulk copies
 // (the hidden rows, the value row, the token's partials) and writes each
 // finished token back with bulk stores; warps 0-7 sum the partials of
@@ -22,8 +23,9 @@
 // shared memory.  The hidden rows of the first stages are requested before
 // the programmatic-launch wait, so their reads overlap the wkv kernel's tail.
 //
-// gate_rows_kernel: the same arithmetic one CTA per token with plain
-// loads, for hidden or out rows that are not 16-byte aligned.
+// engram_forward accepts only 16-byte aligned rows, so every row is one
+// bulk copy away; the largest configuration (D = 8192, H = 4) still gets two
+// stages.
 #include "internal.h"
 #include "ptx.cuh"
 
@@ -33,7 +35,8 @@ namespace {
 constexpr int kRingCompute = 256;                 // warps 0-7
 constexpr int kRingThreads = kRingCompute + 32;   // + warp 8: the copies
 constexpr int kRingMaxStages = 8;
-constexpr uint32_t kRingSmem = 227 * 1024;        // dynamic shared memory of a CTA
+constexpr uint32_t kRingSmem = 227 * 1024;        // dynamic shared memory: one CTA per SM
+constexpr uint32_t kRingSmemHalf = 113 * 1024;    // ... or two, when two stages fit in half
 constexpr uint32_t kRingTail = 512;               // barriers, gates, flag, alignment
 
 struct RingArgs {
@@ -74,7 +77,7 @@ __device__ __forceinline__ uint4 residual8(uint4 x, uint4 v, float g) {
     return make_uint4(r[0], r[1], r[2], r[3]);
 }
 
-__global__ void __launch_bounds__(kRingThreads, 1) gate_ring_kernel(const RingArgs a) {
+__global__ void __launch_bounds__(kRingThreads, 2) gate_ring_kernel(const RingArgs a) {
     extern __shared__ uint8_t ring_raw[];
     uint8_t* smem = reinterpret_cast<uint8_t*>(
         (reinterpret_cast<uintptr_t>(ring_raw) + 127) & ~static_cast<uintptr_t>(127));
@@ -224,62 +227,6 @@ __global__ void __launch_bounds__(kRingThreads, 1) gate_ring_kernel(const RingAr
     }
 }
 
-// One CTA per token, plain loads and stores (rows that bulk copies cannot
-// address).  The partials' hidden^2 sums are used as they are.
-struct RowsArgs {
-    const uint16_t* hidden;
-    int64_t hs_t, hs_h;
-    uint16_t* out;
-    int64_t os_t, os_h;
-    const uint8_t* mask;
-    const float4* partials;
-    const uint16_t* value;
-    float* gate_out;
-    int T, D, H, J;
-    float eps, clamp, inv_d, inv_sqrt_d;
-};
-
-constexpr int kRowsThreads = 256;
-
-__global__ void __launch_bounds__(kRowsThreads) gate_rows_kernel(const RowsArgs a) {
-    __shared__ float g_s[kMaxCopies];
-    const int t = blockIdx.x, tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
-    pdl_wait();  // the partials and the value are complete and visible
-    const bool active = a.mask == nullptr || a.mask[t] != 0;
-    if (warp < a.H) {
-        const float4* p = a.partials + (static_cast<int64_t>(t) * a.H + warp) * a.J;
-        float s_hh = 0.f, s_kk = 0.f, s_hk = 0.f;
-        for (int j = lane; j < a.J; j += 32) {
-            const float4 v = __ldcg(p + j);
-            s_hh += v.x;
-            s_kk += v.y;
-            s_hk += v.z;
-        }
-#pragma unroll
-        for (int o = 16; o > 0; o >>= 1) {
-            s_hh += __shfl_xor_sync(0xFFFFFFFFu, s_hh, o);
-            s_kk += __shfl_xor_sync(0xFFFFFFFFu, s_kk, o);
-            s_hk += __shfl_xor_sync(0xFFFFFFFFu, s_hk, o);
-        }
-        if (lane == 0) {
-            const float g =
-                active ? gate_of(s_hh, s_kk, s_hk, a.inv_d, a.eps, a.inv_sqrt_d, a.clamp) : 0.0f;
-            g_s[warp] = g;
-            a.gate_out[static_cast<int64_t>(t) * a.H + warp] = g;
-        }
-    }
-    __syncthreads();
-    const int nchunk = a.D >> 3;
-    for (int c = tid; c < nchunk; c += kRowsThreads) {
-        const uint4 v = ld_nc_v4(a.value + static_cast<int64_t>(t) * a.D + c * 8);
-        uint4 x[kMaxCopies];
-        for (int h = 0; h < a.H; ++h)  // all loads before any store (in place)
-            x[h] = ld_nc_v4(a.hidden + t * a.hs_t + h * a.hs_h + c * 8);
-        for (int h = 0; h < a.H; ++h)
-            st_v4(a.out + t * a.os_t + h * a.os_h + c * 8, active ? residual8(x[h], v, g_s[h]) : x[h]);
-    }
-}
-
 __global__ void qk_kernel(const uint16_t* q, const uint16_t* k, float* qk, int64_t n) {
     const int64_t i = static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x;
     if (i < n) qk[i] = __uint_as_float(static_cast<uint32_t>(q[i]) << 16) *
@@ -290,11 +237,6 @@ __global__ void qk_kernel(const uint16_t* q, const uint16_t* k, float* qk, int64
 __global__ void debug_value_kernel(const uint16_t* value, int64_t n, float* out) {
     const int64_t i = static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x;
     if (i < n) out[i] = __uint_as_float(static_cast<uint32_t>(value[i]) << 16);
-}
-
-bool rows_aligned(const void* base, const int64_t* strides) {
-    return (reinterpret_cast<uintptr_t>(base) & 15u) == 0 && strides[0] % 8 == 0 &&
-           strides[1] % 8 == 0;
 }
 
 // Stage layout of the ring: H hidden rows | value row | H * J partials.
@@ -326,40 +268,13 @@ cudaError_t launch_gate_from_partials(const engram_handle* h, const void* hidden
     cfg.numAttrs = pdl ? 1 : 0;
 
     const uint32_t stage = ring_stage_bytes(D, H, J);
-    const int stages_fit = static_cast<int>((kRingSmem - kRingTail) / stage);
-    if (rows_aligned(hidden, hs) && rows_aligned(out, os) && stages_fit >= 2) {
-        RingArgs a = {};
-        a.hidden = static_cast<const uint16_t*>(hidden);
-        a.hs_t = hs[0];
-        a.hs_h = hs[1];
-        a.out = static_cast<uint16_t*>(out);
-        a.os_t = os[0];
-        a.os_h = os[1];
-        a.mask = mask;
-        a.value = h->ws.value;
-        a.partials = h->ws.partials;
-        a.gate_out = h->ws.gate;
-        a.T = static_cast<int>(T);
-        a.D = D;
-        a.H = H;
-        a.J = J;
-        a.stages = stages_fit < kRingMaxStages ? stages_fit : kRingMaxStages;
-        a.row_bytes = static_cast<uint32_t>(D) * 2u;
-        a.val_off = static_cast<uint32_t>(H) * a.row_bytes;
-        a.part_off = a.val_off + a.row_bytes;
-        a.stage_bytes = stage;
-        a.eps = eps;
-        a.clamp = clamp;
-        a.inv_d = inv_d;
-        a.inv_sqrt_d = inv_sqrt_d;
-        a.err = h->ws.err;
-        const int64_t grid = T < h->num_sms ? T : h->num_sms;
-        cfg.gridDim = dim3(static_cast<unsigned>(grid));
-        cfg.blockDim = dim3(kRingThreads);
-        cfg.dynamicSmemBytes = kRingSmem;
-        return cudaLaunchKernelEx(&cfg, gate_ring_kernel, a);
-    }
-    RowsArgs a = {};
+    // two CTAs per SM (two independent copy streams) when each still gets two
+    // stages; one CTA with the whole shared memory otherwise
+    const bool two = 2u * stage <= kRingSmemHalf - kRingTail;
+    const uint32_t smem = two ? kRingSmemHalf : kRingSmem;
+    const int stages_fit = static_cast<int>((smem - kRingTail) / stage);
+    if (stages_fit < 2) return cudaErrorInvalidConfiguration;
+    RingArgs a = {};
     a.hidden = static_cast<const uint16_t*>(hidden);
     a.hs_t = hs[0];
     a.hs_h = hs[1];
@@ -367,20 +282,29 @@ cudaError_t launch_gate_from_partials(const engram_handle* h, const void* hidden
     a.os_t = os[0];
     a.os_h = os[1];
     a.mask = mask;
-    a.partials = h->ws.partials;
     a.value = h->ws.value;
+    a.partials = h->ws.partials;
     a.gate_out = h->ws.gate;
     a.T = static_cast<int>(T);
     a.D = D;
     a.H = H;
     a.J = J;
+    a.stages = stages_fit < kRingMaxStages ? stages_fit : kRingMaxStages;
+    a.row_bytes = static_cast<uint32_t>(D) * 2u;
+    a.val_off = static_cast<uint32_t>(H) * a.row_bytes;
+    a.part_off = a.val_off + a.row_bytes;
+    a.stage_bytes = stage;
     a.eps = eps;
     a.clamp = clamp;
     a.inv_d = inv_d;
     a.inv_sqrt_d = inv_sqrt_d;
-    cfg.gridDim = dim3(static_cast<unsigned>(T));
-    cfg.blockDim = dim3(kRowsThreads);
-    return cudaLaunchKernelEx(&cfg, gate_rows_kernel, a);
+    a.err = h->ws.err;
+    const int64_t ctas = static_cast<int64_t>(h->num_sms) * (two ? 2 : 1);
+    const int64_t grid = T < ctas ? T : ctas;
+    cfg.gridDim = dim3(static_cast<unsigned>(grid));
+    cfg.blockDim = dim3(kRingThreads);
+    cfg.dynamicSmemBytes = smem;
+    return cudaLaunchKernelEx(&cfg, gate_ring_kernel, a);
 }
 
 cudaError_t launch_qk(const engram_handle* h, cudaStream_t s) {
