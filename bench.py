@@ -197,13 +197,18 @@ def run_reference(args):
 
 
 def source_digest(names):
-    """sha256 (12 hex) of kernel sources, to tell whether a stored ncu
-    figure still describes the kernel that runs."""
+    """sha256 (12 hex) of kernel sources with comments and whitespace removed,
+    to tell whether a stored ncu figure still describes the code that runs
+    (an edit of a comment does not change the kernel)."""
     import hashlib
+    import re
     h = hashlib.sha256()
     for n in names:
-        with open(os.path.join(ROOT, "hashed_gram_engram_gb300", "csrc", n), "rb") as f:
-            h.update(f.read())
+        with open(os.path.join(ROOT, "hashed_gram_engram_gb300", "csrc", n)) as f:
+            text = f.read()
+        text = re.sub(r"/\*.*?\*/", " ", text, flags=re.S)   # block comments
+        text = re.sub(r"//[^\n]*", " ", text)                 # line comments
+        h.update(" ".join(text.split()).encode())
     return h.hexdigest()[:12]
 
 

@@ -28,19 +28,26 @@
 // from a few warps could not keep enough bytes in flight.
 //
 //   gather   each CTA copies ~1/grid of the T x C hash rows into the
-//            staged buffer (MXFP8: and quantises them into e4m3 codes and
+//            staged buffer (an fp8 table's rows dequantized to bf16 on the
+//            way; MXFP8 wkv: the rows also quantised into e4m3 codes and
 //            scales); grid barrier 1; then every CTA loads the token tiles
 //            of every k-block from the staged rows.  Rows staged by
 //            engram_lookup skip the gather;
 //   epilogue thread = token: for the key columns it sums hidden^2, key^2
 //            and hidden*q*k*key per hc copy into a record per (copy, token,
-//            CTA); grid barrier 2;
+//            CTA).  With one token tile and at most 48 value dims it also
+//            loads the residual's operands now (the value from TMEM, hidden
+//            at its value dims); grid barrier 2;
 //   gates    CTA c reduces the records of rows (token, copy) = c, c + grid,
 //            ... (one warp per row, a fixed summation order: runs are
 //            bit-identical) and publishes the gates; grid barrier 3;
 //   residual every CTA writes hidden + gate * value for its own value dims
 //            (masked tokens keep hidden's bits), the value read straight
-//            from TMEM.
+//            from TMEM (or from the registers loaded before barrier 2).
+//
+// Template parameters: the wkv format (bf16 / MXFP8) and the table format
+// (bf16 / e4m3 with ue8m0 scales), so that neither path pays for the
+// other's code.
 //
 // The launch is programmatic-dependent: the next launch may start once every
 // CTA has begun; before griddepcontrol.wait a CTA only sets up and starts the
