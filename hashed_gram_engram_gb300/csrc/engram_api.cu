@@ -263,7 +263,7 @@ int engram_create(const engram_config* cfg, const engram_weights* w, engram_t** 
     // prefill path (also taken by small T when a decode column slice would
     // be too wide)
     step(dalloc(&ws.partials,
-                ws.rows_alloc * c.hc_mult * (c.dim / prefill_bn(h)) *
+                ws.rows_alloc * c.hc_mult * 2 * (c.dim / prefill_bn(h)) *
                     sizeof(float4),
                 true));
     step(dalloc(&ws.value, ws.rows_alloc * c.dim * 2, true));

@@ -255,7 +255,8 @@ cudaError_t launch_gate_from_partials(const engram_handle* h, const void* hidden
                                       const int64_t* hs, const uint8_t* mask, void* out,
                                       const int64_t* os, int64_t T, cudaStream_t s, bool pdl) {
     const int D = static_cast<int>(h->cfg.dim), H = static_cast<int>(h->cfg.hc_mult);
-    const int J = D / prefill_bn(h);
+    // wkv partial records per (token, copy): one per tile, MXFP8 one per half tile
+    const int J = (h->cfg.wkv_format == ENGRAM_WKV_MXFP8 ? 2 : 1) * (D / prefill_bn(h));
     const float inv_d = 1.0f / static_cast<float>(D);
     const float inv_sqrt_d = 1.0f / sqrtf(static_cast<float>(D));
     const float eps = static_cast<float>(h->cfg.eps), clamp = static_cast<float>(h->cfg.clamp);

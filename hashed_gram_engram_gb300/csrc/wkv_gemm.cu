@@ -14,9 +14,12 @@
 // ("vllm.models.deepseek_v41.amd.engram"), here per N tile instead of per
 // TP rank -- and for a value tile it stores the value in bf16.
 //
-// Roles (192 threads): warp 0 = TMA producer, warp 1 = TMEM owner and MMA
-// issuer, warps 2-5 = epilogue (TMEM lane quarter = warp % 4).  Two TMEM
-// accumulators let the epilogue of one unit overlap the MMAs of the next.
+// Roles: warp 0 = TMA producer, warp 1 = TMEM owner and MMA issuer, then
+// the epilogue warps (TMEM lane quarter = warp % 4): 4 for bf16 (192
+// threads); 8 for MXFP8 (320 threads, two per quarter taking half of the
+// tile's columns each), whose short fp8 MMAs otherwise wait for the
+// epilogue.  Two TMEM accumulators let the epilogue of one unit overlap the
+// MMAs of the next.
 // The weight loads of the first pipeline stages are issued before the
 // programmatic-launch wait, overlapping the gather kernel.
 //
@@ -38,7 +41,8 @@
 namespace engram {
 namespace {
 
-constexpr int kThreads = 192;
+// producer, MMA issuer and 4 epilogue warps (8 for MXFP8, whose tiles' MMAs are short)
+constexpr int threads_for(bool mx) { return mx ? 320 : 192; }
 constexpr int kMaxStages = 8;
 constexpr int kStageBudget = 192 * 1024;
 constexpr uint32_t kTmemCols = 512;
@@ -85,7 +89,7 @@ __device__ __forceinline__ void fail(int* abort_flag, unsigned* err) {
 }
 
 template <bool kMx, int BN>
-__global__ void __launch_bounds__(kThreads, 1)
+__global__ void __launch_bounds__(threads_for(kMx), 1)
     wkv_gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
                     const GemmArgs a) {
     constexpr int kKElems = kMx ? 128 : 64;  // k per 128-byte block
@@ -115,7 +119,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         }
         for (int i = 0; i < 2; ++i) {
             mbar_init(&tfull[i], 1);
-            mbar_init(&tempty[i], 4);
+            mbar_init(&tempty[i], kMx ? 8 : 4);  // every epilogue warp
         }
         mbar_init(drain, 1);
         *abort_flag = 0;
@@ -273,9 +277,15 @@ __global__ void __launch_bounds__(kThreads, 1)
             if (!ok) fail(abort_flag, a.err);
         }
     } else {
-        // Epilogue: TMEM lane quarter q = warp % 4, one accumulator row per thread.
+        // Epilogue: TMEM lane quarter q = warp % 4, one accumulator row per
+        // thread.  MXFP8: two warps per quarter, each taking half of the
+        // tile's 32-column chunks (an epilogue must keep up with one tile's
+        // MMAs, short at fp8), each half writing its own partial record.
         const int q = warp & 3;
         const int row = q * 32 + lane;
+        constexpr int kHalfCh = kMx ? (BN / 32 + 1) / 2 : BN / 32;  // chunks of this warp
+        const int half = kMx ? (warp - 2) >> 2 : 0;
+        const int c0 = half * kHalfCh * 32;          // first column of this warp's half
         Schedule sch(a);
         Unit u;
         bool ok = true;
@@ -292,26 +302,25 @@ __global__ void __launch_bounds__(kThreads, 1)
                 const int h = col0 / a.D;
                 const int d0 = col0 - h * a.D;
                 if (h < a.H) {
-                    uint4 hv[BN / 8];
-                    if (live) {
-                        const uint16_t* hp = a.hidden + t * a.hs_t + h * a.hs_h + d0;
+                    uint4 hv[kHalfCh * 4];
+                    const uint16_t* hp = a.hidden + t * a.hs_t + h * a.hs_h + d0 + c0;
 #pragma unroll
-                        for (int i = 0; i < BN / 8; ++i) hv[i] = ld_nc_v4(hp + 8 * i);
-                    } else {
-#pragma unroll
-                        for (int i = 0; i < BN / 8; ++i) hv[i] = make_uint4(0, 0, 0, 0);
-                    }
+                    for (int i = 0; i < kHalfCh * 4; ++i)
+                        hv[i] = (live && c0 + 8 * i < BN) ? ld_nc_v4(hp + 8 * i)
+                                                          : make_uint4(0, 0, 0, 0);
                     if (!mbar_wait(&tfull[acc], apar, abort_v)) {
                         ok = false;
                         break;
                     }
                     tc_fence_after();
-                    const float* qkp = a.qk + h * a.D + d0;
+                    const float* qkp = a.qk + h * a.D + d0 + c0;
                     float shh = 0.f, skk = 0.f, shk = 0.f;
 #pragma unroll
-                    for (int c = 0; c < BN; c += 32) {
+                    for (int cc = 0; cc < kHalfCh; ++cc) {
+                        const int c = cc * 32;  // within this half
+                        if (c0 + c >= BN) break;
                         uint32_t r[32];
-                        tmem_ld32(taddr + c, r);
+                        tmem_ld32(taddr + c0 + c, r);
                         tmem_ld_wait();
 #pragma unroll
                         for (int j = 0; j < 32; j += 8) {
@@ -333,8 +342,9 @@ __global__ void __launch_bounds__(kThreads, 1)
                     tc_fence_before();
                     __syncwarp();
                     if (lane == 0) mbar_arrive(&tempty[acc]);
-                    if (live)
-                        a.partials[(static_cast<int64_t>(t) * a.H + h) * a.J + d0 / BN] =
+                    if (live)  // (MXFP8: J = 2 records per tile, one per half)
+                        a.partials[(static_cast<int64_t>(t) * a.H + h) * a.J +
+                                   (kMx ? 2 * (d0 / BN) + half : d0 / BN)] =
                             make_float4(shh, skk, shk, 0.f);
                 } else {
                     if (!mbar_wait(&tfull[acc], apar, abort_v)) {
@@ -344,7 +354,9 @@ __global__ void __launch_bounds__(kThreads, 1)
                     tc_fence_after();
                     uint16_t* vp = a.value + static_cast<int64_t>(t) * a.D + d0;
 #pragma unroll
-                    for (int c = 0; c < BN; c += 32) {
+                    for (int cc = 0; cc < kHalfCh; ++cc) {
+                        const int c = c0 + cc * 32;
+                        if (c >= BN) break;
                         uint32_t r[32];
                         tmem_ld32(taddr + c, r);
                         tmem_ld_wait();
@@ -447,11 +459,11 @@ cudaError_t gemm_setup_attributes() {
     return cudaSuccess;
 }
 
-static cudaError_t launch(const void* fn, int grid, const CUtensorMap& tmA, const CUtensorMap& tmB,
-                          const GemmArgs& a, cudaStream_t s, bool pdl) {
+static cudaError_t launch(const void* fn, int grid, int threads, const CUtensorMap& tmA,
+                          const CUtensorMap& tmB, const GemmArgs& a, cudaStream_t s, bool pdl) {
     cudaLaunchConfig_t cfg = {};
     cfg.gridDim = dim3(static_cast<unsigned>(grid));
-    cfg.blockDim = dim3(kThreads);
+    cfg.blockDim = dim3(static_cast<unsigned>(threads));
     cfg.dynamicSmemBytes = kGemmSmemBytes;
     cfg.stream = s;
     cudaLaunchAttribute attr[1];
@@ -494,7 +506,7 @@ cudaError_t launch_wkv_tokens_m(const engram_handle* h, const void* hidden, int6
     a.idesc = idesc_bf16(kBM, kBNPrefill);
     a.D = static_cast<int>(h->cfg.dim);
     a.H = static_cast<int>(h->cfg.hc_mult);
-    a.J = a.D / bn;
+    a.J = (mx ? 2 : 1) * (a.D / bn);  // MXFP8: a partial record per half tile
     a.hidden = static_cast<const uint16_t*>(hidden);
     a.hs_t = hs_t;
     a.hs_h = hs_h;
@@ -510,8 +522,7 @@ cudaError_t launch_wkv_tokens_m(const engram_handle* h, const void* hidden, int6
             : (bn == kBNPrefillMxWide
                    ? reinterpret_cast<const void*>(wkv_gemm_kernel<true, kBNPrefillMxWide>)
                    : reinterpret_cast<const void*>(wkv_gemm_kernel<true, kBNPrefillMx>));
-    return launch(fn,
-                  grid, h->tm_act_m, h->tm_w_n, a, s, pdl);
+    return launch(fn, grid, threads_for(mx), h->tm_act_m, h->tm_w_n, a, s, pdl);
 }
 
 }  // namespace engram
