@@ -82,3 +82,46 @@ def test_product_package_never_reaches_the_oracle():
             if fn.endswith((".py", ".cu", ".cuh", ".h")):
                 src = open(os.path.join(dirpath, fn)).read()
                 assert "oracle" not in src, f"{fn} mentions the oracle"
+
+
+def _header():
+    return open(os.path.join(ROOT, "include", "engram.h")).read()
+
+
+def test_binding_constants_match_the_header():
+    from hashed_gram_engram_gb300 import _lib
+    defines = dict(re.findall(r"^#define\s+(ENGRAM_\w+)\s+\(?(-?\d+)u?\)?", _header(), re.M))
+    assert defines, "no #define constants found"
+    for name, value in defines.items():
+        assert hasattr(_lib, name), f"{name} missing from the binding"
+        assert getattr(_lib, name) == int(value), name
+
+
+def test_binding_structs_match_the_header_layout(tmp_path):
+    """Field order, offsets and sizes of the two ABI structs: the C compiler's
+    view (a probe compiled against include/engram.h) against ctypes'."""
+    from hashed_gram_engram_gb300 import _lib
+    structs = {"engram_config": _lib.engram_config, "engram_weights": _lib.engram_weights}
+    hdr = _header()
+    lines = ['#include <stddef.h>', '#include <stdio.h>', '#include "engram.h"', "int main(void) {"]
+    for sname, cls in structs.items():
+        body = re.search(r"typedef struct %s \{(.*?)\} %s;" % (sname, sname), hdr, re.S).group(1)
+        body = re.sub(r"/\*.*?\*/", "", body, flags=re.S)
+        fields = re.findall(r"(\w+)\s*;", body)
+        assert fields == [f for f, _ in cls._fields_], sname
+        lines.append('printf("%s %%zu\\n", sizeof(%s));' % (sname, sname))
+        for f in fields:
+            lines.append('printf("%s.%s %%zu\\n", offsetof(%s, %s));' % (sname, f, sname, f))
+    lines.append("return 0; }")
+    src = tmp_path / "probe.c"
+    src.write_text("\n".join(lines))
+    exe = tmp_path / "probe"
+    cuda_inc = os.path.join(os.environ.get("CUDA_HOME", "/usr/local/cuda"), "include")
+    subprocess.run(["gcc", "-I", os.path.join(ROOT, "include"), "-I", cuda_inc, str(src), "-o",
+                    str(exe)], check=True)
+    got = dict(line.split() for line in subprocess.run([str(exe)], capture_output=True, text=True,
+                                                       check=True).stdout.splitlines())
+    for sname, cls in structs.items():
+        assert int(got[sname]) == ctypes.sizeof(cls), sname
+        for f, _ in cls._fields_:
+            assert int(got[f"{sname}.{f}"]) == getattr(cls, f).offset, f"{sname}.{f}"
