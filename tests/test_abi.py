@@ -125,3 +125,36 @@ def test_binding_structs_match_the_header_layout(tmp_path):
         assert int(got[sname]) == ctypes.sizeof(cls), sname
         for f, _ in cls._fields_:
             assert int(got[f"{sname}.{f}"]) == getattr(cls, f).offset, f"{sname}.{f}"
+
+
+def test_create_validates_the_table_format_without_a_gpu(lib):
+    """engram_create checks its arguments before touching a device: an fp8
+    table needs its scales and a head_dim that is a multiple of 32, and
+    table_format takes only the two defined values.  The device pointers are
+    fake (aligned, never dereferenced); rows and row_offset are real host
+    arrays."""
+    from hashed_gram_engram_gb300 import _lib
+    rows = np.array([1009, 1019, 1033, 1049, 1061, 1069, 1093, 1103] * 2, np.int64)  # >= C
+    off = W.row_offsets(rows)
+    fake = 1 << 40
+
+    def create(table_format, head_dim, table_scale):
+        n_heads = 8 * 32 // (2 * head_dim) if head_dim <= 128 else 1
+        cfg = _lib.engram_config(dim=256, hc_mult=2, max_ngram_size=3, n_heads=n_heads,
+                                 head_dim=head_dim, eps=1e-6, clamp=1e-6, max_tokens=16,
+                                 wkv_format=_lib.ENGRAM_WKV_BF16,
+                                 table_location=_lib.ENGRAM_TABLE_DEVICE, device=0,
+                                 table_format=table_format)
+        w = _lib.engram_weights(table=fake, row_offset=off.ctypes.data, rows=rows.ctypes.data,
+                                wkv=fake, wkv_scale=None, q_weight=fake, k_weight=fake,
+                                table_scale=table_scale)
+        out = ctypes.c_void_p()
+        rc = lib.engram_create(ctypes.byref(cfg), ctypes.byref(w), ctypes.byref(out))
+        assert out.value is None
+        return rc
+
+    # 2 * n_heads hash columns of head_dim: K = 2 * n_heads * head_dim = 512
+    assert create(_lib.ENGRAM_TABLE_FORMAT_E4M3, 32, None) == _lib.ENGRAM_ERR_INVALID_ARG
+    assert create(2, 32, fake) == _lib.ENGRAM_ERR_INVALID_ARG
+    assert create(-1, 32, None) == _lib.ENGRAM_ERR_INVALID_ARG
+    assert create(_lib.ENGRAM_TABLE_FORMAT_E4M3, 16, fake) == _lib.ENGRAM_ERR_UNSUPPORTED
