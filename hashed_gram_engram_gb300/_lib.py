@@ -38,6 +38,7 @@ ENGRAM_TABLE_DEVICE = 0
 ENGRAM_TABLE_HOST_PINNED = 1
 ENGRAM_TABLE_FORMAT_BF16 = 0
 ENGRAM_TABLE_FORMAT_E4M3 = 1
+ENGRAM_FUSED_PLAN_FIELDS = 16
 
 # Every symbol include/engram.h declares.
 EXPORTED = (
@@ -45,6 +46,7 @@ EXPORTED = (
     "engram_forward_host", "engram_last_error", "engram_device_error", "engram_layout",
     "engram_debug_intermediates", "engram_debug_staged_rows", "engram_profile_enable",
     "engram_profile_read", "engram_gate_noalloc", "engram_debug_staged_mx",
+    "engram_debug_fused_plan",
     "engram_debug_keep_value",
 )
 
@@ -104,6 +106,7 @@ def load(path: str | None = None):
             "engram_debug_intermediates": [vp, vp, vp, i64, vp],
             "engram_debug_staged_rows": [vp, vp, i64, vp],
             "engram_debug_staged_mx": [vp, vp, vp, i64, vp],
+            "engram_debug_fused_plan": [vp, i64, i32, vp, i32],
             "engram_debug_keep_value": [vp, ctypes.c_int],
             "engram_profile_enable": [vp, ctypes.c_int],
             "engram_profile_read": [vp, vp],
@@ -197,6 +200,19 @@ def engram_layout(vocab_size, max_ngram_size, n_heads, n_layers=1):
                                 int(n_layers), primes, offsets), "engram_layout")
     return ([list(primes[l * cols:(l + 1) * cols]) for l in range(n_layers)],
             [list(offsets[l * cols:(l + 1) * cols]) for l in range(n_layers)])
+
+
+FUSED_PLAN_KEYS = ("used", "grid", "max_width", "mtiles", "k_blocks", "w_stages", "x_stages",
+                   "w_stage_bytes", "x_stage_bytes", "x_off", "x_ring", "qk_off", "bar_off",
+                   "smem_bytes", "dual", "Tn")
+
+
+def engram_debug_fused_plan(cfg, T, num_sms):
+    """The fused decode kernel's plan for cfg, T and num_sms (host only)."""
+    out = (ctypes.c_int64 * ENGRAM_FUSED_PLAN_FIELDS)()
+    _check(load().engram_debug_fused_plan(ctypes.byref(cfg), int(T), int(num_sms), out,
+                                          ENGRAM_FUSED_PLAN_FIELDS), "engram_debug_fused_plan")
+    return dict(zip(FUSED_PLAN_KEYS, list(out)))
 
 
 def engram_debug_intermediates(h, gate, value, T, stream=None):

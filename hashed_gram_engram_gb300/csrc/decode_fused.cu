@@ -909,6 +909,39 @@ FusedLayout fused_layout(int64_t N, int64_t D, int64_t H, int num_sms) {
     return L;
 }
 
+// Shared memory of one launch: weight ring | token ring | q*k slice |
+// barriers, from the 1024-byte aligned base.
+FusedSmem fused_smem(const FusedLayout& L, const FusedPlan& p, bool mx) {
+    FusedSmem m = {};
+    if (!L.ok || L.max_width <= 0 || p.mtiles < 1) return m;  // no launch: ok stays false
+    m.x_bytes = static_cast<uint32_t>(p.mtiles == 1 ? p.Tn * 128 : 2 * 16384);
+    m.x_stage_bytes = (m.x_bytes + 1023u) / 1024u * 1024u;
+    m.w_stage_bytes = static_cast<uint32_t>((L.max_width * 128 + 1023) / 1024 * 1024);
+    const uint32_t qk_bytes = kMaxFusedSlice * 4, bar_bytes = 1024;
+    const uint32_t budget = kFusedSmemBytes - 1024;  // after 1024-byte alignment
+    // The MMA reads all 128 rows of a token tile (M = 128) even when T is
+    // smaller; rows past T are never used, but the last stage's 16 KB read
+    // must stay inside this CTA's shared memory.
+    // Token stages: about kXRingTarget bytes of them (at least 4), so that
+    // the tiles in flight cover the L2 round trip of the refills.
+    int xs = static_cast<int>(kXRingTarget / m.x_stage_bytes);
+    xs = xs < 4 ? 4 : (xs > kMaxXStages ? kMaxXStages : xs);
+    m.x_stages = xs;
+    m.x_ring = static_cast<uint32_t>(xs) * m.x_stage_bytes;
+    if (p.mtiles == 1 && m.x_ring < static_cast<uint32_t>(xs - 1) * m.x_stage_bytes + 16384u)
+        m.x_ring = static_cast<uint32_t>(xs - 1) * m.x_stage_bytes + 16384u;
+    const uint32_t fixed = m.x_ring + qk_bytes + bar_bytes;
+    int stages = fixed < budget ? static_cast<int>((budget - fixed) / m.w_stage_bytes) : 0;
+    if (stages > kMaxWStages) stages = kMaxWStages;
+    m.ok = stages >= 2;
+    m.w_stages = stages;
+    m.dual = (!mx && p.mtiles == 1) ? 1 : 0;
+    m.x_off = static_cast<uint32_t>(stages) * m.w_stage_bytes;
+    m.qk_off = m.x_off + m.x_ring;
+    m.bar_off = m.qk_off + qk_bytes;
+    return m;
+}
+
 FusedPlan fused_plan(const engram_handle* h, int64_t T) {
     FusedPlan p = {};
     p.Tn = static_cast<int>((T + 15) / 16 * 16);
@@ -1015,32 +1048,17 @@ cudaError_t launch_decode_fused(engram_handle* h, const void* hidden, const int6
     a.inv_d = 1.0f / static_cast<float>(a.D);
     a.inv_sqrt_d = 1.0f / sqrtf(static_cast<float>(a.D));
     a.err = h->ws.err;
-    // shared memory: weight ring | token ring | q*k slice | barriers
-    a.x_bytes = static_cast<uint32_t>(p.mtiles == 1 ? p.Tn * 128 : 2 * 16384);
-    a.x_stage_bytes = (a.x_bytes + 1023u) / 1024u * 1024u;
-    a.w_stage_bytes = static_cast<uint32_t>((L.max_width * 128 + 1023) / 1024 * 1024);
-    const uint32_t qk_bytes = kMaxFusedSlice * 4, bar_bytes = 1024;
-    const uint32_t budget = kFusedSmemBytes - 1024;  // after 1024-byte alignment
-    // The MMA reads all 128 rows of a token tile (M = 128) even when T is
-    // smaller; rows past T are never used, but the last stage's 16 KB read
-    // must stay inside this CTA's shared memory.
-    // Token stages: about kXRingTarget bytes of them (at least 4), so that
-    // the tiles in flight cover the L2 round trip of the refills.
-    int xs = static_cast<int>(kXRingTarget / a.x_stage_bytes);
-    xs = xs < 4 ? 4 : (xs > kMaxXStages ? kMaxXStages : xs);
-    a.x_stages = xs;
-    uint32_t x_ring = static_cast<uint32_t>(xs) * a.x_stage_bytes;
-    if (p.mtiles == 1 && x_ring < static_cast<uint32_t>(xs - 1) * a.x_stage_bytes + 16384u)
-        x_ring = static_cast<uint32_t>(xs - 1) * a.x_stage_bytes + 16384u;
-    const uint32_t fixed = x_ring + qk_bytes + bar_bytes;
-    int stages = fixed < budget ? static_cast<int>((budget - fixed) / a.w_stage_bytes) : 0;
-    if (stages > kMaxWStages) stages = kMaxWStages;
-    if (stages < 2) return cudaErrorInvalidConfiguration;
-    a.w_stages = stages;
-    a.dual = (!mx && p.mtiles == 1) ? 1 : 0;
-    a.x_off = static_cast<uint32_t>(stages) * a.w_stage_bytes;
-    a.qk_off = a.x_off + x_ring;
-    a.bar_off = a.qk_off + qk_bytes;
+    const FusedSmem m = fused_smem(L, p, mx);
+    if (!m.ok) return cudaErrorInvalidConfiguration;
+    a.x_bytes = m.x_bytes;
+    a.x_stage_bytes = m.x_stage_bytes;
+    a.w_stage_bytes = m.w_stage_bytes;
+    a.x_stages = m.x_stages;
+    a.w_stages = m.w_stages;
+    a.dual = m.dual;
+    a.x_off = m.x_off;
+    a.qk_off = m.qk_off;
+    a.bar_off = m.bar_off;
 
     cudaLaunchConfig_t cfg = {};
     cfg.gridDim = dim3(static_cast<unsigned>(L.grid));

@@ -406,6 +406,32 @@ int engram_forward(engram_t* h, const void* hidden, const int64_t hidden_strides
     return cuda_err(h, e);
 }
 
+int engram_debug_fused_plan(const engram_config* cfg, int64_t T, int32_t num_sms,
+                            int64_t* out, int32_t n_out) {
+    if (cfg == nullptr || out == nullptr || n_out < ENGRAM_FUSED_PLAN_FIELDS || num_sms < 1 ||
+        T < 1 || cfg->dim <= 0 || cfg->hc_mult <= 0 || cfg->max_ngram_size < 2 ||
+        cfg->n_heads < 1 || cfg->head_dim <= 0)
+        return ENGRAM_ERR_INVALID_ARG;
+    // the host planning of engram_create and engram_forward, on a handle
+    // that holds only the configuration (no device is touched)
+    engram_handle h;
+    std::memset(static_cast<void*>(&h), 0, sizeof(h));
+    h.cfg = *cfg;
+    h.C = (cfg->max_ngram_size - 1) * cfg->n_heads;
+    h.K = h.C * cfg->head_dim;
+    h.N = cfg->dim * (cfg->hc_mult + 1);
+    h.fused = fused_layout(h.N, cfg->dim, cfg->hc_mult, num_sms);
+    const bool mx = cfg->wkv_format == ENGRAM_WKV_MXFP8;
+    const FusedPlan p = fused_plan(&h, T);
+    const FusedSmem m = fused_smem(h.fused, p, mx);
+    const int64_t v[ENGRAM_FUSED_PLAN_FIELDS] = {
+        fused_supported(&h, T) && m.ok ? 1 : 0, h.fused.grid, h.fused.max_width, p.mtiles,
+        p.k_blocks, m.w_stages, m.x_stages, m.w_stage_bytes, m.x_stage_bytes, m.x_off,
+        m.x_ring, m.qk_off, m.bar_off, kFusedSmemBytes, m.dual, p.Tn};
+    for (int i = 0; i < ENGRAM_FUSED_PLAN_FIELDS; ++i) out[i] = v[i];
+    return ENGRAM_OK;
+}
+
 int engram_forward_host(engram_t* h, const void* hidden_host, const int32_t* hash_ids_host,
                         const uint8_t* token_mask_host, void* out_host, int64_t T,
                         cudaStream_t stream) {

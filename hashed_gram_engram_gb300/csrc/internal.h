@@ -83,6 +83,14 @@ struct FusedPlan {
     int Tn, mtiles, k_blocks;
 };
 
+// Shared-memory plan of one fused launch (byte offsets from the 1024-byte
+// aligned base): weight ring | token ring | q*k slice | barriers.
+struct FusedSmem {
+    uint32_t x_bytes, x_stage_bytes, w_stage_bytes, x_ring, x_off, qk_off, bar_off;
+    int x_stages, w_stages, dual;
+    bool ok;  // at least two weight stages fit
+};
+
 }  // namespace engram
 
 struct engram_handle {
@@ -132,6 +140,7 @@ cudaError_t launch_unpack_scales(const engram_handle* h, uint8_t* out, int64_t T
 // decode_fused.cu
 FusedLayout fused_layout(int64_t N, int64_t D, int64_t H, int num_sms);
 FusedPlan fused_plan(const engram_handle* h, int64_t T);
+FusedSmem fused_smem(const FusedLayout& L, const FusedPlan& p, bool mx);
 bool fused_supported(const engram_handle* h, int64_t T);
 cudaError_t fused_setup_attributes();
 cudaError_t gate_setup_attributes();

@@ -151,6 +151,18 @@ int engram_forward(engram_t* h, const void* hidden, const int64_t hidden_strides
                    const uint8_t* token_mask, void* out, const int64_t out_strides[3],
                    int64_t T, cudaStream_t stream);
 
+/* Validation hook, host only (no device is touched): the fused decode
+ * kernel's plan for a configuration, T tokens and num_sms SMs, as
+ * engram_forward would launch it.  out[0..ENGRAM_FUSED_PLAN_FIELDS) =
+ *   used (1 if the fused kernel serves T), grid, widest column slice,
+ *   token tiles, k-blocks, weight stages, token stages, weight stage bytes,
+ *   token stage bytes, token ring offset, token ring bytes, q*k offset,
+ *   barrier offset, dynamic shared memory bytes, two MMA issuers (0/1), Tn.
+ * Offsets count from the 1024-byte aligned base of the shared memory. */
+#define ENGRAM_FUSED_PLAN_FIELDS 16
+int engram_debug_fused_plan(const engram_config* cfg, int64_t T, int32_t num_sms,
+                            int64_t* out, int32_t n_out);
+
 /* The same forward over HOST buffers: copies hidden, hash_ids and token_mask
  * (pinned host memory for asynchronous copies) into handle-owned device
  * buffers, runs engram_forward, and copies out back to the host buffer, all
