@@ -54,6 +54,8 @@ def parse():
     p.add_argument("--no-e4m3-table", action="store_true",
                    help="skip the workloads whose hash table is fp8 (e4m3 + ue8m0 per 32)")
     p.add_argument("--cpu-seconds", type=float, default=10.0)
+    p.add_argument("--ref-seconds", type=float, default=90.0,
+                   help="wall time the reference arm's warm-up and timed steps aim for")
     p.add_argument("--layers", type=int, default=6)
     p.add_argument("--case", choices=["decode", "prefill", "mxfp8_decode", "mxfp8_prefill"],
                    default=None,
@@ -151,6 +153,13 @@ def cpu_oracle_tokens_per_s(wl, case_host, inputs_host, seconds, max_tokens=None
             return done / el, done, el
 
 
+def decode_config(wl):
+    """The decode workload's keys, shared by both arms' JSON lines."""
+    return {"workload": wl.name, "T": wl.T, "dim": wl.dim, "hc_mult": wl.hc_mult,
+            "n_hash_cols": wl.n_hash_cols, "head_dim": wl.head_dim,
+            "table_rows": wl.total_rows, "wkv": f"bf16 [{wl.N}, {wl.K}]", "mask": None}
+
+
 def run_reference(args):
     """CPU oracle as the reference arm: bounded samples of the decode step."""
     import numpy as np
@@ -169,9 +178,9 @@ def run_reference(args):
                 rows=np.asarray(wl.rows, np.int64), wkv=W.bits(wts["wkv"]),
                 q=W.bits(wts["q_weight"]), k=W.bits(wts["k_weight"]))
     inp = dict(hidden=W.bits(step["hidden"]), ids=step["hash_ids"].numpy(), mask=None)
-    # size the per-step sample so that warmup + steps take about 90 s
+    # size the per-step sample so that warmup + steps take about --ref-seconds
     per_tok, _, _ = cpu_oracle_tokens_per_s(wl, host, inp, 0.0, max_tokens=1)
-    budget = 90.0 / max(1, args.steps + args.warmup)
+    budget = args.ref_seconds / max(1, args.steps + args.warmup)
     n = int(max(1, min(wl.T, budget * per_tok)))
     for _ in range(args.warmup):
         cpu_oracle_tokens_per_s(wl, host, inp, 0.0, max_tokens=n)
@@ -185,9 +194,7 @@ def run_reference(args):
         "n_gpus": world, "steps": args.steps, "warmup": args.warmup,
         "ms_per_step": 1000.0 * el / args.steps, "higher_is_better": True, "scaling": "weak",
         "vs_baseline": None, "dtype": "f64", "data": "synthetic",
-        "config": {"workload": wl.name, "T": wl.T, "dim": wl.dim, "hc_mult": wl.hc_mult,
-                   "n_hash_cols": wl.n_hash_cols, "head_dim": wl.head_dim,
-                   "wkv": "bf16 [20480, 1024]", "tokens_per_step_sample": n},
+        "config": dict(decode_config(wl), tokens_per_step_sample=n),
         "cpu_baseline": {"value": value, "unit": "tokens/s", "cores": 1, "kind": "oracle",
                          "sample": f"{n} of the {wl.T} decode-step tokens per step"},
         "e2e": {"value": value, "unit": "tokens/s", "h2d_bytes_per_step": 0,
@@ -456,9 +463,7 @@ def main():
         "steps": steps, "warmup": args.warmup, "ms_per_step": ms_step,
         "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "bf16",
         "data": "synthetic",
-        "config": {"workload": "decode", "T": wl.T, "dim": wl.dim, "hc_mult": wl.hc_mult,
-                   "n_hash_cols": wl.n_hash_cols, "head_dim": wl.head_dim,
-                   "table_rows": wl.total_rows, "wkv": "bf16 [20480, 1024]", "mask": None,
+        "config": {**decode_config(wl),
                    "layers_rotated": NL,
                    "l2": f"inputs larger than L2: {NL} layers' weights ({NL * 40} MiB) rotated",
                    "timing": f"CUDA graph of {per_graph} steps replayed {replays}x, events on "
