@@ -26,15 +26,16 @@ typedef CUresult (*EncodeTiledFn)(CUtensorMap*, CUtensorMapDataType, cuuint32_t,
                                   CUtensorMapL2promotion, CUtensorMapFloatOOBfill);
 
 EncodeTiledFn encode_fn() {
-    static EncodeTiledFn fn = nullptr;
-    if (fn == nullptr) {
+    // initialised once, also when handles are created from several threads
+    static const EncodeTiledFn fn = [] {
         void* p = nullptr;
         cudaDriverEntryPointQueryResult q;
         if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &p, 12000,
                                              cudaEnableDefault, &q) == cudaSuccess &&
             q == cudaDriverEntryPointSuccess)
-            fn = reinterpret_cast<EncodeTiledFn>(p);
-    }
+            return reinterpret_cast<EncodeTiledFn>(p);
+        return static_cast<EncodeTiledFn>(nullptr);
+    }();
     return fn;
 }
 
@@ -332,6 +333,7 @@ int engram_lookup(engram_t* h, const int32_t* hash_ids, int64_t ids_row_stride, 
     }
     if (hash_ids == nullptr || ids_row_stride < h->C) return set_err(h, ENGRAM_ERR_INVALID_ARG);
     DeviceGuard guard(h->cfg.device);
+    if (!guard.ok) return set_err(h, ENGRAM_ERR_CUDA);
     cudaError_t e = launch_gather(h, hash_ids, ids_row_stride, T, background != 0,
                                   h->cfg.wkv_format == ENGRAM_WKV_MXFP8, stream, false);
     if (e != cudaSuccess) return cuda_err(h, e);
@@ -360,6 +362,7 @@ int engram_forward(engram_t* h, const void* hidden, const int64_t hidden_strides
     if (hash_ids == nullptr && h->staged_T != T) return set_err(h, ENGRAM_ERR_INVALID_ARG);
 
     DeviceGuard guard(h->cfg.device);
+    if (!guard.ok) return set_err(h, ENGRAM_ERR_CUDA);
     const bool prof = h->profiling != 0;
     bool first = true;
     cudaError_t e = cudaSuccess;
@@ -375,7 +378,7 @@ int engram_forward(engram_t* h, const void* hidden, const int64_t hidden_strides
         mark(1);
         e = launch_decode_fused(h, hidden, hidden_strides, hash_ids, ids_row_stride, token_mask,
                                 out, out_strides, T, stream, !prof);
-        if (hash_ids != nullptr) h->staged_T = T;  // the kernel staged the rows
+        if (hash_ids != nullptr && e == cudaSuccess) h->staged_T = T;  // the kernel staged the rows
         mark(2);
         mark(3);
         h->last_path = 3;
@@ -442,6 +445,7 @@ int engram_forward_host(engram_t* h, const void* hidden_host, const int32_t* has
     if (hidden_host == nullptr || hash_ids_host == nullptr || out_host == nullptr)
         return set_err(h, ENGRAM_ERR_INVALID_ARG);
     DeviceGuard guard(h->cfg.device);
+    if (!guard.ok) return set_err(h, ENGRAM_ERR_CUDA);
     const int64_t H = h->cfg.hc_mult, D = h->cfg.dim, C = h->C;
     Workspace& ws = h->ws;
     cudaError_t e = cudaSuccess;
@@ -483,6 +487,7 @@ int engram_last_error(engram_t* h, int sync) {
 int engram_device_error(engram_t* h, uint32_t* bits, int clear) {
     if (h == nullptr || bits == nullptr) return ENGRAM_ERR_INVALID_ARG;
     DeviceGuard guard(h->cfg.device);
+    if (!guard.ok) return ENGRAM_ERR_CUDA;
     cudaError_t e = cudaDeviceSynchronize();
     if (e == cudaSuccess) e = cudaMemcpy(bits, h->ws.err, sizeof(unsigned), cudaMemcpyDeviceToHost);
     if (e == cudaSuccess && clear) e = cudaMemset(h->ws.err, 0, sizeof(unsigned));
@@ -500,6 +505,7 @@ int engram_debug_intermediates(engram_t* h, float* gate, float* value, int64_t T
     if (h == nullptr || T < 0 || T > h->cfg.max_tokens) return ENGRAM_ERR_INVALID_ARG;
     if (T == 0) return ENGRAM_OK;
     DeviceGuard guard(h->cfg.device);
+    if (!guard.ok) return ENGRAM_ERR_CUDA;
     cudaError_t e = cudaSuccess;
     if (gate != nullptr)
         e = cudaMemcpyAsync(gate, h->ws.gate, T * h->cfg.hc_mult * sizeof(float),
@@ -518,6 +524,7 @@ int engram_debug_staged_rows(engram_t* h, void* rows, int64_t T, cudaStream_t st
         return ENGRAM_ERR_INVALID_ARG;
     if (T == 0) return ENGRAM_OK;
     DeviceGuard guard(h->cfg.device);
+    if (!guard.ok) return ENGRAM_ERR_CUDA;
     cudaError_t e = cudaMemcpyAsync(rows, h->ws.staged, T * h->K * 2, cudaMemcpyDeviceToDevice,
                                     stream);
     return e == cudaSuccess ? ENGRAM_OK : ENGRAM_ERR_CUDA;
@@ -529,6 +536,7 @@ int engram_debug_staged_mx(engram_t* h, uint8_t* codes, uint8_t* scales, int64_t
     if (h->cfg.wkv_format != ENGRAM_WKV_MXFP8) return ENGRAM_ERR_INVALID_ARG;
     if (T == 0) return ENGRAM_OK;
     DeviceGuard guard(h->cfg.device);
+    if (!guard.ok) return ENGRAM_ERR_CUDA;
     cudaError_t e = cudaSuccess;
     if (codes != nullptr)
         e = cudaMemcpyAsync(codes, h->ws.staged_q, T * h->K, cudaMemcpyDeviceToDevice, stream);
@@ -545,9 +553,17 @@ int engram_debug_keep_value(engram_t* h, int enable) {
 int engram_profile_enable(engram_t* h, int enable) {
     if (h == nullptr) return ENGRAM_ERR_INVALID_ARG;
     DeviceGuard guard(h->cfg.device);
+    if (!guard.ok) return set_err(h, ENGRAM_ERR_CUDA);
     if (enable && h->ev[0] == nullptr) {
-        for (cudaEvent_t& ev : h->ev)
-            if (cudaEventCreate(&ev) != cudaSuccess) return set_err(h, ENGRAM_ERR_CUDA);
+        for (cudaEvent_t& ev : h->ev) {
+            if (cudaEventCreate(&ev) == cudaSuccess) continue;
+            ev = nullptr;
+            for (cudaEvent_t& made : h->ev) {  // all or none
+                if (made != nullptr) cudaEventDestroy(made);
+                made = nullptr;
+            }
+            return set_err(h, ENGRAM_ERR_CUDA);
+        }
     }
     h->profiling = enable != 0;
     return set_err(h, ENGRAM_OK);
@@ -556,6 +572,7 @@ int engram_profile_enable(engram_t* h, int enable) {
 int engram_profile_read(engram_t* h, float ms[3]) {
     if (h == nullptr || ms == nullptr || h->ev[0] == nullptr) return ENGRAM_ERR_INVALID_ARG;
     DeviceGuard guard(h->cfg.device);
+    if (!guard.ok) return ENGRAM_ERR_CUDA;
     if (cudaEventSynchronize(h->ev[3]) != cudaSuccess) return set_err(h, ENGRAM_ERR_CUDA);
     for (int i = 0; i < 3; ++i) {
         ms[i] = 0.f;
