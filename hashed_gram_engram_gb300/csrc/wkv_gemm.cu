@@ -503,7 +503,7 @@ cudaError_t launch_wkv_tokens_m(const engram_handle* h, const void* hidden, int6
     if (a.stages > kMaxStages) a.stages = kMaxStages;
     // MXFP8: two accumulators plus a 16-column scale slot per stage in TMEM
     if (mx && a.stages > (512 - 2 * bn) / 16) a.stages = (512 - 2 * bn) / 16;
-    a.idesc = idesc_bf16(kBM, kBNPrefill);
+    a.idesc = idesc_bf16(kBM, kBNPrefill);  // bf16 only: MXFP8 builds one per k step
     a.D = static_cast<int>(h->cfg.dim);
     a.H = static_cast<int>(h->cfg.hc_mult);
     a.J = (mx ? 2 : 1) * (a.D / bn);  // MXFP8: a partial record per half tile
