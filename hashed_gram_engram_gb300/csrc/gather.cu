@@ -5,9 +5,10 @@
 // consecutive lanes, so every 128-byte row is one fully used request.  Each
 // thread keeps kUnroll independent row reads in flight to cover the
 // latency of random rows in HBM or, for an offloaded table, in host memory
-// across the host link.  A persistent grid near the SM count (halved for
-// background lookups) follows the page's note that the table dwarfs TLB
-// reach.  Optionally the same pass emits the MXFP8 form of the rows: e4m3
+// across the host link.  The grid is capped at a few CTAs per SM (half the
+// SMs for a background lookup) that loop over the chunks: the table spans
+// far more memory than the TLBs map, as the lookup's page points out.
+// Optionally the same pass emits the MXFP8 form of the rows: e4m3
 // codes and one E8M0 scale per 32 consecutive k (smallest power of two that
 // keeps the block maximum within 448; round-to-nearest-even, saturating),
 // the scales stored as the tcgen05 scale-factor atoms the GEMM copies.

@@ -4,8 +4,8 @@
  * One Engram layer, as documented on the vLLM API page
  * "vllm.models.deepseek_v4_1.common.engram" (class Engram): hash ids fetch
  * one row per hash column from prime-sized hashed n-gram tables; the wkv
- * projection turns the concatenated rows into one key per hc copy plus a
- * shared value; a gate -- sigmoid of the signed square root of a normalised
+ * projection maps the concatenated rows to a key for each hc copy and a
+ * value common to all copies; a gate -- sigmoid of the signed square root of a normalised
  * dot product of the residual stream against the key -- scales the value
  * that is added to the stream; a False token mask leaves a position
  * untouched.
