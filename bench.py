@@ -194,7 +194,9 @@ def run_reference(args):
         "n_gpus": world, "steps": args.steps, "warmup": args.warmup,
         "ms_per_step": 1000.0 * el / args.steps, "higher_is_better": True, "scaling": "weak",
         "vs_baseline": None, "dtype": "f64", "data": "synthetic",
-        "config": dict(decode_config(wl), tokens_per_step_sample=n),
+        "config": dict(decode_config(wl), tokens_per_step_sample=n,
+                       seeds={"layers": [int(wl.seed)],
+                              "generator": "torch.Generator.manual_seed per tensor kind"}),
         "cpu_baseline": {"value": value, "unit": "tokens/s", "cores": 1, "kind": "oracle",
                          "sample": f"{n} of the {wl.T} decode-step tokens per step"},
         "e2e": {"value": value, "unit": "tokens/s", "h2d_bytes_per_step": 0,
@@ -465,6 +467,8 @@ def main():
         "data": "synthetic",
         "config": {**decode_config(wl),
                    "layers_rotated": NL,
+                   "seeds": {"layers": [int(L["wl"].seed) for L in layers],
+                             "generator": "torch.Generator.manual_seed per tensor kind"},
                    "l2": f"inputs larger than L2: {NL} layers' weights ({NL * 40} MiB) rotated",
                    "timing": f"CUDA graph of {per_graph} steps replayed {replays}x, events on "
                              "the launch stream",

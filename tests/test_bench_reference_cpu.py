@@ -30,6 +30,7 @@ def test_reference_arm_json_line():
     cfg = d["config"]
     for k, v in bench.decode_config(W.DECODE).items():
         assert cfg[k] == v, k
+    assert cfg["seeds"]["layers"] == [W.DECODE.seed]
     n = cfg["tokens_per_step_sample"]
     assert 1 <= n <= W.DECODE.T
     # the value is the sampled tokens over the timed steps' wall time
