@@ -5,7 +5,7 @@ import math
 
 import numpy as np
 import pytest
-import sympy
+sympy = pytest.importorskip("sympy")
 import torch
 
 import oracle
