@@ -25,10 +25,12 @@ from ._lib import (EngramError, engram_config, engram_create, engram_debug_inter
                    engram_lookup, engram_profile_enable, engram_profile_read,
                    engram_weights, ENGRAM_WKV_BF16, ENGRAM_WKV_MXFP8,
                    ENGRAM_TABLE_DEVICE, ENGRAM_TABLE_HOST_PINNED, ENGRAM_TABLE_FORMAT_BF16,
-                   ENGRAM_TABLE_FORMAT_E4M3, ENGRAM_DEVERR_BAD_HASH_ID, ENGRAM_DEVERR_TIMEOUT)
+                   ENGRAM_TABLE_FORMAT_E4M3, ENGRAM_DEVERR_BAD_HASH_ID, ENGRAM_DEVERR_TIMEOUT,
+                   engram_prefetch_create, engram_prefetch_destroy, engram_prefetch_forward,
+                   engram_prefetch_join, engram_prefetch_pending, engram_prefetch_start)
 
 __all__ = [
-    "Engram", "EngramError", "engram_config", "engram_weights", "engram_create",
+    "Engram", "EngramPrefetch", "EngramError", "engram_config", "engram_weights", "engram_create",
     "engram_destroy", "engram_lookup", "engram_forward", "engram_forward_host",
     "engram_gate_noalloc", "engram_debug_staged_mx", "engram_debug_keep_value",
     "engram_last_error", "engram_device_error", "engram_layout", "engram_debug_intermediates",
@@ -36,6 +38,8 @@ __all__ = [
     "ENGRAM_WKV_BF16", "ENGRAM_WKV_MXFP8", "ENGRAM_TABLE_DEVICE",
     "ENGRAM_TABLE_HOST_PINNED", "ENGRAM_TABLE_FORMAT_BF16", "ENGRAM_TABLE_FORMAT_E4M3",
     "ENGRAM_DEVERR_BAD_HASH_ID", "ENGRAM_DEVERR_TIMEOUT",
+    "engram_prefetch_create", "engram_prefetch_destroy", "engram_prefetch_start",
+    "engram_prefetch_forward", "engram_prefetch_join", "engram_prefetch_pending",
 ]
 
 
@@ -159,3 +163,66 @@ class Engram:
         scales = torch.empty((T, K // 32), dtype=torch.uint8, device=dev)
         engram_debug_staged_mx(self.handle, codes, scales, T, stream)
         return codes, scales
+
+
+class EngramPrefetch:
+    """Lookups of several layers run ahead on a side stream (class
+    EngramPrefetch's start / forward / join on the prefetch page, with
+    Engram.prepare_embeddings).  start() stages every layer's rows as soon
+    as the step's hash ids exist; forward(i, ...) waits only for layer i's
+    rows.  The layers must outlive this object; while it lives, only it
+    looks up rows for them."""
+
+    def __init__(self, layers):
+        self.layers = list(layers)
+        self.handle = engram_prefetch_create([L.handle for L in self.layers])
+        self.T = None
+
+    def close(self):
+        if getattr(self, "handle", None):
+            engram_prefetch_destroy(self.handle)
+            self.handle = None
+
+    def __del__(self):
+        try:
+            self.close()
+        except Exception:
+            pass
+
+    def _stream(self, stream):
+        import torch
+        if stream is not None:
+            return stream
+        return torch.cuda.current_stream(torch.device("cuda", self.layers[0].device))
+
+    def start(self, hash_ids, background=True, stream=None):
+        """hash_ids: one int32 [T, C] device tensor per layer (same T)."""
+        assert len(hash_ids) == len(self.layers)
+        T = int(hash_ids[0].shape[0])
+        assert all(int(x.shape[0]) == T for x in hash_ids)
+        strides = [x.stride(0) if T else L.n_hash_cols for x, L in zip(hash_ids, self.layers)]
+        engram_prefetch_start(self.handle, hash_ids, strides, T, int(bool(background)),
+                              self._stream(stream))
+        self.T = T
+
+    def forward(self, i, hidden, hash_ids=None, token_mask=None, out=None, stream=None):
+        """Layer i's forward; hash_ids is needed only when nothing was staged
+        ahead for it."""
+        import torch
+        T = hidden.shape[0]
+        if out is None:
+            out = torch.empty_like(hidden)
+        ids_stride = hash_ids.stride(0) if hash_ids is not None and T else \
+            self.layers[i].n_hash_cols
+        mask = None
+        if token_mask is not None:
+            mask = token_mask if token_mask.dtype == torch.uint8 else token_mask.to(torch.uint8)
+        engram_prefetch_forward(self.handle, i, hidden, hidden.stride(), hash_ids, ids_stride,
+                                mask, out, out.stride(), T, self._stream(stream))
+        return out
+
+    def join(self, stream=None):
+        engram_prefetch_join(self.handle, self._stream(stream))
+
+    def pending(self, i) -> bool:
+        return engram_prefetch_pending(self.handle, i)

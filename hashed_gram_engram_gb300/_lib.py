@@ -48,6 +48,8 @@ EXPORTED = (
     "engram_profile_read", "engram_gate_noalloc", "engram_debug_staged_mx",
     "engram_debug_fused_plan",
     "engram_debug_keep_value",
+    "engram_prefetch_create", "engram_prefetch_destroy", "engram_prefetch_start",
+    "engram_prefetch_forward", "engram_prefetch_join", "engram_prefetch_pending",
 )
 
 
@@ -112,6 +114,12 @@ def load(path: str | None = None):
             "engram_profile_read": [vp, vp],
             "engram_gate_noalloc": [vp, vp, vp, i64, vp, vp, vp, vp, vp, i64, i64, i64,
                                     ctypes.c_double, ctypes.c_double, vp],
+            "engram_prefetch_create": [vp, i32, vp],
+            "engram_prefetch_destroy": [vp],
+            "engram_prefetch_start": [vp, vp, vp, i64, ctypes.c_int, vp],
+            "engram_prefetch_forward": [vp, i32, vp, vp, vp, i64, vp, vp, vp, i64, vp],
+            "engram_prefetch_join": [vp, vp],
+            "engram_prefetch_pending": [vp, i32],
         }
         for name, args in sig.items():
             f = getattr(L, name)
@@ -253,3 +261,42 @@ def engram_gate_noalloc(hidden, hidden_strides, kv, kv_row_stride, q_weight, k_w
         _ptr(hidden), _i64x3(hidden_strides), _ptr(kv), int(kv_row_stride), _ptr(q_weight),
         _ptr(k_weight), _ptr(token_mask), _ptr(out), _i64x3(out_strides), int(T), int(H),
         int(D), float(eps), float(clamp), _stream(stream)), "engram_gate_noalloc")
+
+
+def engram_prefetch_create(handles) -> int:
+    arr = (ctypes.c_void_p * len(handles))(*handles)
+    p = ctypes.c_void_p()
+    _check(load().engram_prefetch_create(arr, len(handles), ctypes.byref(p)),
+           "engram_prefetch_create")
+    return p.value
+
+
+def engram_prefetch_destroy(p) -> None:
+    _check(load().engram_prefetch_destroy(p), "engram_prefetch_destroy")
+
+
+def engram_prefetch_start(p, hash_ids, ids_row_strides, T, background=1, stream=None):
+    n = len(hash_ids)
+    ids = (ctypes.c_void_p * n)(*[_ptr(x) for x in hash_ids])
+    st = (ctypes.c_int64 * n)(*[int(x) for x in ids_row_strides])
+    return _check(load().engram_prefetch_start(p, ids, st, int(T), int(background),
+                                               _stream(stream)), "engram_prefetch_start")
+
+
+def engram_prefetch_forward(p, layer, hidden, hidden_strides, hash_ids, ids_row_stride,
+                            token_mask, out, out_strides, T, stream=None):
+    return _check(load().engram_prefetch_forward(
+        p, int(layer), _ptr(hidden), _i64x3(hidden_strides), _ptr(hash_ids),
+        int(ids_row_stride), _ptr(token_mask), _ptr(out), _i64x3(out_strides), int(T),
+        _stream(stream)), "engram_prefetch_forward")
+
+
+def engram_prefetch_join(p, stream=None):
+    return _check(load().engram_prefetch_join(p, _stream(stream)), "engram_prefetch_join")
+
+
+def engram_prefetch_pending(p, layer) -> bool:
+    rc = load().engram_prefetch_pending(p, int(layer))
+    if rc < 0:
+        _check(rc, "engram_prefetch_pending")
+    return rc == 1

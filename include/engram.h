@@ -259,6 +259,58 @@ int engram_debug_staged_mx(engram_t* h, uint8_t* codes, uint8_t* scales, int64_t
 int engram_profile_enable(engram_t* h, int enable);
 int engram_profile_read(engram_t* h, float ms[3]);
 
+/* ------------------------------------------------------------------------
+ * Lookups of several layers run ahead on a side stream.  This follows the
+ * prefetch page ("vllm.models.deepseek_v41.nvidia.specialized_decode.
+ * engram.prefetch": class EngramPrefetch with start, forward and join, and
+ * the module note on looking up rows on a prefetch stream ahead of the
+ * decoder layers) and Engram.prepare_embeddings.  The engine learns a step's
+ * hash ids before its decoder layers run.  engram_prefetch_start stages
+ * every layer's rows at that point; each layer's forward then waits only
+ * for its own rows.  The pages' side-stream wkv chain is not part of this.
+ *
+ * Host-side orchestration only: no kernel of its own.
+ * engram_prefetch_create
+ *   layers: n_layers >= 1 handles on one device.  They are borrowed and must
+ *   outlive the prefetcher; while it lives, only it may call engram_lookup
+ *   on them.  It owns a non-blocking side stream and one event per layer.
+ * engram_prefetch_start
+ *   Orders the side stream after all work issued on `stream` so far.  That
+ *   covers the hash ids, and the previous step's forwards if they ran on
+ *   `stream`: their staged rows are about to be overwritten.  Then, on the
+ *   side stream, it runs engram_lookup(layers[l], hash_ids[l],
+ *   ids_row_stride[l], T, background) for every layer and records the
+ *   layer's event.  hash_ids[l]: device int32 [T, C_l] with row stride
+ *   ids_row_stride[l] >= C_l.  Each layer is then "pending".  Returns the
+ *   first failing lookup's code; the layers before it stay pending.
+ * engram_prefetch_forward
+ *   Layer `layer`'s engram_forward on `stream`.  If the layer is pending,
+ *   `stream` first waits on the layer's event, and the forward consumes the
+ *   staged rows: T must equal the start's T, and hash_ids is ignored.  If
+ *   not, it is the plain forward and needs hash_ids.  Either way the layer
+ *   is no longer pending afterwards.
+ * engram_prefetch_join
+ *   Makes `stream` wait for every pending layer's lookup and clears the
+ *   pending flags.  Call it before ending a stream capture that started the
+ *   prefetch and did not forward every layer.
+ * engram_prefetch_pending
+ *   1 if the layer is pending, 0 if not, ENGRAM_ERR_INVALID_ARG for a bad
+ *   argument.
+ * A stream capture of start / forward / join on one stream records the side
+ * stream's work into the graph. */
+typedef struct engram_prefetch engram_prefetch_t;
+int engram_prefetch_create(engram_t* const* layers, int32_t n_layers, engram_prefetch_t** out);
+int engram_prefetch_destroy(engram_prefetch_t* p);
+int engram_prefetch_start(engram_prefetch_t* p, const int32_t* const* hash_ids,
+                          const int64_t* ids_row_stride, int64_t T, int background,
+                          cudaStream_t stream);
+int engram_prefetch_forward(engram_prefetch_t* p, int32_t layer, const void* hidden,
+                            const int64_t hidden_strides[3], const int32_t* hash_ids,
+                            int64_t ids_row_stride, const uint8_t* token_mask, void* out,
+                            const int64_t out_strides[3], int64_t T, cudaStream_t stream);
+int engram_prefetch_join(engram_prefetch_t* p, cudaStream_t stream);
+int engram_prefetch_pending(const engram_prefetch_t* p, int32_t layer);
+
 #ifdef __cplusplus
 }
 #endif

@@ -75,6 +75,23 @@ def test_null_handle_arguments_are_rejected_without_a_gpu(lib):
     assert out.value is None
 
 
+def test_prefetch_arguments_are_rejected_without_a_gpu(lib):
+    out = ctypes.c_void_p()
+    none = (ctypes.c_void_p * 2)(None, None)
+    assert lib.engram_prefetch_create(None, 1, ctypes.byref(out)) == -1
+    assert lib.engram_prefetch_create(none, 0, ctypes.byref(out)) == -1
+    assert lib.engram_prefetch_create(none, 2, ctypes.byref(out)) == -1  # null handles
+    assert lib.engram_prefetch_create(none, 2, None) == -1
+    assert out.value is None
+    st = (ctypes.c_int64 * 3)(0, 0, 1)
+    assert lib.engram_prefetch_start(None, none, st, 1, 1, None) == -1
+    assert lib.engram_prefetch_forward(None, 0, None, st, None, 0, None, None, st, 1,
+                                       None) == -1
+    assert lib.engram_prefetch_join(None, None) == -1
+    assert lib.engram_prefetch_pending(None, 0) == -1
+    assert lib.engram_prefetch_destroy(None) == 0
+
+
 def test_product_package_never_reaches_the_oracle():
     pkg = os.path.join(ROOT, "hashed_gram_engram_gb300")
     for dirpath, _, files in os.walk(pkg):

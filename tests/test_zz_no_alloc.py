@@ -5,8 +5,8 @@ array instead of allocated memory.
 Its output is checked against engram_forward (the handle's own path) on the
 same inputs, for two calls in a row with different inputs and sizes, so a
 call that read another call's leftover partials would fail.  The file sorts
-last so that it also runs after every other test has used the device; it
-builds its own layers and passes alone as well."""
+after the single-layer parity files, so it also runs once those have used
+the device; it builds its own layers and passes alone as well."""
 import numpy as np
 import pytest
 import torch
