@@ -285,7 +285,8 @@ __global__ void __launch_bounds__(kThreads, 1)
     uint4 pre[4] = {}, pre2[4] = {};
     bool pre_good = true, pre2_good = true;
     if (warp >= 2 && warp < 6 && tid - 64 < g_n) pre_good = fetch(tid - 64, pre);
-    if constexpr (!kMx)  // (MXFP8 items are 32 k: a CTA never has more than 128)
+    if constexpr (!kMx)  // (MXFP8: one item per thread ahead; a second one measured slower;
+                         // the gather loop below fetches any further items either way)
         if (warp >= 2 && warp < 6 && tid - 64 + 128 < g_n) pre2_good = fetch(tid - 64 + 128, pre2);
     if (warp == 1) {
         tmem_alloc(tmem_slot, kTmemCols);
