@@ -5,10 +5,10 @@
  * "vllm.models.deepseek_v4_1.common.engram" (class Engram): hash ids fetch
  * one row per hash column from prime-sized hashed n-gram tables; the wkv
  * projection maps the concatenated rows to a key for each hc copy and a
- * value common to all copies; a gate -- sigmoid of the signed square root of a normalised
- * dot product of the residual stream against the key -- scales the value
- * that is added to the stream; a False token mask leaves a position
- * untouched.
+ * value common to all copies; a gate -- sigmoid of the signed square root
+ * of a normalised dot product of the residual stream against the key --
+ * scales the value that is added to the stream; a False token mask leaves
+ * a position untouched.
  *
  * Notation: T tokens, D = dim (hidden_size), H = hc_mult, C = n_hash_cols =
  * (max_ngram_size - 1) * n_heads, E = head_dim, K = C * E, N = D * (H + 1).
