@@ -273,10 +273,12 @@ def make_layer(W, Engram, wl, device_index, max_tokens, layer_seed, table=None):
 def algorithmic_bytes(wl):
     """HBM bytes one forward of wl must move: wkv (and its scales), hidden in
     and out, the gathered rows (from HBM unless the table is offloaded),
-    ids, q and k."""
+    ids, the token mask (one byte per token, when there is one), q and k."""
     mx = wl.wkv_format == "mxfp8"
     b = (wl.N * wl.K * (1 if mx else 2) + 2 * wl.T * wl.hc_mult * wl.dim * 2
          + wl.T * wl.n_hash_cols * 4 + 2 * wl.hc_mult * wl.dim * 2)
+    if wl.mask_p is not None:
+        b += wl.T
     if mx:
         b += (wl.N // 32) * (wl.K // 32)
     if wl.table_location != "host":
