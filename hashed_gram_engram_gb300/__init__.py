@@ -12,8 +12,6 @@ is no CPU or PyTorch fallback: without the built library every call raises.
 """
 from __future__ import annotations
 
-import ctypes
-
 import numpy as np
 
 from . import _lib

@@ -5,14 +5,13 @@ and ragged tails on both wkv schedules), whole-output at the decode
 config, sampled tokens at the prefill config, plus the edge cases: T = 0,
 maximum T, all-False masks, in-place and strided views, out-of-range ids,
 and run-to-run determinism."""
-import dataclasses
 
 import numpy as np
 import pytest
 import torch
 
 import workloads as W
-from engram_case import Case, compare, np_bf16
+from engram_case import Case, compare
 from hashed_gram_engram_gb300 import EngramError, ENGRAM_DEVERR_BAD_HASH_ID
 
 pytestmark = pytest.mark.gpu

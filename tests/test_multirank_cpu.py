@@ -12,7 +12,6 @@ import subprocess
 import sys
 
 import numpy as np
-import pytest
 import torch.distributed as dist
 import torch.multiprocessing as mp
 
