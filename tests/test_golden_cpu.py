@@ -76,3 +76,15 @@ def test_out_bits(ex, res):
     assert np.array_equal(res["out_bf16"], exp)
     # the masked token keeps hidden's -0.0
     assert res["out_bf16"][3, 1, 0] == 0x8000
+
+
+def test_fixture_regenerates_from_its_derivation(ex):
+    """The expected block is what tests/golden/derive_worked_example.py
+    computes from the fixture's inputs in exact arithmetic (fractions and
+    50-digit decimals, no oracle code)."""
+    import importlib.util
+    spec = importlib.util.spec_from_file_location(
+        "derive_worked_example", os.path.join(HERE, "golden", "derive_worked_example.py"))
+    mod = importlib.util.module_from_spec(spec)
+    spec.loader.exec_module(mod)
+    assert mod.derive(ex) == ex["expected"]

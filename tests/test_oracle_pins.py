@@ -171,6 +171,68 @@ def test_wkv_mxfp8_matches_numpy_matmul():
     assert np.allclose(kv, np_bf16(A) @ Wf.T, rtol=1e-12, atol=1e-15)
 
 
+def _mx_qact_case(seed=14, T=5, K=128, N=96):
+    """Random e4m3 codes for both operands (torch casts of normals: never a
+    NaN code), activation scales that differ per token and per 32-k block,
+    weight scales that differ per 32-row and per 32-k block, and the
+    products decoded independently of the oracle: torch's float8_e4m3fn
+    widening times an exact ldexp power of two."""
+    rng = np.random.default_rng(seed)
+    Aq = torch.from_numpy(rng.standard_normal((T, K)) * 40).to(torch.float8_e4m3fn)
+    Wq = torch.from_numpy(rng.standard_normal((N, K))).to(torch.float8_e4m3fn)
+    As = rng.permutation(np.arange(100, 100 + T * (K // 32))).reshape(T, K // 32).astype(np.uint8)
+    Ws = rng.permutation(np.arange(112, 112 + (N // 32) * (K // 32))).reshape(
+        N // 32, K // 32).astype(np.uint8)
+    a_dec = Aq.to(torch.float64).numpy() * np.ldexp(1.0, np.repeat(As.astype(np.int64) - 127, 32, 1))
+    w_dec = Wq.to(torch.float64).numpy() * np.ldexp(1.0, np.repeat(np.repeat(
+        Ws.astype(np.int64) - 127, 32, 0), 32, 1))
+    return (Aq.view(torch.uint8).numpy(), As, Wq.view(torch.uint8).numpy(), Ws,
+            a_dec @ w_dec.T)
+
+
+def test_wkv_mxfp8_qact_matches_numpy_matmul():
+    """Both operands MXFP8 (the quantised-activation reference of the
+    block-scaled MMA path): kv[t, n] = sum_k a(t, k) w(n, k), a with the
+    scale of (token t, k-block k/32), w with that of (row block n/32,
+    k-block k/32)."""
+    Aq, As, Wq, Ws, ref = _mx_qact_case()
+    kv = oracle.wkv_mxfp8_qact(Aq, As, Wq, Ws)
+    assert kv.shape == ref.shape
+    assert np.allclose(kv, ref, rtol=1e-12, atol=0.0)
+    # a scale read with the wrong index would move whole 32-blocks by powers
+    # of two: the check above is far tighter than that
+    assert np.abs(ref).max() > 0
+
+
+def test_forward_quantize_act_uses_quantised_rows_and_dequantised_weights():
+    """forward(..., quantize_act=True) = mx_quantize (pinned above) of the
+    gathered rows, then the contraction against the dequantised weights,
+    recomputed here with torch and numpy."""
+    wl = W.TINY_MXFP8
+    d = W.make_all(wl, "cpu")
+    Wq = W.bits(d["wkv"])
+    Ws = d["wkv_scale"].numpy() if hasattr(d["wkv_scale"], "numpy") else d["wkv_scale"]
+    r = oracle.forward(W.bits(d["table"]), d["row_offset"], d["rows"], d["hash_ids"].numpy(),
+                       wl.head_dim, Wq, W.bits(d["hidden"]), W.bits(d["q_weight"]),
+                       W.bits(d["k_weight"]), W.bits(d["token_mask"]), Ws=Ws,
+                       quantize_act=True)
+    T, K = wl.T, wl.K
+    codes, scales = oracle.mx_quantize(r["rows"].reshape(T, K))
+    a_dec = torch.from_numpy(codes).view(torch.float8_e4m3fn).to(torch.float64).numpy() * \
+        np.ldexp(1.0, np.repeat(scales.astype(np.int64) - 127, 32, 1))
+    w_dec = torch.from_numpy(np.ascontiguousarray(Wq).view(np.uint8)).view(
+        torch.float8_e4m3fn).to(torch.float64).numpy() * np.ldexp(1.0, np.repeat(np.repeat(
+            np.asarray(Ws).astype(np.int64) - 127, 32, 0), 32, 1))
+    ref = a_dec @ w_dec.T
+    assert np.allclose(r["kv"], ref, rtol=1e-12, atol=1e-300)
+    # and it differs from the unquantised contraction (the rows really were quantised)
+    plain = oracle.forward(W.bits(d["table"]), d["row_offset"], d["rows"],
+                           d["hash_ids"].numpy(), wl.head_dim, Wq, W.bits(d["hidden"]),
+                           W.bits(d["q_weight"]), W.bits(d["k_weight"]),
+                           W.bits(d["token_mask"]), Ws=Ws)
+    assert not np.array_equal(plain["kv"], r["kv"])
+
+
 def test_mx_quantize_scale_is_minimal_and_codes_match_torch():
     rng = np.random.default_rng(5)
     x = rng.standard_normal((4, 128)) * np.array([1e-3, 0.02, 3.0, 700.0])[:, None]
