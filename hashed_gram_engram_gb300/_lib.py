@@ -50,6 +50,7 @@ EXPORTED = (
     "engram_debug_keep_value",
     "engram_prefetch_create", "engram_prefetch_destroy", "engram_prefetch_start",
     "engram_prefetch_forward", "engram_prefetch_join", "engram_prefetch_pending",
+    "engram_debug_barrier_skew",
 )
 
 
@@ -115,6 +116,7 @@ def load(path: str | None = None):
             "engram_gate_noalloc": [vp, vp, vp, i64, vp, vp, vp, vp, vp, i64, i64, i64,
                                     ctypes.c_double, ctypes.c_double, vp],
             "engram_prefetch_create": [vp, i32, vp],
+            "engram_debug_barrier_skew": [vp, i64],
             "engram_prefetch_destroy": [vp],
             "engram_prefetch_start": [vp, vp, vp, i64, ctypes.c_int, vp],
             "engram_prefetch_forward": [vp, i32, vp, vp, vp, i64, vp, vp, vp, i64, vp],
@@ -300,3 +302,7 @@ def engram_prefetch_pending(p, layer) -> bool:
     if rc < 0:
         _check(rc, "engram_prefetch_pending")
     return rc == 1
+
+
+def engram_debug_barrier_skew(h, delta):
+    return _check(load().engram_debug_barrier_skew(h, int(delta)), "engram_debug_barrier_skew")

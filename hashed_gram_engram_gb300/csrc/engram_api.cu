@@ -119,14 +119,21 @@ int64_t span_bytes(const int64_t* s, int64_t T, int64_t H, int64_t D) {
     return ((T - 1) * s[0] + (H - 1) * s[1] + (D - 1) * s[2] + 1) * 2;
 }
 
-int check_view(const void* p, const int64_t* s, int64_t H, int64_t D) {
+int check_view(const void* p, const int64_t* s) {
     if (p == nullptr || s == nullptr) return ENGRAM_ERR_INVALID_ARG;
     if (s[0] < 0 || s[1] < 0 || s[2] != 1) return s[2] != 1 && s[2] > 0 ? ENGRAM_ERR_UNSUPPORTED
                                                                         : ENGRAM_ERR_INVALID_ARG;
     if (!aligned16(p) || (s[0] % 8) != 0 || (s[1] % 8) != 0) return ENGRAM_ERR_UNSUPPORTED;
-    (void)H;
-    (void)D;
     return ENGRAM_OK;
+}
+
+// An output view's T*H rows of D elements must be disjoint (nested
+// copy-inside-token or token-inside-copy): rows that overlap would be
+// written by several threads at once.
+bool rows_disjoint(const int64_t* s, int64_t T, int64_t H, int64_t D) {
+    if (H == 1) return T == 1 || s[0] >= D;
+    if (T == 1) return s[1] >= D;
+    return (s[1] >= D && s[0] >= H * s[1]) || (s[0] >= D && s[1] >= T * s[0]);
 }
 
 }  // namespace
@@ -278,7 +285,7 @@ int engram_create(const engram_config* cfg, const engram_weights* w, engram_t** 
                     true));
     }
     step(dalloc(&ws.fvalue, ws.kv_tpitch * c.dim * sizeof(float), true));
-    step(dalloc(&ws.grid_bar, 8 * sizeof(unsigned), true));
+    step(dalloc(&ws.grid_bar, kFusedCounters * sizeof(unsigned long long), true));
     step(dalloc(&ws.qk, c.hc_mult * c.dim * sizeof(float), false));
     step(dalloc(&ws.err, sizeof(unsigned), true));
     if (e == cudaSuccess)
@@ -349,16 +356,22 @@ int engram_forward(engram_t* h, const void* hidden, const int64_t hidden_strides
     if (T > h->cfg.max_tokens) return set_err(h, ENGRAM_ERR_T_EXCEEDS_MAX);
     if (T == 0) return set_err(h, ENGRAM_OK);
     const int64_t H = h->cfg.hc_mult, D = h->cfg.dim;
-    int rc = check_view(hidden, hidden_strides, H, D);
+    int rc = check_view(hidden, hidden_strides);
     if (rc != ENGRAM_OK) return set_err(h, rc);
-    rc = check_view(out, out_strides, H, D);
+    rc = check_view(out, out_strides);
     if (rc != ENGRAM_OK) return set_err(h, rc);
+    if (!rows_disjoint(out_strides, T, H, D)) return set_err(h, ENGRAM_ERR_INVALID_ARG);
     const bool same = hidden == out && hidden_strides[0] == out_strides[0] &&
                       hidden_strides[1] == out_strides[1];
-    if (!same && ranges_overlap(hidden, span_bytes(hidden_strides, T, H, D), out,
-                                span_bytes(out_strides, T, H, D)))
+    const int64_t ob = span_bytes(out_strides, T, H, D);
+    if (!same && ranges_overlap(hidden, span_bytes(hidden_strides, T, H, D), out, ob))
         return set_err(h, ENGRAM_ERR_INVALID_ARG);
     if (hash_ids != nullptr && ids_row_stride < h->C) return set_err(h, ENGRAM_ERR_INVALID_ARG);
+    // the ids and the mask are read while out is written: no overlap
+    if ((hash_ids != nullptr &&
+         ranges_overlap(out, ob, hash_ids, ((T - 1) * ids_row_stride + h->C) * 4)) ||
+        (token_mask != nullptr && ranges_overlap(out, ob, token_mask, T)))
+        return set_err(h, ENGRAM_ERR_INVALID_ARG);
     if (hash_ids == nullptr && h->staged_T != T) return set_err(h, ENGRAM_ERR_INVALID_ARG);
 
     DeviceGuard guard(h->cfg.device);
@@ -406,6 +419,19 @@ int engram_forward(engram_t* h, const void* hidden, const int64_t hidden_strides
         h->last_path = 2;
     }
     mark(3);
+    return cuda_err(h, e);
+}
+
+int engram_debug_barrier_skew(engram_t* h, int64_t delta) {
+    if (h == nullptr || delta < 0) return ENGRAM_ERR_INVALID_ARG;
+    DeviceGuard guard(h->cfg.device);
+    if (!guard.ok) return ENGRAM_ERR_CUDA;
+    // the fused kernel's launch counter (the first of its four 64-bit counters)
+    unsigned long long ctr = 0;
+    cudaError_t e = cudaDeviceSynchronize();
+    if (e == cudaSuccess) e = cudaMemcpy(&ctr, h->ws.grid_bar, sizeof(ctr), cudaMemcpyDeviceToHost);
+    ctr += static_cast<unsigned long long>(delta);
+    if (e == cudaSuccess) e = cudaMemcpy(h->ws.grid_bar, &ctr, sizeof(ctr), cudaMemcpyHostToDevice);
     return cuda_err(h, e);
 }
 
@@ -494,7 +520,7 @@ int engram_device_error(engram_t* h, uint32_t* bits, int clear) {
     if (e == cudaSuccess && (*bits & ENGRAM_DEVERR_TIMEOUT)) {
         // an unwound launch can leave the grid barrier's arrival count
         // short: start it again from zero
-        e = cudaMemset(h->ws.grid_bar, 0, 8 * sizeof(unsigned));
+        e = cudaMemset(h->ws.grid_bar, 0, kFusedCounters * sizeof(unsigned long long));
     }
     if (e != cudaSuccess) return ENGRAM_ERR_CUDA;
     return ENGRAM_OK;

@@ -35,6 +35,7 @@
 // device address is looked up once per device, on the first call there (a
 // T = 0 call does only this), which may also load the library's device code
 // onto that device: make that first call before capturing a stream.
+#include <cstdint>
 #include <mutex>
 
 #include "internal.h"
@@ -168,25 +169,75 @@ cudaError_t launch_noalloc(const NoallocArgs& a, cudaStream_t s) {
     return cudaGetLastError();
 }
 
-// Device address of g_partials, per device, resolved on first use.
+// Device address of g_partials: looked up on the first call on a device and
+// again whenever the context current on that device changes (after a
+// cudaDeviceReset the primary context is a new one, and a caller may make a
+// context of its own current), so a stale address is never passed to a
+// kernel.  Contexts are told apart by their driver-assigned unique id; if
+// the driver cannot report one, the address is looked up on every call.
+typedef CUresult (*CtxGetCurrentFn)(CUcontext*);
+typedef CUresult (*CtxGetIdFn)(CUcontext, unsigned long long*);
+
+template <class Fn>
+Fn driver_fn(const char* name) {
+    void* p = nullptr;
+    cudaDriverEntryPointQueryResult q;
+    if (cudaGetDriverEntryPointByVersion(name, &p, 12000, cudaEnableDefault, &q) == cudaSuccess &&
+        q == cudaDriverEntryPointSuccess)
+        return reinterpret_cast<Fn>(p);
+    return nullptr;
+}
+
+bool current_context_id(unsigned long long* id) {
+    static const CtxGetCurrentFn get_current = driver_fn<CtxGetCurrentFn>("cuCtxGetCurrent");
+    static const CtxGetIdFn get_id = driver_fn<CtxGetIdFn>("cuCtxGetId");
+    if (get_current == nullptr || get_id == nullptr) return false;
+    CUcontext ctx = nullptr;
+    if (get_current(&ctx) != CUDA_SUCCESS || ctx == nullptr) return false;
+    return get_id(ctx, id) == CUDA_SUCCESS;
+}
+
+struct ScratchEntry {
+    unsigned long long ctx_id;
+    void* addr;
+};
 std::mutex g_scratch_mu;
-void* g_scratch_addr[kMaxDevices] = {};
+ScratchEntry g_scratch[kMaxDevices] = {};
 
 cudaError_t scratch_address(int dev, void** out) {
     std::lock_guard<std::mutex> lock(g_scratch_mu);
-    if (g_scratch_addr[dev] == nullptr) {
+    unsigned long long id = 0;
+    const bool known = current_context_id(&id);
+    if (!known || g_scratch[dev].addr == nullptr || g_scratch[dev].ctx_id != id) {
         void* p = nullptr;
         const cudaError_t e = cudaGetSymbolAddress(&p, g_partials);
         if (e != cudaSuccess) return e;
-        g_scratch_addr[dev] = p;
+        // (the lookup initialises the device's primary context if it was not yet)
+        if (current_context_id(&id)) {
+            g_scratch[dev].ctx_id = id;
+            g_scratch[dev].addr = p;
+        } else {
+            g_scratch[dev].addr = nullptr;  // no id to key on: look up every call
+        }
+        *out = p;
+        return cudaSuccess;
     }
-    *out = g_scratch_addr[dev];
+    *out = g_scratch[dev].addr;
     return cudaSuccess;
 }
 
 bool bad_view(const void* p, const int64_t* st) {
     return p == nullptr || st == nullptr || st[0] < 0 || st[1] < 0 || st[2] != 1 ||
            (reinterpret_cast<uintptr_t>(p) & 15u) != 0 || st[0] % 8 != 0 || st[1] % 8 != 0;
+}
+
+// A [T, H, D] view (unit dim stride) whose T*H rows of D elements are
+// disjoint: rows nested copy-inside-token or token-inside-copy.  An output
+// whose rows overlap would be written by several threads at once.
+bool rows_disjoint(const int64_t* st, int64_t T, int64_t H, int64_t D) {
+    if (H == 1) return T == 1 || st[0] >= D;
+    if (T == 1) return st[1] >= D;
+    return (st[1] >= D && st[0] >= H * st[1]) || (st[0] >= D && st[1] >= T * st[0]);
 }
 
 // Bytes spanned by a [T, H, D] bf16 view (non-negative strides, d stride 1).
@@ -218,13 +269,16 @@ extern "C" int engram_gate_noalloc(const void* hidden, const int64_t hidden_stri
                                         reinterpret_cast<uintptr_t>(q_weight) |
                                         reinterpret_cast<uintptr_t>(k_weight)) & 15u) != 0)
             return ENGRAM_ERR_INVALID_ARG;
-        // out may be hidden itself (same strides); no other overlap with
-        // hidden or kv
+        // out's rows must not overlap each other; out may be hidden itself
+        // (same strides) but overlap no other input
         const int64_t ob = span(out_strides, T, H, D);
         const bool in_place = out == hidden && out_strides[0] == hidden_strides[0] &&
                               out_strides[1] == hidden_strides[1];
-        if ((!in_place && overlap(out, ob, hidden, span(hidden_strides, T, H, D))) ||
-            overlap(out, ob, kv, ((T - 1) * kv_row_stride + (H + 1) * D) * 2))
+        if (!rows_disjoint(out_strides, T, H, D) ||
+            (!in_place && overlap(out, ob, hidden, span(hidden_strides, T, H, D))) ||
+            overlap(out, ob, kv, ((T - 1) * kv_row_stride + (H + 1) * D) * 2) ||
+            overlap(out, ob, q_weight, H * D * 2) || overlap(out, ob, k_weight, H * D * 2) ||
+            (token_mask != nullptr && overlap(out, ob, token_mask, T)))
             return ENGRAM_ERR_INVALID_ARG;
         if (T > kNoallocMaxPartials || T * H * (D / kSlice) > kNoallocMaxPartials)
             return ENGRAM_ERR_SCRATCH_LIMIT;

@@ -140,7 +140,9 @@ int engram_lookup(engram_t* h, const int32_t* hash_ids, int64_t ids_row_stride, 
  *   hidden, out: device bf16 [T, H, D]; strides in ELEMENTS {t, h, d}; the d
  *       stride must be 1 and the t and h strides multiples of 8 (16-byte rows).
  *       out may be the same buffer as hidden with the same strides (in place);
- *       any other overlap is INVALID_ARG.
+ *       any other overlap with hidden, and any overlap of out with hash_ids
+ *       or token_mask, is INVALID_ARG; so is an out whose T*H rows overlap
+ *       each other (rows must nest copy-inside-token or token-inside-copy).
  *   hash_ids: as for engram_lookup, or NULL to use the rows staged by the
  *       last engram_lookup (which must have had the same T).
  *   token_mask: device bytes [T] (0 = False), or NULL for no mask.
@@ -219,8 +221,10 @@ int engram_debug_staged_rows(engram_t* h, void* rows, int64_t T, cudaStream_t st
  * Arithmetic: as engram_forward, split into partial sums per 256-dim slice
  * that are added in slice order (the partials/finish split of the gate in
  * "vllm.models.deepseek_v41.amd.engram", slices in place of ranks).
- *   hidden, out: device bf16 [T, H, D], strides as for engram_forward
- *       (in place allowed, any other overlap with hidden or kv is INVALID_ARG).
+ *   hidden, out: device bf16 [T, H, D], strides as for engram_forward;
+ *       out's rows must not overlap each other, out may be hidden itself
+ *       (same pointer and strides), and any other overlap of out with
+ *       hidden, kv, q_weight, k_weight or token_mask is INVALID_ARG.
  *   kv: device bf16 [T, (H+1)*D] with row stride kv_row_stride >= (H+1)*D
  *       elements (a multiple of 8): keys of copy h in columns [h*D, (h+1)*D),
  *       the shared value in [H*D, (H+1)*D).
@@ -235,7 +239,11 @@ int engram_debug_staged_rows(engram_t* h, void* rows, int64_t T, cudaStream_t st
  * time (unordered streams, concurrent host threads) corrupt each other's
  * results, so order them.  The first call on each device (T = 0 does only
  * this) looks up the array's address and may load the library's device code
- * there; make it before capturing a stream.  Uses the current device. */
+ * there; make it before capturing a stream.  The address is kept per device
+ * together with the id of the context that was current, and looked up again
+ * when another context is current there (after cudaDeviceReset, or a
+ * caller's own driver-API context): make a T = 0 call after such a change,
+ * before any capture.  Uses the current device. */
 #define ENGRAM_NOALLOC_MAX_PARTIALS 131072
 int engram_gate_noalloc(const void* hidden, const int64_t hidden_strides[3], const void* kv,
                         int64_t kv_row_stride, const void* q_weight, const void* k_weight,
@@ -258,6 +266,15 @@ int engram_debug_staged_mx(engram_t* h, uint8_t* codes, uint8_t* scales, int64_t
  * ms[0..2] (0 for a kernel that did not run). */
 int engram_profile_enable(engram_t* h, int enable);
 int engram_profile_read(engram_t* h, float ms[3]);
+
+/* Test hook for failure detection: adds delta (>= 0) to the fused decode
+ * kernel's launch counter.  With delta > 0 the next fused launch waits at
+ * its grid barriers for arrivals that never come.  Each bounded wait runs out
+ * (1 s); the launch sets ENGRAM_DEVERR_TIMEOUT, lets its copies and MMAs
+ * land, frees TMEM and returns without writing out.  engram_device_error
+ * then reports the bit and resets the counters, and the next launch runs
+ * normally.  Synchronous.  Nothing faults, traps or hangs. */
+int engram_debug_barrier_skew(engram_t* h, int64_t delta);
 
 /* ------------------------------------------------------------------------
  * Lookups of several layers run ahead on a side stream.  This follows the

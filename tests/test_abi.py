@@ -90,6 +90,7 @@ def test_prefetch_arguments_are_rejected_without_a_gpu(lib):
     assert lib.engram_prefetch_join(None, None) == -1
     assert lib.engram_prefetch_pending(None, 0) == -1
     assert lib.engram_prefetch_destroy(None) == 0
+    assert lib.engram_debug_barrier_skew(None, 1) == -1
 
 
 def test_product_package_never_reaches_the_oracle():

@@ -79,3 +79,25 @@ def test_scratch_limit(lib):
     one = dict(H=1, D=256, hs=strides(256, 256), os=strides(256, 256), kv_stride=512)
     assert call(lib, T=131073, **one) == SCRATCH
     assert call(lib, T=131072, **one) == CUDA_ERR
+
+
+def test_output_rows_must_be_disjoint(lib):
+    # rows of out that overlap each other would be written by several threads
+    assert call(lib, os=strides(H * D, 0)) == INVALID
+    assert call(lib, os=strides(D, D)) == INVALID
+    assert call(lib, os=strides(0, D)) == INVALID
+    # in place on a hidden broadcast over the copies: rejected for the same reason
+    assert call(lib, hs=strides(H * D, 0), out=HID, os=strides(H * D, 0)) == INVALID
+    # copy-major rows (a transposed view) are disjoint
+    assert call(lib, os=strides(D, T * D)) == CUDA_ERR
+    # one token or one copy: only the other stride matters
+    assert call(lib, T=1, os=strides(0, D)) == CUDA_ERR
+    assert call(lib, H=1, os=strides(D, 0), hs=strides(D, 0), kv_stride=2 * D) == CUDA_ERR
+
+
+def test_output_must_not_alias_q_k_or_mask(lib):
+    assert call(lib, out=Q) == INVALID
+    assert call(lib, out=K - 16) == INVALID
+    assert call(lib, mask=OUT + 64) == INVALID
+    span = ((T - 1) * H * D + (H - 1) * D + D) * 2
+    assert call(lib, mask=OUT + span) == CUDA_ERR
