@@ -6,12 +6,50 @@ import numpy as np
 import torch
 
 import oracle
+import oracle_pool
 import workloads as W
 from hashed_gram_engram_gb300 import Engram
 
 
 def np_bf16(bits):
     return (np.asarray(bits, np.uint32) << 16).view(np.float32).astype(np.float64)
+
+
+def oracle_all(case, inp, quantize_act=False, workers=None):
+    """Oracle outputs for every token of a large step: the gather in this
+    process, then wkv and the gate over token chunks in spawned worker
+    processes, one single-threaded oracle each (the host's cores in
+    parallel).  Returns rows, out_f64, out_bf16, gate and value (the last D
+    kv columns; the keys are not kept)."""
+    import concurrent.futures as cf
+    import multiprocessing as mp
+    import os
+    import tempfile
+    hs = case.host()
+    wl = case.wl
+    ids = inp["hash_ids"].cpu().numpy()
+    if hs["table_scale"] is None:
+        rows, nbad = oracle.gather(hs["table"], case.row_offset, case.rows, ids, wl.head_dim)
+    else:
+        rows, nbad = oracle.gather_e4m3(hs["table"], hs["table_scale"], case.row_offset,
+                                        case.rows, ids, wl.head_dim)
+    hidden = W.bits(inp["hidden"])
+    mask = None if inp["token_mask"] is None else W.bits(inp["token_mask"])
+    T = hidden.shape[0]
+    workers = workers or max(1, min(32, os.cpu_count() or 1))
+    bounds = np.linspace(0, T, workers * 2 + 1).astype(int)
+    with tempfile.TemporaryDirectory() as d:
+        w_path = os.path.join(d, "w.npy")
+        np.save(w_path, hs["wkv"])
+        jobs = [(rows[a:b], w_path, hs["wkv_scale"], hidden[a:b], hs["q"], hs["k"],
+                 None if mask is None else mask[a:b], wl.eps, wl.clamp, quantize_act,
+                 wl.hc_mult, wl.dim) for a, b in zip(bounds[:-1], bounds[1:]) if b > a]
+        with cf.ProcessPoolExecutor(max_workers=workers,
+                                    mp_context=mp.get_context("spawn")) as ex:
+            parts = list(ex.map(oracle_pool.oracle_chunk, jobs))
+    ref = {k: np.concatenate([p[k] for p in parts]) for k in parts[0]}
+    ref.update(rows=rows, n_bad=nbad)
+    return ref
 
 
 class Case:
@@ -93,7 +131,7 @@ def compare(case: Case, inp, out, ref, tokens=None, gate=None, value=None, tol=N
     assert err <= tol, f"max abs err {err} > {tol}"
     # rounding-level agreement: the only differences left are the fp32
     # projection, the bf16 value of the token-as-M path and the final RTNE
-    value_ref = ref["kv"][:, wl.hc_mult * wl.dim:]
+    value_ref = ref["value"] if "value" in ref else ref["kv"][:, wl.hc_mult * wl.dim:]
     bound = 2.0 ** -8 * np.abs(exp) + 2.0 ** -8 * np.abs(value_ref)[:, None, :] + 1e-5
     if rounding:
         assert np.all(np.abs(got - exp) <= bound), "output differs beyond rounding level"

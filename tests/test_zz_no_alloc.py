@@ -2,9 +2,10 @@
 the caller computed, with its cross-CTA partial sums in a fixed device
 array instead of allocated memory.
 
-Its output is checked against engram_forward (the handle's own path) on the
-same inputs, for two calls in a row with different inputs and sizes, so a
-call that read another call's leftover partials would fail.  The file sorts
+Its output is checked against the oracle's gate and residual on the same
+bf16 kv, and against engram_forward (the handle's own path) on the same
+inputs, for two calls in a row with different inputs and sizes, so a call
+that read another call's leftover partials would fail.  The file sorts
 after the single-layer parity files, so it also runs once those have used
 the device; it builds its own layers and passes alone as well."""
 import numpy as np
@@ -107,6 +108,34 @@ def test_two_calls_match_engram_forward():
         again = _noalloc(case, inp, kv)
         torch.cuda.synchronize()
         assert torch.equal(again, out)
+        case.layer.close()
+
+
+@pytest.mark.gpu
+def test_matches_oracle_gate_on_the_same_kv():
+    """Against the oracle's gate and residual (fp64) on the very bf16 kv the
+    entry point is given, widened exactly: the only differences left are the
+    kernel's fp32 sums and the final bf16 rounding of each output."""
+    import oracle
+    for wl, T in ((W.DECODE, 64), (W.TINY, 333)):
+        case = Case(wl, max_tokens=T)
+        inp = case.step_inputs(T=T, step=300)
+        case.layer.lookup(inp["hash_ids"])
+        kv = _kv(case, T)
+        out = _noalloc(case, inp, kv)
+        torch.cuda.synchronize()
+        mask = None if inp["token_mask"] is None else W.bits(inp["token_mask"])
+        ref = oracle.gate(W.bits(inp["hidden"]), np_bf16(W.bits(kv)), W.bits(case.q),
+                          W.bits(case.k), mask, wl.eps, wl.clamp)
+        got = np_bf16(W.bits(out))
+        exp = ref["out_f64"]
+        v = np_bf16(W.bits(kv[:, wl.hc_mult * wl.dim:]))[:, None, :]
+        bound = 2.0 ** -8 * np.abs(exp) + 1e-5 * np.abs(v) + 1e-6
+        assert np.all(np.abs(got - exp) <= bound), f"max diff {np.abs(got - exp).max()}"
+        assert np.abs(got - exp).max() <= wl.tol
+        if mask is not None:
+            m = mask.astype(bool)
+            assert np.array_equal(W.bits(out)[~m], W.bits(inp["hidden"])[~m])
         case.layer.close()
 
 
