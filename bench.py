@@ -43,7 +43,7 @@ L2_FLUSH_BYTES = 512 << 20
 def parse():
     p = argparse.ArgumentParser()
     p.add_argument("--gpus", type=int, default=1)
-    p.add_argument("--steps", type=int, default=2000)
+    p.add_argument("--steps", type=int, default=200)
     p.add_argument("--warmup", type=int, default=20)
     p.add_argument("--impl", default="ours", choices=["ours", "reference"])
     p.add_argument("--no-prefill", action="store_true")
@@ -294,35 +294,132 @@ def row_bytes(wl):
     return wl.T * wl.K * 2
 
 
-def time_rotation(torch, layers, stream, steps, warmup):
-    """Forwards rotating over the layers, captured in one CUDA graph and
-    replayed; returns (ms per step, steps timed, steps per graph, replays)."""
+def time_rotation(torch, layers, stream, steps, warmup, min_ms=20.0, min_samples=5):
+    """Forwards rotating over the layers: `warmup` untimed steps, then a CUDA
+    graph of exactly `steps` forwards, replayed until at least `min_ms` of
+    replays and `min_samples` replays were timed, each replay bracketed by
+    its own events on the launch stream.  Returns (median ms per step over
+    the replays, steps per timed sample, the per-replay ms per step)."""
     def step(L):
         L["layer"].forward(L["hidden"], L["ids"], L.get("mask"), out=L["out"], stream=stream)
 
     NL = len(layers)
-    for _ in range(max(3, warmup)):
-        for L in layers:
-            step(L)
+    for i in range(max(3, warmup)):
+        step(layers[i % NL])
     torch.cuda.synchronize()
-    per_graph = NL * max(1, 24 // NL)
     graph = torch.cuda.CUDAGraph()
     with torch.cuda.graph(graph, stream=stream):
-        for i in range(per_graph):
+        for i in range(steps):
             step(layers[i % NL])
-    for _ in range(3):
-        graph.replay()
+    graph.replay()  # the first replay uploads the graph: untimed
     torch.cuda.synchronize()
-    replays = max(1, steps // per_graph)
-    e0 = torch.cuda.Event(enable_timing=True)
-    e1 = torch.cuda.Event(enable_timing=True)
-    e0.record(stream)
-    for _ in range(replays):
+    samples = []
+    total = 0.0
+    while len(samples) < min_samples or total < min_ms:
+        torch.cuda.synchronize()
+        e0 = torch.cuda.Event(enable_timing=True)
+        e1 = torch.cuda.Event(enable_timing=True)
+        e0.record(stream)
         graph.replay()
-    e1.record(stream)
+        e1.record(stream)
+        torch.cuda.synchronize()
+        ms = e0.elapsed_time(e1)
+        total += ms
+        samples.append(ms / steps)
+        if len(samples) >= 10000:
+            break
+    del graph
+    return statistics.median(samples), steps, samples
+
+
+def time_prefetch_rotation(torch, EngramPrefetch, layers, stream, steps, warmup, min_ms=20.0,
+                           min_samples=5):
+    """The same forwards with every layer's lookup staged ahead on a side
+    stream (class EngramPrefetch's start / forward / join): per group of
+    the rotated layers, start() issues all their lookups (background grid)
+    at once and each forward waits only for its own layer's rows, so a
+    lookup runs beside the previous layers' forwards.  Captured in one CUDA
+    graph of ceil(steps / layers) groups.  Returns (median ms per step,
+    steps per sample, per-replay ms per step)."""
+    NL = len(layers)
+    pf = EngramPrefetch([L["layer"] for L in layers])
+    groups = max(1, (steps + NL - 1) // NL)
+    n = groups * NL
+
+    def group():
+        pf.start([L["ids"] for L in layers], background=True, stream=stream)
+        for i, L in enumerate(layers):
+            pf.forward(i, L["hidden"], None, L.get("mask"), out=L["out"], stream=stream)
+        pf.join(stream=stream)
+
+    for _ in range(max(3, warmup)):
+        group()
     torch.cuda.synchronize()
-    n = replays * per_graph
-    return e0.elapsed_time(e1) / n, n, per_graph, replays
+    graph = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(graph, stream=stream):
+        for _ in range(groups):
+            group()
+    graph.replay()
+    torch.cuda.synchronize()
+    samples, total = [], 0.0
+    while len(samples) < min_samples or total < min_ms:
+        e0 = torch.cuda.Event(enable_timing=True)
+        e1 = torch.cuda.Event(enable_timing=True)
+        e0.record(stream)
+        graph.replay()
+        e1.record(stream)
+        torch.cuda.synchronize()
+        ms = e0.elapsed_time(e1)
+        total += ms
+        samples.append(ms / n)
+        if len(samples) >= 10000:
+            break
+    del graph
+    pf.close()
+    return statistics.median(samples), n, samples
+
+
+def fp8_peak_tflops(torch, dev):
+    """Dense fp8 tensor throughput of this GPU from library GEMMs (cuBLAS via
+    torch._scaled_mm at 8192^3, best of 10 with CUDA events): e4m3 operands
+    with per-tensor scales, and with E8M0 scales per 32 elements (the MXFP8
+    form the prefill GEMM uses).  Returns {kind: TFLOP/s} for the forms this
+    torch build supports."""
+    M = N = K = 8192
+    out = {}
+    a = torch.randn(M, K, device=dev).to(torch.float8_e4m3fn)
+    b = torch.randn(N, K, device=dev).to(torch.float8_e4m3fn)
+
+    def best(fn):
+        for _ in range(3):
+            fn()
+        torch.cuda.synchronize()
+        t = []
+        for _ in range(10):
+            e0 = torch.cuda.Event(enable_timing=True)
+            e1 = torch.cuda.Event(enable_timing=True)
+            e0.record()
+            fn()
+            e1.record()
+            torch.cuda.synchronize()
+            t.append(e0.elapsed_time(e1))
+        return 2.0 * M * N * K / (min(t) * 1e-3) / 1e12
+
+    one = torch.ones((), device=dev, dtype=torch.float32)
+    try:
+        out["e4m3_per_tensor"] = best(
+            lambda: torch._scaled_mm(a, b.t(), one, one, out_dtype=torch.bfloat16))
+    except Exception as e:  # noqa: BLE001 - reported, not fatal
+        out["e4m3_per_tensor_error"] = str(e).splitlines()[0][:160]
+    try:
+        e8 = torch.float8_e8m0fnu
+        sa = torch.full((M * K // 32,), 127, dtype=torch.uint8, device=dev).view(e8)
+        sb = torch.full((N * K // 32,), 127, dtype=torch.uint8, device=dev).view(e8)
+        out["mxfp8_block32"] = best(
+            lambda: torch._scaled_mm(a, b.t(), sa, sb, out_dtype=torch.bfloat16))
+    except Exception as e:  # noqa: BLE001
+        out["mxfp8_block32_error"] = str(e).splitlines()[0][:160]
+    return out
 
 
 def run_case(args):
@@ -363,7 +460,8 @@ def main():
 
     import __graft_entry__ as g
     import workloads as W
-    from hashed_gram_engram_gb300 import Engram, engram_profile_enable, engram_profile_read
+    from hashed_gram_engram_gb300 import (Engram, EngramPrefetch, engram_profile_enable,
+                                          engram_profile_read)
 
     rank, local, world = dist_env()
     if world > 1:
@@ -376,7 +474,6 @@ def main():
         dist.barrier()
     g.build()
     hbm_peak, bf16_peak, peak_kind = peaks()
-    fp8_peak = 2.0 * bf16_peak  # dense fp8 : bf16 = 4.5 : 2.25 nominal
     stream = torch.cuda.Stream(dev)
     torch.cuda.set_stream(stream)
 
@@ -408,8 +505,7 @@ def main():
     clocks.start()
     if world > 1:
         dist.barrier()
-    ms_step, steps, per_graph, replays = time_rotation(torch, layers, stream, args.steps,
-                                                       args.warmup)
+    ms_step, steps, samples = time_rotation(torch, layers, stream, args.steps, args.warmup)
     if world > 1:
         dist.barrier()
     clk = clocks.stop()
@@ -472,8 +568,11 @@ def main():
                    "seeds": {"layers": [int(L["wl"].seed) for L in layers],
                              "generator": "torch.Generator.manual_seed per tensor kind"},
                    "l2": f"inputs larger than L2: {NL} layers' weights ({NL * 40} MiB) rotated",
-                   "timing": f"CUDA graph of {per_graph} steps replayed {replays}x, events on "
-                             "the launch stream",
+                   "timing": f"CUDA graph of exactly {steps} steps (--steps), replayed "
+                             f"{len(samples)}x, each replay timed by CUDA events on the launch "
+                             f"stream; value from the median replay",
+                   "replay_ms_per_step": {"min": min(samples), "median": ms_step,
+                                          "max": max(samples)},
                    "parallelism": f"replicas x{world} (token-sharded, no collective)"},
         "roofline": {"bound": "hbm",
                      "kernel": "decode_fused_kernel (gather + tcgen05 wkv + gate, one launch)",
@@ -486,10 +585,11 @@ def main():
         "e2e": {"value": world * wl.T / (e2e_ms * 1e-3), "unit": "tokens/s",
                 "h2d_bytes_per_step": int(hid_h.numel() * 2 + ids_h.numel() * 4),
                 "d2h_bytes_per_step": int(out_h.numel() * 2)},
-        "gpu_launches": steps,
+        "gpu_launches": steps * len(samples),
+        "gpu_launches_per_step": 1,
         "clocks": clk,
     }
-    launches = steps
+    launches = steps * len(samples)
 
     def prefill_block(layer, pw, kernel_name, peak, peak_name):
         """Per-step time of a prefill forward and its kernels' event times."""
@@ -554,7 +654,7 @@ def main():
         # T = 4096 prefill step on the first layer
         mw = W.MXFP8_DECODE
         mlayers = rotation_layers(mw, NL, W.MXFP8_PREFILL.T, seed0=50)
-        m_ms, m_steps, _, _ = time_rotation(torch, mlayers, stream, args.steps, args.warmup)
+        m_ms, m_steps, m_samp = time_rotation(torch, mlayers, stream, args.steps, args.warmup)
         m_ms = max_over_ranks(m_ms)
         mb = algorithmic_bytes(mw)
         line["mxfp8_decode"] = {
@@ -567,11 +667,22 @@ def main():
                          "unit": "GB/s", "frac": mb / (m_ms * 1e-3) / 1e9 / hbm_peak,
                          "algorithmic_bytes": mb, "peak_kind": peak_kind},
         }
-        launches += m_steps
+        launches += m_steps * len(m_samp)
         if not args.no_prefill:
+            # the fp8 tensor peak this GPU reaches with library GEMMs: the
+            # MXFP8 (E8M0 per 32) form when the torch build has it, else
+            # per-tensor e4m3, else 2 x the measured bf16 peak (nominal ratio)
+            fp8 = fp8_peak_tflops(torch, dev)
+            if "mxfp8_block32" in fp8:
+                fp8_peak, fp8_kind = fp8["mxfp8_block32"], "measured: cuBLAS MXFP8 GEMM 8192^3"
+            elif "e4m3_per_tensor" in fp8:
+                fp8_peak, fp8_kind = fp8["e4m3_per_tensor"], "measured: cuBLAS e4m3 GEMM 8192^3"
+            else:
+                fp8_peak, fp8_kind = 2.0 * bf16_peak, f"{peak_kind} bf16 x 2 (nominal ratio)"
+            line["fp8_peak_measured"] = fp8
             n, line["mxfp8_prefill"] = prefill_block(
                 mlayers[0]["layer"], W.MXFP8_PREFILL, "wkv_gemm_kernel<mxfp8>", fp8_peak,
-                f"{peak_kind} bf16 x 2 (fp8:bf16 nominal ratio)")
+                fp8_kind)
             launches += n
         for L in mlayers:
             L["layer"].close()
@@ -588,8 +699,13 @@ def main():
                     f"{int(need) >> 30} GiB pinned table, {avail >> 30} GiB host memory free"}, 0
         otable = (W.make_table(ow, "cuda"), W.make_table_scale(ow, "cuda"))
         olayers = rotation_layers(ow, 4, ow.T, table=otable, seed0=seed0)
-        o_ms, o_steps, _, _ = time_rotation(torch, olayers, stream, args.steps, args.warmup)
+        o_ms, o_steps, o_samp = time_rotation(torch, olayers, stream, args.steps, args.warmup)
         o_ms = max_over_ranks(o_ms)
+        # the same rotation with each layer's host-table lookup staged ahead
+        # on a side stream, beside the previous layers' forwards
+        p_ms, p_steps, p_samp = time_prefetch_rotation(torch, EngramPrefetch, olayers, stream,
+                                                       args.steps, args.warmup)
+        p_ms = max_over_ranks(p_ms)
         ob = algorithmic_bytes(ow)
         host_b = row_bytes(ow)
         kind = "e4m3 codes + ue8m0 scales per 32" if fp8 else "bf16"
@@ -604,11 +720,18 @@ def main():
                          "achieved": ob / (o_ms * 1e-3) / 1e9, "peak": hbm_peak,
                          "unit": "GB/s", "frac": ob / (o_ms * 1e-3) / 1e9 / hbm_peak,
                          "algorithmic_bytes": ob, "peak_kind": peak_kind},
+            "prefetched": {
+                "how": "EngramPrefetch: all layers' lookups (background grid) on a side stream "
+                       "at start, each forward waits for its own rows only",
+                "tokens_per_s": world * ow.T / (p_ms * 1e-3), "ms_per_step": p_ms,
+                "steps": p_steps,
+                "host_link_GB_per_s": host_b / (p_ms * 1e-3) / 1e9,
+                "roofline_frac": ob / (p_ms * 1e-3) / 1e9 / hbm_peak},
         }
         for L in olayers:
             L["layer"].close()
         del olayers, otable
-        return res, o_steps
+        return res, o_steps * len(o_samp) + p_steps * len(p_samp) * 2
 
     if not args.no_offload:
         line["offload"], n = offload_line(W.OFFLOAD, 70)
@@ -619,7 +742,7 @@ def main():
         # offload step with e4m3 rows and ue8m0 scales, dequantized by the gather
         ew = W.DECODE_E4M3
         elayers = rotation_layers(ew, NL, ew.T, seed0=90)
-        e_ms, e_steps, _, _ = time_rotation(torch, elayers, stream, args.steps, args.warmup)
+        e_ms, e_steps, e_samp = time_rotation(torch, elayers, stream, args.steps, args.warmup)
         e_ms = max_over_ranks(e_ms)
         eb = algorithmic_bytes(ew)
         line["decode_e4m3_table"] = {
@@ -632,7 +755,7 @@ def main():
                          "unit": "GB/s", "frac": eb / (e_ms * 1e-3) / 1e9 / hbm_peak,
                          "algorithmic_bytes": eb, "peak_kind": peak_kind},
         }
-        launches += e_steps
+        launches += e_steps * len(e_samp)
         for L in elayers:
             L["layer"].close()
         del elayers
@@ -640,7 +763,6 @@ def main():
             line["offload_e4m3_table"], n = offload_line(W.OFFLOAD_E4M3, 110)
             launches += n
 
-    line["gpu_launches"] = steps
     line["gpu_launches_all_timed_regions"] = launches
     if rank == 0:
         print(json.dumps(line), flush=True)

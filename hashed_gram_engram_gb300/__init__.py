@@ -6,7 +6,7 @@ is no CPU or PyTorch fallback: without the built library every call raises.
 
     from hashed_gram_engram_gb300 import Engram
     layer = Engram(dim=4096, hc_mult=4, max_ngram_size=3, n_heads=8, head_dim=64,
-                   max_tokens=64, table=table, rows=rows, wkv=wkv,
+                   max_tokens=64, table=table, rows=rows, row_offset=offsets, wkv=wkv,
                    q_weight=q, k_weight=k)
     out = layer.forward(hidden, hash_ids, token_mask)
 """
@@ -56,7 +56,7 @@ class Engram:
     """
 
     def __init__(self, *, dim, hc_mult, max_ngram_size, n_heads, head_dim, max_tokens,
-                 table, rows, wkv, q_weight, k_weight, row_offset=None, wkv_scale=None,
+                 table, rows, row_offset, wkv, q_weight, k_weight, wkv_scale=None,
                  eps=1e-6, clamp=1e-6, wkv_format=None, table_location=None, device=None,
                  keep_value=False, table_scale=None):
         import torch
@@ -64,8 +64,8 @@ class Engram:
         self.n_hash_cols = (int(max_ngram_size) - 1) * int(n_heads)
         self.max_tokens = int(max_tokens)
         rows = np.ascontiguousarray(np.asarray(rows, dtype=np.int64))
-        if row_offset is None:
-            row_offset = np.concatenate([[0], np.cumsum(rows)[:-1]])
+        # each column's first row in the table, as the caller laid it out
+        # (engram_layout gives the bucket sizes and offsets of EngramLayout)
         row_offset = np.ascontiguousarray(np.asarray(row_offset, dtype=np.int64))
         if wkv_format is None:
             wkv_format = ENGRAM_WKV_MXFP8 if wkv_scale is not None else ENGRAM_WKV_BF16
@@ -80,6 +80,23 @@ class Engram:
                             table_location=int(table_location), device=int(device),
                             table_format=ENGRAM_TABLE_FORMAT_BF16 if table_scale is None
                             else ENGRAM_TABLE_FORMAT_E4M3)
+        # the table's element type must match its declared format: the
+        # kernels index rows by the format's row bytes, so a mismatch would
+        # read past the end of the table
+        n_rows = int(row_offset[-1] + rows[-1]) if len(rows) else 0
+        if table_scale is None:
+            if table.dtype != torch.bfloat16:
+                raise ValueError("a bf16 table is expected (an fp8 table needs table_scale)")
+        elif table.dtype != torch.uint8 or table_scale.dtype != torch.uint8:
+            raise ValueError("an fp8 table is uint8 e4m3 codes with uint8 ue8m0 table_scale")
+        if table.dim() != 2 or table.shape[1] != self.head_dim or table.shape[0] < n_rows or \
+                not table.is_contiguous():
+            raise ValueError(f"table must be contiguous [>= {n_rows}, {self.head_dim}]")
+        if table_scale is not None and (table_scale.dim() != 2 or
+                                        table_scale.shape[0] < n_rows or
+                                        table_scale.shape[1] != self.head_dim // 32 or
+                                        not table_scale.is_contiguous()):
+            raise ValueError(f"table_scale must be contiguous [>= {n_rows}, {self.head_dim // 32}]")
         w = engram_weights(table=table.data_ptr(), row_offset=row_offset.ctypes.data,
                            rows=rows.ctypes.data, wkv=wkv.data_ptr(),
                            wkv_scale=None if wkv_scale is None else wkv_scale.data_ptr(),

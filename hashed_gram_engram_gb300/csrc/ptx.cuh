@@ -125,20 +125,6 @@ __device__ __forceinline__ void tma_load_2d_hint(void* dst, const CUtensorMap* m
         : "memory");
 }
 
-// Four rows of a 2-D tensor (row indices r0..r3, one box wide) into four
-// consecutive box rows of shared memory; rows outside the tensor read as
-// zeros.  The tensor map's box must be one row high.
-__device__ __forceinline__ void tma_gather4(void* dst, const CUtensorMap* map, uint64_t* bar,
-                                            int32_t col, int32_t r0, int32_t r1, int32_t r2,
-                                            int32_t r3) {
-    asm volatile(
-        "cp.async.bulk.tensor.2d.shared::cluster.global.tile::gather4.mbarrier::complete_tx::bytes"
-        " [%0], [%1, {%3, %4, %5, %6, %7}], [%2];" ::"r"(smem_addr(dst)),
-        "l"(reinterpret_cast<uint64_t>(map)), "r"(smem_addr(bar)), "r"(col), "r"(r0), "r"(r1),
-        "r"(r2), "r"(r3)
-        : "memory");
-}
-
 // Contiguous global -> shared copy (both 16-byte aligned, size a multiple
 // of 16), completion as transaction bytes on `bar`.
 __device__ __forceinline__ void bulk_load(void* dst, const void* src, uint32_t bytes,
