@@ -117,17 +117,7 @@ struct FusedArgs {
     float eps, clamp, inv_d, inv_sqrt_d;
     unsigned* err;
     uint32_t x_off, qk_off, bar_off;
-    uint32_t rec_slot;  // bytes of one copy's records in shared memory (0: read them from L2)
 };
-
-// 64-bit counters of the fused kernel (they only grow): the launch counter,
-// grid barrier 1, then per hc copy the arrivals of the CTAs holding its keys
-// and the number of launches whose gates of that copy are published.
-constexpr int kCtrLaunch = 0;
-constexpr int kCtrBar1 = 1;
-constexpr int kCtrArrive = 2;
-constexpr int kCtrGates = kCtrArrive + kMaxCopies;
-static_assert(kCtrGates + kMaxCopies <= kFusedCounters, "counter block too small");
 
 __device__ __forceinline__ int first_granule(int cta, int n, int G) {
     return static_cast<int>(static_cast<int64_t>(cta) * n / G);
@@ -175,13 +165,6 @@ __device__ __forceinline__ void grid_arrive(unsigned long long* ctr) {
     asm volatile("red.release.gpu.global.add.u64 [%0], 1;" ::"l"(ctr) : "memory");
 }
 
-// Arrival that returns the count before it (acquire-release at gpu scope).
-__device__ __forceinline__ unsigned long long arrive_fetch(unsigned long long* ctr) {
-    unsigned long long old;
-    asm volatile("atom.acq_rel.gpu.global.add.u64 %0, [%1], 1;" : "=l"(old) : "l"(ctr) : "memory");
-    return old;
-}
-
 __device__ __forceinline__ bool grid_wait(const unsigned long long* ctr, unsigned long long target) {
     const uint64_t t0 = globaltimer_ns();
     uint32_t spins = 0;
@@ -210,11 +193,9 @@ __global__ void __launch_bounds__(kThreads, 1)
     uint64_t* drain = tfull + 1;
     uint64_t* drain2 = drain + 1;  // the second issuer's in-flight MMAs
     uint64_t* scbar = drain2 + 1;         // MXFP8: every scale word is in TMEM
-    uint64_t* recbar = scbar + 1;         // a copy's records are in shared memory
-    unsigned long long* epoch_s = reinterpret_cast<unsigned long long*>(recbar + 1);
+    unsigned long long* epoch_s = reinterpret_cast<unsigned long long*>(scbar + 1);
     uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(epoch_s + 1);
     int* abort_flag = reinterpret_cast<int*>(tmem_slot + 1);
-    uint32_t* last_s = reinterpret_cast<uint32_t*>(abort_flag + 1);  // copies whose gates this CTA computes
     const volatile int* abort_v = abort_flag;
 
     const int tid = threadIdx.x;
@@ -274,9 +255,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         mbar_init(drain, 1);
         mbar_init(drain2, 1);
         mbar_init(scbar, 128);
-        mbar_init(recbar, 1);
         *abort_flag = 0;
-        *last_s = 0;
         fence_barrier_init();
         tma_prefetch_desc(&tm_x);
         pdl_launch_dependents();
@@ -299,7 +278,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     pdl_wait();
     if (tid == 0) {
         // this launch's epoch: stable until CTA 0 advances it at the end
-        *epoch_s = *reinterpret_cast<volatile unsigned long long*>(a.bar + kCtrLaunch) + 1ull;
+        *epoch_s = *reinterpret_cast<volatile unsigned long long*>(a.bar) + 1ull;
     }
     // (a thread's second item too, so that two id -> row chains overlap when
     // rows cross the host link)
@@ -499,8 +478,8 @@ __global__ void __launch_bounds__(kThreads, 1)
         // grid barrier 1 (the counter advances on every launch, gather or not)
         named_barrier_sync(1, 128);
         if (etid == 0) {
-            grid_arrive(a.bar + kCtrBar1);
-            if (a.gather && !grid_wait(a.bar + kCtrBar1, target)) fail(abort_flag, a.err);
+            grid_arrive(a.bar + 1);
+            if (a.gather && !grid_wait(a.bar + 1, target)) fail(abort_flag, a.err);
         }
         named_barrier_sync(1, 128);  // qk_s complete; grid barrier 1 has passed
         // Token tiles: k-block kb of the first Tn staged rows into stage
@@ -712,103 +691,58 @@ __global__ void __launch_bounds__(kThreads, 1)
                 }
             }
         }
-        // the records are read by another CTA's bulk copy (the async proxy)
-        fence_proxy_async();
+        // every record this CTA owes is written: grid barrier 2 (the release
+        // add of one thread covers the CTA's writes ordered before it by the
+        // named barrier)
+        named_barrier_sync(1, 128);
+        if (etid == 0) {
+            grid_arrive(a.bar + 2);
+            if (!grid_wait(a.bar + 2, target)) fail(abort_flag, a.err);
+        }
     }
 
     __syncwarp();
     tc_fence_before();
     __syncthreads();
     if (!*abort_v) {
-        // Gates.  The CTAs holding keys of copy h count their arrivals on the
-        // copy's counter once their records are written (the __syncthreads
-        // above orders every thread's records before thread 0's release).
-        // The CTA whose arrival completes the count for this launch reduces
-        // copy h's records for every token: a bulk copy brings them into
-        // shared memory (the weight ring is idle now), then one warp per
-        // token adds records l, l + 32, ... in lane l and a shuffle tree
-        // finishes (a fixed order: runs are bit-identical).  It publishes
-        // the gates with a release add on the copy's flag; every CTA waits
-        // for all H flags before the residual.
-        if (tid == 0) {
-            uint32_t last = 0;
-            for (int h = 0; h < a.H; ++h) {
-                if (c < a.cf[h] || c >= a.cf[h] + a.nh[h]) continue;
-                const unsigned long long before = arrive_fetch(a.bar + kCtrArrive + h);
-                if (before + 1ull == *epoch_s * static_cast<unsigned long long>(a.nh[h]))
-                    last |= 1u << h;
+        // Gates: CTA c reduces the rows (token, copy) r = c, c + G, ...; one
+        // warp per row, lane l adding the records of the copy's CTAs l,
+        // l + 32, ..., then a shuffle tree (a fixed order); grid barrier 3.
+        const int HR = a.T * a.H;
+        for (int r = c + warp * G; r < HR; r += kWarps * G) {
+            const int t = r / a.H, h = r - t * a.H;
+            const float4* rr = a.rec + a.rec_base[h] + static_cast<int64_t>(t) * a.nh[h];
+            float s_hh = 0.f, s_kk = 0.f, s_hk = 0.f;
+            for (int j = lane; j < a.nh[h]; j += 32) {
+                const float4 v = __ldcg(rr + j);
+                s_hh += v.x;
+                s_kk += v.y;
+                s_hk += v.z;
             }
-            *last_s = last;
-            if (last != 0 && a.rec_slot != 0) {
-                // (at most two copies: a key run spans at most two)
-                fence_proxy_async();  // the other CTAs' records, acquired above
-                uint32_t bytes = 0;
-                for (int h = 0; h < a.H; ++h)
-                    if ((last >> h) & 1u) bytes += static_cast<uint32_t>(a.T * a.nh[h]) * 16u;
-                mbar_arrive_expect_tx(recbar, bytes);
-                uint32_t off = 0;
-                for (int h = 0; h < a.H; ++h) {
-                    if (!((last >> h) & 1u)) continue;
-                    bulk_load(smem + off, a.rec + a.rec_base[h],
-                              static_cast<uint32_t>(a.T * a.nh[h]) * 16u, recbar);
-                    off += a.rec_slot;
-                }
-                if (!mbar_wait(recbar, 0, nullptr)) fail(abort_flag, a.err);
-            }
-        }
-        __syncthreads();
-        const uint32_t last = *abort_v ? 0u : *last_s;
-        uint32_t off = 0;
-        for (int h = 0; h < a.H; ++h) {
-            if (!((last >> h) & 1u)) continue;
-            const int nh = a.nh[h];
-            const float4* rg = a.rec + a.rec_base[h];  // (records too large for shared memory)
-            const float4* rs = reinterpret_cast<const float4*>(smem + off);
-            off += a.rec_slot;
-            for (int t = warp; t < a.T; t += kWarps) {
-                float s_hh = 0.f, s_kk = 0.f, s_hk = 0.f;
-                for (int j = lane; j < nh; j += 32) {
-                    const float4 v = a.rec_slot != 0 ? rs[t * nh + j]
-                                                     : __ldcg(rg + static_cast<int64_t>(t) * nh + j);
-                    s_hh += v.x;
-                    s_kk += v.y;
-                    s_hk += v.z;
-                }
 #pragma unroll
-                for (int o = 16; o > 0; o >>= 1) {
-                    s_hh += __shfl_xor_sync(0xFFFFFFFFu, s_hh, o);
-                    s_kk += __shfl_xor_sync(0xFFFFFFFFu, s_kk, o);
-                    s_hk += __shfl_xor_sync(0xFFFFFFFFu, s_hk, o);
-                }
-                if (lane == 0) {
-                    const bool active = a.mask == nullptr || a.mask[t] != 0;
-                    const float hr = 1.0f / sqrtf(s_hh * a.inv_d + a.eps);
-                    const float kr = 1.0f / sqrtf(s_kk * a.inv_d + a.eps);
-                    const float dot = s_hk * hr * kr * a.inv_sqrt_d;
-                    float gi = sqrtf(fmaxf(fabsf(dot), a.clamp));
-                    if (dot < 0.0f) gi = -gi;
-                    a.gate_out[t * a.H + h] = active ? 1.0f / (1.0f + expf(-gi)) : 0.0f;
-                }
+            for (int o = 16; o > 0; o >>= 1) {
+                s_hh += __shfl_xor_sync(0xFFFFFFFFu, s_hh, o);
+                s_kk += __shfl_xor_sync(0xFFFFFFFFu, s_kk, o);
+                s_hk += __shfl_xor_sync(0xFFFFFFFFu, s_hk, o);
+            }
+            if (lane == 0) {
+                const bool active = a.mask == nullptr || a.mask[t] != 0;
+                const float hr = 1.0f / sqrtf(s_hh * a.inv_d + a.eps);
+                const float kr = 1.0f / sqrtf(s_kk * a.inv_d + a.eps);
+                const float dot = s_hk * hr * kr * a.inv_sqrt_d;
+                float gi = sqrtf(fmaxf(fabsf(dot), a.clamp));
+                if (dot < 0.0f) gi = -gi;
+                a.gate_out[r] = active ? 1.0f / (1.0f + expf(-gi)) : 0.0f;
             }
         }
         __syncthreads();
-        if (tid == 0 && !*abort_v) {
-            if (last != 0) {
-                __threadfence();  // the gates, ordered before by __syncthreads
-                for (int h = 0; h < a.H; ++h)
-                    if ((last >> h) & 1u) grid_arrive(a.bar + kCtrGates + h);
-            }
-            for (int h = 0; h < a.H; ++h)
-                if (!grid_wait(a.bar + kCtrGates + h, *epoch_s)) {
-                    fail(abort_flag, a.err);
-                    break;
-                }
+        if (tid == 0) {
+            grid_arrive(a.bar + 3);
+            if (!grid_wait(a.bar + 3, target)) fail(abort_flag, a.err);
         }
         __syncthreads();
     }
     if (*abort_v) {
-        // (a bulk copy of records may still be landing in shared memory)
-        if (tid == 0 && *last_s != 0 && a.rec_slot != 0) mbar_wait(recbar, 0, nullptr);
         // let in-flight copies and MMAs land before shared memory and TMEM go
         if (tid == 0) {
             for (int j = w_issued > a.w_stages ? w_issued - a.w_stages : 0; j < w_issued; ++j)
@@ -899,15 +833,8 @@ __global__ void __launch_bounds__(kThreads, 1)
             }
         }
     }
-    // Advance the launch counter once every CTA has read this launch's epoch:
-    // each reads it before its grid barrier 1 arrival, so CTA 0 waits for
-    // all G arrivals there (long since complete in the normal case).
-    if (c == 0 && tid == 0) {
-        if (grid_wait(a.bar + kCtrBar1, target))
-            atomicAdd(a.bar + kCtrLaunch, 1ull);
-        else
-            fail(abort_flag, a.err);
-    }
+    // every CTA has read this launch's epoch (it passed barrier 3): advance it
+    if (c == 0 && tid == 0) atomicAdd(a.bar, 1ull);
     tc_fence_before();
     __syncthreads();
     tc_fence_after();
@@ -1013,18 +940,11 @@ FusedSmem fused_smem(const FusedLayout& L, const FusedPlan& p, bool mx) {
     m.x_off = static_cast<uint32_t>(stages) * m.w_stage_bytes;
     m.qk_off = m.x_off + m.x_ring;
     m.bar_off = m.qk_off + qk_bytes;
-    // After the projection the rings are idle: the CTA that reduces a copy's
-    // gate records copies them there, one slot per copy (at most two).
-    int nh_max = 0;
-    for (int h = 0; h < kMaxCopies; ++h) nh_max = L.nh[h] > nh_max ? L.nh[h] : nh_max;
-    const uint32_t slot = static_cast<uint32_t>((p.T * nh_max * 16 + 127) / 128 * 128);
-    m.rec_slot = 2 * slot <= m.bar_off ? slot : 0u;
     return m;
 }
 
 FusedPlan fused_plan(const engram_handle* h, int64_t T) {
     FusedPlan p = {};
-    p.T = static_cast<int>(T);
     p.Tn = static_cast<int>((T + 15) / 16 * 16);
     p.mtiles = static_cast<int>((T + 127) / 128);
     p.k_blocks = static_cast<int>(h->K * (h->cfg.wkv_format == ENGRAM_WKV_MXFP8 ? 1 : 2) / 128);
@@ -1140,7 +1060,6 @@ cudaError_t launch_decode_fused(engram_handle* h, const void* hidden, const int6
     a.x_off = m.x_off;
     a.qk_off = m.qk_off;
     a.bar_off = m.bar_off;
-    a.rec_slot = m.rec_slot;
 
     cudaLaunchConfig_t cfg = {};
     cfg.gridDim = dim3(static_cast<unsigned>(L.grid));

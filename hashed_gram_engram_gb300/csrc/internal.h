@@ -23,7 +23,7 @@ constexpr int kMaxCopies = 4;                     // largest hc_mult
 constexpr int kMaxFusedT = 256;                   // largest T of the fused decode kernel
 constexpr int kMaxFusedSlice = 256;               // widest column slice of one CTA (MMA N)
 constexpr int kMaxFusedTMx = 128;                 // largest T of the fused kernel, MXFP8 wkv
-constexpr int kFusedCounters = 16;                // 64-bit counters of the fused kernel
+constexpr int kFusedCounters = 4;                 // 64-bit counters of the fused kernel
 
 // MXFP8 scale-factor atoms: the E8M0 scales of 128 rows x 128 k (4 scales
 // per row) as the 512-byte image tcgen05.cp .32x128b.warpx4 copies into
@@ -59,8 +59,7 @@ struct Workspace {
     // fused decode kernel: wkv packed k-block-major (128 bytes of k per row
     // and block) as swizzled shared-memory images, each CTA's columns
     // consecutive; gate-partial records; the fp32 value (validation only);
-    // the kernel's counters (launch, grid barrier 1, per-copy arrivals and
-    // published gates)
+    // the kernel's counters (a launch counter and three grid barriers)
     uint8_t* wpack = nullptr;
     float* fpart = nullptr;     // records: per hc copy [kv_tpitch][CTAs covering it][4]
     float* fvalue = nullptr;    // [kv_tpitch][D]
@@ -82,7 +81,7 @@ struct FusedLayout {
 };
 
 struct FusedPlan {
-    int T, Tn, mtiles, k_blocks;
+    int Tn, mtiles, k_blocks;
 };
 
 // Shared-memory plan of one fused launch (byte offsets from the 1024-byte
@@ -90,8 +89,7 @@ struct FusedPlan {
 struct FusedSmem {
     uint32_t x_bytes, x_stage_bytes, w_stage_bytes, x_ring, x_off, qk_off, bar_off;
     int x_stages, w_stages, dual;
-    uint32_t rec_slot;  // shared-memory bytes per copy of gate records (0: read from L2)
-    bool ok;            // at least two weight stages fit
+    bool ok;  // at least two weight stages fit
 };
 
 }  // namespace engram
