@@ -57,6 +57,9 @@ def parse():
     p.add_argument("--ref-seconds", type=float, default=90.0,
                    help="wall time the reference arm's warm-up and timed steps aim for")
     p.add_argument("--layers", type=int, default=6)
+    p.add_argument("--min-ms", type=float, default=20.0,
+                   help="least total replay time per timed workload (the median of at least "
+                        "5 replays is reported); 0 for short profiler runs")
     p.add_argument("--case", choices=["decode", "prefill", "mxfp8_decode", "mxfp8_prefill"],
                    default=None,
                    help="only run W + K plain forwards of one layer of that workload (the "
@@ -333,16 +336,18 @@ def time_rotation(torch, layers, stream, steps, warmup, min_ms=20.0, min_samples
 
 
 def time_prefetch_rotation(torch, EngramPrefetch, layers, stream, steps, warmup, min_ms=20.0,
-                           min_samples=5):
+                           min_samples=5, wkv=False):
     """The same forwards with every layer's lookup staged ahead on a side
     stream (class EngramPrefetch's start / forward / join): per group of
     the rotated layers, start() issues all their lookups (background grid)
     at once and each forward waits only for its own layer's rows, so a
     lookup runs beside the previous layers' forwards.  Captured in one CUDA
-    graph of ceil(steps / layers) groups.  Returns (median ms per step,
-    steps per sample, per-replay ms per step)."""
+    graph of ceil(steps / layers) groups.  With wkv=True each layer's
+    projection runs ahead on the side stream too (EngramPrefetch's wkv
+    chain) and the forward is the gate and residual alone.  Returns (median
+    ms per step, steps per sample, per-replay ms per step)."""
     NL = len(layers)
-    pf = EngramPrefetch([L["layer"] for L in layers])
+    pf = EngramPrefetch([L["layer"] for L in layers], wkv=wkv)
     groups = max(1, (steps + NL - 1) // NL)
     n = groups * NL
 
@@ -505,7 +510,8 @@ def main():
     clocks.start()
     if world > 1:
         dist.barrier()
-    ms_step, steps, samples = time_rotation(torch, layers, stream, args.steps, args.warmup)
+    ms_step, steps, samples = time_rotation(torch, layers, stream, args.steps, args.warmup,
+                                            args.min_ms)
     if world > 1:
         dist.barrier()
     clk = clocks.stop()
@@ -654,7 +660,8 @@ def main():
         # T = 4096 prefill step on the first layer
         mw = W.MXFP8_DECODE
         mlayers = rotation_layers(mw, NL, W.MXFP8_PREFILL.T, seed0=50)
-        m_ms, m_steps, m_samp = time_rotation(torch, mlayers, stream, args.steps, args.warmup)
+        m_ms, m_steps, m_samp = time_rotation(torch, mlayers, stream, args.steps, args.warmup,
+                                              args.min_ms)
         m_ms = max_over_ranks(m_ms)
         mb = algorithmic_bytes(mw)
         line["mxfp8_decode"] = {
@@ -699,13 +706,18 @@ def main():
                     f"{int(need) >> 30} GiB pinned table, {avail >> 30} GiB host memory free"}, 0
         otable = (W.make_table(ow, "cuda"), W.make_table_scale(ow, "cuda"))
         olayers = rotation_layers(ow, 4, ow.T, table=otable, seed0=seed0)
-        o_ms, o_steps, o_samp = time_rotation(torch, olayers, stream, args.steps, args.warmup)
+        o_ms, o_steps, o_samp = time_rotation(torch, olayers, stream, args.steps, args.warmup,
+                                              args.min_ms)
         o_ms = max_over_ranks(o_ms)
         # the same rotation with each layer's host-table lookup staged ahead
         # on a side stream, beside the previous layers' forwards
         p_ms, p_steps, p_samp = time_prefetch_rotation(torch, EngramPrefetch, olayers, stream,
-                                                       args.steps, args.warmup)
+                                                       args.steps, args.warmup, args.min_ms)
         p_ms = max_over_ranks(p_ms)
+        k_ms, k_steps, k_samp = time_prefetch_rotation(torch, EngramPrefetch, olayers, stream,
+                                                       args.steps, args.warmup, args.min_ms,
+                                                       wkv=True)
+        k_ms = max_over_ranks(k_ms)
         ob = algorithmic_bytes(ow)
         host_b = row_bytes(ow)
         kind = "e4m3 codes + ue8m0 scales per 32" if fp8 else "bf16"
@@ -727,11 +739,17 @@ def main():
                 "steps": p_steps,
                 "host_link_GB_per_s": host_b / (p_ms * 1e-3) / 1e9,
                 "roofline_frac": ob / (p_ms * 1e-3) / 1e9 / hbm_peak},
+            "prefetched_wkv": {
+                "how": "EngramPrefetch(wkv=True): each layer's gather and projection (the fused "
+                       "kernel writing bf16 kv) on the side stream, the forward is "
+                       "engram_gate_noalloc over that kv",
+                "tokens_per_s": world * ow.T / (k_ms * 1e-3), "ms_per_step": k_ms,
+                "steps": k_steps, "roofline_frac": ob / (k_ms * 1e-3) / 1e9 / hbm_peak},
         }
         for L in olayers:
             L["layer"].close()
         del olayers, otable
-        return res, o_steps * len(o_samp) + p_steps * len(p_samp) * 2
+        return res, o_steps * len(o_samp) + p_steps * len(p_samp) * 2 + k_steps * len(k_samp) * 2
 
     if not args.no_offload:
         line["offload"], n = offload_line(W.OFFLOAD, 70)
@@ -742,7 +760,8 @@ def main():
         # offload step with e4m3 rows and ue8m0 scales, dequantized by the gather
         ew = W.DECODE_E4M3
         elayers = rotation_layers(ew, NL, ew.T, seed0=90)
-        e_ms, e_steps, e_samp = time_rotation(torch, elayers, stream, args.steps, args.warmup)
+        e_ms, e_steps, e_samp = time_rotation(torch, elayers, stream, args.steps, args.warmup,
+                                              args.min_ms)
         e_ms = max_over_ranks(e_ms)
         eb = algorithmic_bytes(ew)
         line["decode_e4m3_table"] = {

@@ -169,6 +169,22 @@ class Engram:
         engram_debug_staged_rows(self.handle, rows, T, stream)
         return rows
 
+    def wkv(self, hash_ids=None, stream=None, kv=None):
+        """bf16 kv [T, N] (keys of copies 0..H-1, then the value) of hash_ids,
+        or of the last lookup's rows; decode-sized T only."""
+        import torch
+        from ._lib import engram_wkv
+        T = hash_ids.shape[0] if hash_ids is not None else None
+        if T is None:
+            raise ValueError("pass hash_ids, or kv sized for the staged T")
+        N = (self.hc_mult + 1) * self.dim
+        if kv is None:
+            kv = torch.empty((T, N), dtype=torch.bfloat16,
+                             device=torch.device("cuda", self.device))
+        engram_wkv(self.handle, hash_ids, hash_ids.stride(0) if T else self.n_hash_cols, kv,
+                   kv.stride(0), T, stream)
+        return kv
+
     def staged_mx(self, T, stream=None):
         """e4m3 codes [T, K] and E8M0 scales [T, K/32] of the staged rows (MXFP8)."""
         import torch
@@ -188,9 +204,13 @@ class EngramPrefetch:
     rows.  The layers must outlive this object; while it lives, only it
     looks up rows for them."""
 
-    def __init__(self, layers):
+    def __init__(self, layers, wkv=False):
+        """wkv=True also runs each layer's projection on the side stream
+        (where its fused decode launch serves T); forward then runs only the
+        gate and residual."""
         self.layers = list(layers)
-        self.handle = engram_prefetch_create([L.handle for L in self.layers])
+        self.handle = engram_prefetch_create([L.handle for L in self.layers],
+                                             _lib.ENGRAM_PREFETCH_WKV if wkv else 0)
         self.T = None
 
     def close(self):

@@ -51,6 +51,7 @@ EXPORTED = (
     "engram_prefetch_create", "engram_prefetch_destroy", "engram_prefetch_start",
     "engram_prefetch_forward", "engram_prefetch_join", "engram_prefetch_pending",
     "engram_debug_barrier_skew",
+    "engram_wkv",
 )
 
 
@@ -115,8 +116,9 @@ def load(path: str | None = None):
             "engram_profile_read": [vp, vp],
             "engram_gate_noalloc": [vp, vp, vp, i64, vp, vp, vp, vp, vp, i64, i64, i64,
                                     ctypes.c_double, ctypes.c_double, vp],
-            "engram_prefetch_create": [vp, i32, vp],
             "engram_debug_barrier_skew": [vp, i64],
+            "engram_prefetch_create": [vp, i32, i32, vp],
+            "engram_wkv": [vp, vp, i64, vp, i64, i64, vp],
             "engram_prefetch_destroy": [vp],
             "engram_prefetch_start": [vp, vp, vp, i64, ctypes.c_int, vp],
             "engram_prefetch_forward": [vp, i32, vp, vp, vp, i64, vp, vp, vp, i64, vp],
@@ -265,12 +267,20 @@ def engram_gate_noalloc(hidden, hidden_strides, kv, kv_row_stride, q_weight, k_w
         int(D), float(eps), float(clamp), _stream(stream)), "engram_gate_noalloc")
 
 
-def engram_prefetch_create(handles) -> int:
+ENGRAM_PREFETCH_WKV = 1
+
+
+def engram_prefetch_create(handles, flags=0) -> int:
     arr = (ctypes.c_void_p * len(handles))(*handles)
     p = ctypes.c_void_p()
-    _check(load().engram_prefetch_create(arr, len(handles), ctypes.byref(p)),
+    _check(load().engram_prefetch_create(arr, len(handles), int(flags), ctypes.byref(p)),
            "engram_prefetch_create")
     return p.value
+
+
+def engram_wkv(h, hash_ids, ids_row_stride, kv, kv_row_stride, T, stream=None):
+    return _check(load().engram_wkv(h, _ptr(hash_ids), int(ids_row_stride), _ptr(kv),
+                                    int(kv_row_stride), int(T), _stream(stream)), "engram_wkv")
 
 
 def engram_prefetch_destroy(p) -> None:

@@ -111,7 +111,9 @@ struct FusedArgs {
     int rec_base[kMaxCopies];  // float4 offset of each copy's block
     int cf[kMaxCopies];        // first CTA holding each copy's keys
     int nh[kMaxCopies];        // number of CTAs holding each copy's keys
-    float* value;              // fp32 [T][D] for validation, or null
+    float* value;              // fp32 [T][D]: each CTA's value dims, read by the residual items
+    uint16_t* kv;              // kv mode: bf16 [T][kv_ld] keys then value; no gate, no residual
+    int64_t kv_ld;
     unsigned long long* bar;   // launch counter, then three barrier counters
     float* gate_out;
     float eps, clamp, inv_d, inv_sqrt_d;
@@ -123,35 +125,18 @@ __device__ __forceinline__ int first_granule(int cta, int n, int G) {
     return static_cast<int>(static_cast<int64_t>(cta) * n / G);
 }
 
-// out = hidden + g * value at 16 dims of every hc copy of one token, rounded
-// to bf16; a masked token keeps hidden's bits.  hin: hidden there, v: the
-// value (fp32).
-__device__ __forceinline__ void residual16(uint16_t* out, int64_t os_t, int64_t os_h, int t, int d,
-                                           int H, const uint4 (&hin)[kMaxCopies][2],
-                                           const float* v, const float* g, bool active) {
+// 16 fp32 values (bit patterns) -> 16 bf16 (nearest even) at dst, 32-byte
+// aligned: two 16-byte stores.
+__device__ __forceinline__ void store_bf16x16(uint16_t* dst, const uint32_t (&r)[16]) {
+    uint4 o[2];
 #pragma unroll
-    for (int h = 0; h < kMaxCopies; ++h) {
-        if (h >= H) continue;
-        uint4 o0 = hin[h][0], o1 = hin[h][1];
-        if (active) {
-            const float gh = g[h];
-            const uint32_t w0[4] = {o0.x, o0.y, o0.z, o0.w};
-            const uint32_t w1[4] = {o1.x, o1.y, o1.z, o1.w};
-            uint32_t p0[4], p1[4];
-#pragma unroll
-            for (int k = 0; k < 4; ++k) {
-                p0[k] = pack_bf16x2(fmaf(gh, v[2 * k], bf16lo(w0[k])),
-                                    fmaf(gh, v[2 * k + 1], bf16hi(w0[k])));
-                p1[k] = pack_bf16x2(fmaf(gh, v[8 + 2 * k], bf16lo(w1[k])),
-                                    fmaf(gh, v[8 + 2 * k + 1], bf16hi(w1[k])));
-            }
-            o0 = make_uint4(p0[0], p0[1], p0[2], p0[3]);
-            o1 = make_uint4(p1[0], p1[1], p1[2], p1[3]);
-        }
-        uint16_t* op = out + t * os_t + h * os_h + d;
-        st_v4(op, o0);
-        st_v4(op + 8, o1);
-    }
+    for (int h = 0; h < 2; ++h)
+        o[h] = make_uint4(pack_bf16x2(__uint_as_float(r[8 * h + 0]), __uint_as_float(r[8 * h + 1])),
+                          pack_bf16x2(__uint_as_float(r[8 * h + 2]), __uint_as_float(r[8 * h + 3])),
+                          pack_bf16x2(__uint_as_float(r[8 * h + 4]), __uint_as_float(r[8 * h + 5])),
+                          pack_bf16x2(__uint_as_float(r[8 * h + 6]), __uint_as_float(r[8 * h + 7])));
+    st_v4(dst, o[0]);
+    st_v4(dst + 8, o[1]);
 }
 
 __device__ __forceinline__ void fail(int* abort_flag, unsigned* err) {
@@ -301,14 +286,13 @@ __global__ void __launch_bounds__(kThreads, 1)
     const uint32_t tm_sfa = tmem_base + kMaxFusedSlice;                     // tokens
     const uint32_t tm_sfb = tm_sfa + 8u * static_cast<uint32_t>(a.kb128);  // weights
 
-    // One token tile and at most kEarlyChunks 16-dim value chunks: the
-    // epilogue warps load the residual's operands (the value from TMEM, hidden
-    // at the CTA's value dims, which no other CTA touches) before grid
-    // barrier 2, so after barrier 3 only the gates are waited for.
-    constexpr int kEarlyChunks = 3;
-    const bool early = a.mtiles == 1 && (vlen >> 4) <= kEarlyChunks;
-    float ev[kEarlyChunks][16];
-    uint4 eh[kEarlyChunks][kMaxCopies][2];
+    const bool kvm = a.kv != nullptr;  // kv mode: hidden, mask and out are not read
+    // This CTA's residual items after grid barrier 2: (token, 256-dim block)
+    // pairs [i0, i1) of the T * D/256 in token-major order.
+    const int nb = a.D >> 8;
+    const int n_items = kvm ? 0 : a.T * nb;
+    const int it0 = static_cast<int>(static_cast<int64_t>(c) * n_items / G);
+    const int it1 = static_cast<int>(static_cast<int64_t>(c + 1) * n_items / G);
 
     if (warp == 0) {
         if (lane == 0) {
@@ -559,7 +543,7 @@ __global__ void __launch_bounds__(kThreads, 1)
 #pragma unroll
             for (int ci = 0; ci < kKeyChunks; ++ci) {
                 hv[2 * ci] = hv[2 * ci + 1] = make_uint4(0u, 0u, 0u, 0u);
-                if (live && ci * 16 < klen) {
+                if (live && !kvm && ci * 16 < klen) {
                     const int n0 = k0 + ci * 16;
                     const int h = n0 / a.D, d0 = n0 - h * a.D;
                     const uint16_t* hp = a.hidden + t * a.hs_t + h * a.hs_h + d0;
@@ -594,6 +578,10 @@ __global__ void __launch_bounds__(kThreads, 1)
                         r[e] = __float_as_uint(__uint_as_float(r[e]) + __uint_as_float(r2[e]));
                 }
                 tmem_ld_wait();
+                if (kvm) {
+                    if (live) store_bf16x16(a.kv + static_cast<int64_t>(t) * a.kv_ld + k0 + ci * 16, r);
+                    continue;
+                }
                 const int n0 = k0 + ci * 16;  // 16 columns never straddle an hc copy
                 const int hi = n0 / a.D - h0;
                 const uint32_t w[8] = {hv[2 * ci].x,     hv[2 * ci].y,     hv[2 * ci].z,
@@ -612,7 +600,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                 acc[hi][1] += skk;
                 acc[hi][2] += shk;
             }
-            if (live) {
+            if (live && !kvm) {
                 // a record for every copy whose CTA range includes this CTA
                 // (zeros where it holds none of the copy's keys)
                 const int hl = klen > 0 ? (k0 + klen - 1) / a.D : -1;  // last copy of the run
@@ -624,8 +612,30 @@ __global__ void __launch_bounds__(kThreads, 1)
                             : make_float4(0.f, 0.f, 0.f, 0.f);
                 }
             }
-            if (a.value != nullptr) {
-                // validation: the fp32 value of this CTA's dims
+            if (kvm) {
+                for (int ci = 0; ci * 16 < vlen; ++ci) {
+                    uint32_t r[16];  // every lane loads (tcgen05.ld is warp-wide)
+                    const uint32_t va =
+                        tmem_base + lane_base + static_cast<uint32_t>(m * kMaxFusedSlice + ci * 16);
+                    tmem_ld16(va, r);
+                    if (a.dual) {
+                        uint32_t r2[16];
+                        tmem_ld16(va + 256u, r2);
+                        tmem_ld_wait();
+#pragma unroll
+                        for (int e = 0; e < 16; ++e)
+                            r[e] = __float_as_uint(__uint_as_float(r[e]) + __uint_as_float(r2[e]));
+                    }
+                    tmem_ld_wait();
+                    if (live)
+                        store_bf16x16(a.kv + static_cast<int64_t>(t) * a.kv_ld +
+                                          static_cast<int64_t>(a.H) * a.D + v0 + ci * 16,
+                                      r);
+                }
+            }
+            if (!kvm) {
+                // the fp32 value of this CTA's dims for every token: the residual
+                // items after grid barrier 2 read it from L2
                 for (int ci = 0; ci * 16 < vlen; ++ci) {
                     uint32_t r[16];
                     const uint32_t va =
@@ -652,45 +662,15 @@ __global__ void __launch_bounds__(kThreads, 1)
                     }
                 }
             }
-            // the residual reads hidden at the value dims: start it towards L2
-            // (plain per-line prefetches; bulk ones would queue on the TMA unit)
-            if (live && vlen > 0 && !early)
-                for (int h = 0; h < a.H; ++h) {
-                    const uint16_t* hp = a.hidden + t * a.hs_t + h * a.hs_h + v0;
-                    prefetch_line_l2(hp);
-                    prefetch_line_l2(hp + vlen - 1);
-                }
         }
-        if (early && go) {
-            const int t = q * 32 + lane;
-            const bool live = t < a.T;
-#pragma unroll
-            for (int ci = 0; ci < kEarlyChunks; ++ci) {
-                if (ci >= (vlen >> 4)) break;
-                uint32_t r[16];  // every lane loads (tcgen05.ld is warp-wide)
-                const uint32_t va = tmem_base + lane_base + static_cast<uint32_t>(ci * 16);
-                tmem_ld16(va, r);
-                if (a.dual) {
-                    uint32_t r2[16];
-                    tmem_ld16(va + 256u, r2);
-                    tmem_ld_wait();
-#pragma unroll
-                    for (int e = 0; e < 16; ++e)
-                        r[e] = __float_as_uint(__uint_as_float(r[e]) + __uint_as_float(r2[e]));
-                }
-                tmem_ld_wait();
-#pragma unroll
-                for (int e = 0; e < 16; ++e) ev[ci][e] = __uint_as_float(r[e]);
-#pragma unroll
-                for (int h = 0; h < kMaxCopies; ++h) {
-                    if (live && h < a.H) {
-                        const uint16_t* hp = a.hidden + t * a.hs_t + h * a.hs_h + v0 + ci * 16;
-                        eh[ci][h][0] = ld_nc_v4(hp);
-                        eh[ci][h][1] = ld_nc_v4(hp + 8);
-                    }
-                }
+        // the residual items' hidden rows towards L2 (read after barrier 2;
+        // plain per-line prefetches, four 128-byte lines per copy and item)
+        if (go)
+            for (int l = etid; l < (it1 - it0) * a.H * 4; l += 128) {
+                const int item = it0 + l / (a.H * 4), r = l - (l / (a.H * 4)) * (a.H * 4);
+                const int t = item / nb, d = (item - t * nb) * 256 + (r & 3) * 64;
+                prefetch_line_l2(a.hidden + t * a.hs_t + (r >> 2) * a.hs_h + d);
             }
-        }
         // every record this CTA owes is written: grid barrier 2 (the release
         // add of one thread covers the CTA's writes ordered before it by the
         // named barrier)
@@ -704,13 +684,41 @@ __global__ void __launch_bounds__(kThreads, 1)
     __syncwarp();
     tc_fence_before();
     __syncthreads();
-    if (!*abort_v) {
-        // Gates: CTA c reduces the rows (token, copy) r = c, c + G, ...; one
-        // warp per row, lane l adding the records of the copy's CTAs l,
-        // l + 32, ..., then a shuffle tree (a fixed order); grid barrier 3.
-        const int HR = a.T * a.H;
-        for (int r = c + warp * G; r < HR; r += kWarps * G) {
-            const int t = r / a.H, h = r - t * a.H;
+    // Residual items: every CTA finishes its (token, 256-dim block) items
+    // straight after grid barrier 2.  Each thread first loads its task (8
+    // dims of one item: the fp32 value and the H hidden chunks); warps reduce
+    // the gate of every (token, copy) its items touch from the records (lane
+    // l adds records l, l + 32, ..., then a shuffle tree: a fixed order, so
+    // runs are bit-identical) into shared memory; then out = hidden +
+    // gate * value (masked tokens keep hidden's bits).  The records, the
+    // value and hidden all come in one round trip, and no CTA waits for
+    // another's gates.
+    float* gate_s = qk_s;  // (the q*k slice is no longer needed)
+    const int tok0 = it1 > it0 ? it0 / nb : 0;
+    const int ntok = it1 > it0 ? (it1 - 1) / nb - tok0 + 1 : 0;
+    if (!*abort_v && ntok > 0) {
+        const int ntask = (it1 - it0) * 32;
+        auto task_at = [&](int k, int& t, int& d) {
+            const int item = it0 + (k >> 5);
+            t = item / nb;
+            d = (item - t * nb) * 256 + (k & 31) * 8;
+        };
+        // the first task's operands, before the gates
+        float4 v0 = make_float4(0.f, 0.f, 0.f, 0.f), v1 = v0;
+        uint4 x[kMaxCopies];
+        int t0 = 0, d0 = 0;
+        const bool has0 = tid < ntask;
+        if (has0) {
+            task_at(tid, t0, d0);
+            const float4* vp = reinterpret_cast<const float4*>(a.value + static_cast<int64_t>(t0) * a.D + d0);
+            v0 = __ldcg(vp);
+            v1 = __ldcg(vp + 1);
+#pragma unroll
+            for (int h = 0; h < kMaxCopies; ++h)
+                if (h < a.H) x[h] = ld_nc_v4(a.hidden + t0 * a.hs_t + h * a.hs_h + d0);
+        }
+        for (int r = warp; r < ntok * a.H; r += kWarps) {
+            const int t = tok0 + r / a.H, h = r - (r / a.H) * a.H;
             const float4* rr = a.rec + a.rec_base[h] + static_cast<int64_t>(t) * a.nh[h];
             float s_hh = 0.f, s_kk = 0.f, s_hk = 0.f;
             for (int j = lane; j < a.nh[h]; j += 32) {
@@ -732,15 +740,44 @@ __global__ void __launch_bounds__(kThreads, 1)
                 const float dot = s_hk * hr * kr * a.inv_sqrt_d;
                 float gi = sqrtf(fmaxf(fabsf(dot), a.clamp));
                 if (dot < 0.0f) gi = -gi;
-                a.gate_out[r] = active ? 1.0f / (1.0f + expf(-gi)) : 0.0f;
+                const float g = active ? 1.0f / (1.0f + expf(-gi)) : 0.0f;
+                gate_s[r] = g;
+                a.gate_out[t * a.H + h] = g;  // (CTAs sharing a token write the same bits)
             }
         }
         __syncthreads();
-        if (tid == 0) {
-            grid_arrive(a.bar + 3);
-            if (!grid_wait(a.bar + 3, target)) fail(abort_flag, a.err);
+        auto finish = [&](int t, int d, const float4& va, const float4& vb, const uint4 (&xh)[kMaxCopies]) {
+            const bool active = a.mask == nullptr || a.mask[t] != 0;
+            const float v[8] = {va.x, va.y, va.z, va.w, vb.x, vb.y, vb.z, vb.w};
+#pragma unroll
+            for (int h = 0; h < kMaxCopies; ++h) {
+                if (h >= a.H) continue;
+                uint4 o = xh[h];
+                if (active) {
+                    const float g = gate_s[(t - tok0) * a.H + h];
+                    const uint32_t w[4] = {o.x, o.y, o.z, o.w};
+                    uint32_t p[4];
+#pragma unroll
+                    for (int k = 0; k < 4; ++k)
+                        p[k] = pack_bf16x2(fmaf(g, v[2 * k], bf16lo(w[k])),
+                                           fmaf(g, v[2 * k + 1], bf16hi(w[k])));
+                    o = make_uint4(p[0], p[1], p[2], p[3]);
+                }
+                st_v4(a.out + t * a.os_t + h * a.os_h + d, o);
+            }
+        };
+        if (has0) finish(t0, d0, v0, v1, x);
+        for (int k = tid + kThreads; k < ntask; k += kThreads) {
+            int t, d;
+            task_at(k, t, d);
+            const float4* vp = reinterpret_cast<const float4*>(a.value + static_cast<int64_t>(t) * a.D + d);
+            const float4 va = __ldcg(vp), vb = __ldcg(vp + 1);
+            uint4 xh[kMaxCopies];
+#pragma unroll
+            for (int h = 0; h < kMaxCopies; ++h)
+                if (h < a.H) xh[h] = ld_nc_v4(a.hidden + t * a.hs_t + h * a.hs_h + d);
+            finish(t, d, va, vb, xh);
         }
-        __syncthreads();
     }
     if (*abort_v) {
         // let in-flight copies and MMAs land before shared memory and TMEM go
@@ -769,71 +806,8 @@ __global__ void __launch_bounds__(kThreads, 1)
     }
     tc_fence_after();
 
-    // Residual at this CTA's value dims: thread = token (TMEM lane); the
-    // value comes straight from the accumulator.
-    const int nchunk_v = vlen >> 4;
-    if (warp >= 2 && warp < 6 && nchunk_v > 0 && early) {
-        const int q = warp & 3;
-        const int t = q * 32 + lane;
-        if (t < a.T) {
-            const bool active = a.mask == nullptr || a.mask[t] != 0;
-            float g[kMaxCopies];
-#pragma unroll
-            for (int h = 0; h < kMaxCopies; ++h)
-                g[h] = (active && h < a.H) ? __ldcg(a.gate_out + static_cast<int64_t>(t) * a.H + h)
-                                           : 0.f;
-#pragma unroll
-            for (int ci = 0; ci < kEarlyChunks; ++ci)
-                if (ci < nchunk_v)
-                    residual16(a.out, a.os_t, a.os_h, t, v0 + ci * 16, a.H, eh[ci], ev[ci], g,
-                               active);
-        }
-    } else if (warp >= 2 && warp < 6 && nchunk_v > 0) {
-        const int q = warp & 3;
-        const uint32_t lane_base = static_cast<uint32_t>(q * 32) << 16;
-        for (int m = 0; m < a.mtiles; ++m) {
-            if (m * 128 + q * 32 >= a.T) continue;  // warp-uniform: no live token
-            const int t = m * 128 + q * 32 + lane;
-            const bool live = t < a.T;
-            const bool active = live && (a.mask == nullptr || a.mask[t] != 0);
-            float g[kMaxCopies];
-#pragma unroll
-            for (int h = 0; h < kMaxCopies; ++h)
-                g[h] = (active && h < a.H) ? __ldcg(a.gate_out + static_cast<int64_t>(t) * a.H + h)
-                                           : 0.f;
-            for (int ci = 0; ci < nchunk_v; ++ci) {
-                uint32_t r[16];  // every lane loads (tcgen05.ld is warp-wide)
-                const uint32_t va =
-                    tmem_base + lane_base + static_cast<uint32_t>(m * kMaxFusedSlice + ci * 16);
-                tmem_ld16(va, r);
-                if (a.dual) {
-                    uint32_t r2[16];
-                    tmem_ld16(va + 256u, r2);
-                    tmem_ld_wait();
-#pragma unroll
-                    for (int e = 0; e < 16; ++e)
-                        r[e] = __float_as_uint(__uint_as_float(r[e]) + __uint_as_float(r2[e]));
-                }
-                tmem_ld_wait();
-                if (!live) continue;
-                const int d = v0 + ci * 16;
-                uint4 hin[kMaxCopies][2];
-#pragma unroll
-                for (int h = 0; h < kMaxCopies; ++h) {  // all loads before any store (in place)
-                    if (h < a.H) {
-                        const uint16_t* hp = a.hidden + t * a.hs_t + h * a.hs_h + d;
-                        hin[h][0] = ld_nc_v4(hp);
-                        hin[h][1] = ld_nc_v4(hp + 8);
-                    }
-                }
-                float v[16];
-#pragma unroll
-                for (int e = 0; e < 16; ++e) v[e] = __uint_as_float(r[e]);
-                residual16(a.out, a.os_t, a.os_h, t, d, a.H, hin, v, g, active);
-            }
-        }
-    }
-    // every CTA has read this launch's epoch (it passed barrier 3): advance it
+    // every CTA read this launch's epoch before its barrier 2 arrival, and
+    // this CTA passed barrier 2: advance it
     if (c == 0 && tid == 0) atomicAdd(a.bar, 1ull);
     tc_fence_before();
     __syncthreads();
@@ -994,7 +968,7 @@ cudaError_t launch_fused_debug_value(const engram_handle* h, float* value, int64
 cudaError_t launch_decode_fused(engram_handle* h, const void* hidden, const int64_t* hs,
                                 const int32_t* ids, int64_t ids_stride, const uint8_t* mask,
                                 void* out, const int64_t* os, int64_t T, cudaStream_t s,
-                                bool pdl) {
+                                bool pdl, uint16_t* kv, int64_t kv_ld) {
     const FusedPlan p = fused_plan(h, T);
     const FusedLayout& L = h->fused;
     const bool mx = h->cfg.wkv_format == ENGRAM_WKV_MXFP8;
@@ -1025,12 +999,14 @@ cudaError_t launch_decode_fused(engram_handle* h, const void* hidden, const int6
     a.staged_s = h->ws.staged_s;
     a.wscale = h->wkv_scale;
     a.hidden = static_cast<const uint16_t*>(hidden);
-    a.hs_t = hs[0];
-    a.hs_h = hs[1];
+    a.hs_t = hs != nullptr ? hs[0] : 0;
+    a.hs_h = hs != nullptr ? hs[1] : 0;
     a.out = static_cast<uint16_t*>(out);
-    a.os_t = os[0];
-    a.os_h = os[1];
+    a.os_t = os != nullptr ? os[0] : 0;
+    a.os_h = os != nullptr ? os[1] : 0;
     a.mask = mask;
+    a.kv = kv;  // kv mode: hidden, out and mask unused
+    a.kv_ld = kv_ld;
     a.qk = h->ws.qk;
     a.wpack = h->ws.wpack;
     a.rec = reinterpret_cast<float4*>(h->ws.fpart);
@@ -1041,7 +1017,7 @@ cudaError_t launch_decode_fused(engram_handle* h, const void* hidden, const int6
         a.rec_base[hh] = base;
         base += static_cast<int>(h->ws.kv_tpitch) * L.nh[hh];
     }
-    a.value = h->keep_value ? h->ws.fvalue : nullptr;
+    a.value = h->ws.fvalue;  // the value exchange buffer of the residual items
     a.bar = reinterpret_cast<unsigned long long*>(h->ws.grid_bar);
     a.gate_out = h->ws.gate;
     a.eps = static_cast<float>(h->cfg.eps);

@@ -435,6 +435,30 @@ int engram_debug_barrier_skew(engram_t* h, int64_t delta) {
     return cuda_err(h, e);
 }
 
+int engram_wkv(engram_t* h, const int32_t* hash_ids, int64_t ids_row_stride, void* kv,
+               int64_t kv_row_stride, int64_t T, cudaStream_t stream) {
+    if (h == nullptr) return ENGRAM_ERR_INVALID_ARG;
+    if (T < 0) return set_err(h, ENGRAM_ERR_INVALID_ARG);
+    if (T > h->cfg.max_tokens) return set_err(h, ENGRAM_ERR_T_EXCEEDS_MAX);
+    if (T == 0) return set_err(h, ENGRAM_OK);
+    if (kv == nullptr || !aligned16(kv) || kv_row_stride < h->N || kv_row_stride % 8 != 0)
+        return set_err(h, ENGRAM_ERR_INVALID_ARG);
+    if (hash_ids != nullptr && ids_row_stride < h->C) return set_err(h, ENGRAM_ERR_INVALID_ARG);
+    if (hash_ids == nullptr && h->staged_T != T) return set_err(h, ENGRAM_ERR_INVALID_ARG);
+    if (!fused_supported(h, T)) return set_err(h, ENGRAM_ERR_UNSUPPORTED);
+    DeviceGuard guard(h->cfg.device);
+    if (!guard.ok) return set_err(h, ENGRAM_ERR_CUDA);
+    // the decode kernel in kv mode: gather (when ids are given) and
+    // projection, the gate and residual left out
+    const cudaError_t e =
+        launch_decode_fused(h, nullptr, nullptr, hash_ids, ids_row_stride, nullptr, nullptr,
+                            nullptr, T, stream, h->profiling == 0, static_cast<uint16_t*>(kv),
+                            kv_row_stride);
+    if (hash_ids != nullptr && e == cudaSuccess) h->staged_T = T;
+    h->last_path = 0;  // no gate or value of a forward to report
+    return cuda_err(h, e);
+}
+
 int engram_debug_fused_plan(const engram_config* cfg, int64_t T, int32_t num_sms,
                             int64_t* out, int32_t n_out) {
     if (cfg == nullptr || out == nullptr || n_out < ENGRAM_FUSED_PLAN_FIELDS || num_sms < 1 ||
@@ -537,7 +561,7 @@ int engram_debug_intermediates(engram_t* h, float* gate, float* value, int64_t T
         e = cudaMemcpyAsync(gate, h->ws.gate, T * h->cfg.hc_mult * sizeof(float),
                             cudaMemcpyDeviceToDevice, stream);
     if (e == cudaSuccess && value != nullptr) {
-        if (h->last_path == 0 || (h->last_path == 3 && !h->keep_value))
+        if (h->last_path == 0)
             return ENGRAM_ERR_INVALID_ARG;
         e = h->last_path == 3 ? launch_fused_debug_value(h, value, T, stream)
                               : launch_debug_value(h, value, T, stream);

@@ -152,7 +152,7 @@ cudaError_t launch_fused_debug_value(const engram_handle* h, float* value, int64
 cudaError_t launch_decode_fused(engram_handle* h, const void* hidden, const int64_t* hs,
                                 const int32_t* ids, int64_t ids_stride, const uint8_t* mask,
                                 void* out, const int64_t* os, int64_t T, cudaStream_t s,
-                                bool pdl);
+                                bool pdl, uint16_t* kv = nullptr, int64_t kv_ld = 0);
 
 // gate.cu
 cudaError_t launch_gate_from_partials(const engram_handle* h, const void* hidden,

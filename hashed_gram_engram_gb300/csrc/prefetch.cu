@@ -30,6 +30,10 @@ struct engram_prefetch {
     cudaEvent_t start_ev;   // the caller's stream at start
     cudaStream_t side;
     int64_t T;              // tokens of the last start
+    int32_t flags;
+    uint16_t** kv;          // ENGRAM_PREFETCH_WKV: per layer bf16 [kv_rows, N]
+    int64_t* kv_rows;
+    bool* kv_ready;         // the last start ran this layer's wkv (else its lookup only)
 };
 
 namespace {
@@ -54,6 +58,12 @@ void release(engram_prefetch* p) {
             if (p->done[i] != nullptr) cudaEventDestroy(p->done[i]);
     if (p->start_ev != nullptr) cudaEventDestroy(p->start_ev);
     if (p->side != nullptr) cudaStreamDestroy(p->side);
+    if (p->kv != nullptr)
+        for (int32_t i = 0; i < p->n; ++i)
+            if (p->kv[i] != nullptr) cudaFree(p->kv[i]);
+    delete[] p->kv;
+    delete[] p->kv_rows;
+    delete[] p->kv_ready;
     delete[] p->done;
     delete[] p->pending;
     delete[] p->layers;
@@ -64,10 +74,12 @@ void release(engram_prefetch* p) {
 
 extern "C" {
 
-int engram_prefetch_create(engram_t* const* layers, int32_t n_layers, engram_prefetch_t** out) {
+int engram_prefetch_create(engram_t* const* layers, int32_t n_layers, int32_t flags,
+                           engram_prefetch_t** out) {
     if (out == nullptr) return ENGRAM_ERR_INVALID_ARG;
     *out = nullptr;
-    if (layers == nullptr || n_layers < 1) return ENGRAM_ERR_INVALID_ARG;
+    if (layers == nullptr || n_layers < 1 || (flags & ~ENGRAM_PREFETCH_WKV) != 0)
+        return ENGRAM_ERR_INVALID_ARG;
     for (int32_t i = 0; i < n_layers; ++i)
         if (layers[i] == nullptr) return ENGRAM_ERR_INVALID_ARG;
     const int dev = layers[0]->cfg.device;
@@ -82,7 +94,12 @@ int engram_prefetch_create(engram_t* const* layers, int32_t n_layers, engram_pre
     p->layers = new (std::nothrow) engram_t*[n_layers];
     p->pending = new (std::nothrow) bool[n_layers];
     p->done = new (std::nothrow) cudaEvent_t[n_layers];
-    if (p->layers == nullptr || p->pending == nullptr || p->done == nullptr) {
+    p->flags = flags;
+    p->kv = new (std::nothrow) uint16_t*[n_layers];
+    p->kv_rows = new (std::nothrow) int64_t[n_layers];
+    p->kv_ready = new (std::nothrow) bool[n_layers];
+    if (p->layers == nullptr || p->pending == nullptr || p->done == nullptr ||
+        p->kv == nullptr || p->kv_rows == nullptr || p->kv_ready == nullptr) {
         release(p);
         return ENGRAM_ERR_OOM;
     }
@@ -90,6 +107,9 @@ int engram_prefetch_create(engram_t* const* layers, int32_t n_layers, engram_pre
         p->layers[i] = layers[i];
         p->pending[i] = false;
         p->done[i] = nullptr;
+        p->kv[i] = nullptr;
+        p->kv_rows[i] = 0;
+        p->kv_ready[i] = false;
     }
     Guard g(dev);
     cudaError_t e = g.ok ? cudaSuccess : cudaErrorInvalidDevice;
@@ -97,9 +117,18 @@ int engram_prefetch_create(engram_t* const* layers, int32_t n_layers, engram_pre
     if (e == cudaSuccess) e = cudaEventCreateWithFlags(&p->start_ev, cudaEventDisableTiming);
     for (int32_t i = 0; i < n_layers && e == cudaSuccess; ++i)
         e = cudaEventCreateWithFlags(&p->done[i], cudaEventDisableTiming);
+    // wkv mode: a kv buffer per layer for the largest T its fused launch serves
+    for (int32_t i = 0; i < n_layers && e == cudaSuccess && (flags & ENGRAM_PREFETCH_WKV); ++i) {
+        const engram_handle* h = layers[i];
+        const int64_t tmax = h->cfg.wkv_format == ENGRAM_WKV_MXFP8 ? kMaxFusedTMx : kMaxFusedT;
+        p->kv_rows[i] = h->cfg.max_tokens < tmax ? h->cfg.max_tokens : tmax;
+        if (h->fused.ok)
+            e = cudaMalloc(reinterpret_cast<void**>(&p->kv[i]),
+                           static_cast<size_t>(p->kv_rows[i] * h->N * 2));
+    }
     if (e != cudaSuccess) {
         release(p);
-        return ENGRAM_ERR_CUDA;
+        return e == cudaErrorMemoryAllocation ? ENGRAM_ERR_OOM : ENGRAM_ERR_CUDA;
     }
     *out = p;
     return ENGRAM_OK;
@@ -134,8 +163,16 @@ int engram_prefetch_start(engram_prefetch_t* p, const int32_t* const* hash_ids,
     if (e == cudaSuccess) e = cudaStreamWaitEvent(p->side, p->start_ev, 0);
     if (e != cudaSuccess) return ENGRAM_ERR_CUDA;
     for (int32_t i = 0; i < p->n; ++i) {
-        const int rc = engram_lookup(p->layers[i], hash_ids[i], ids_row_stride[i], T,
-                                     background, p->side);
+        engram_handle* h = p->layers[i];
+        // wkv mode, where the layer's fused launch serves T: gather and
+        // projection here, only the gate and residual left for forward
+        p->kv_ready[i] = p->kv[i] != nullptr && T > 0 && T <= p->kv_rows[i] &&
+                         fused_supported(h, T);
+        const int rc = p->kv_ready[i]
+                           ? engram_wkv(h, hash_ids[i], ids_row_stride[i], p->kv[i], h->N, T,
+                                        p->side)
+                           : engram_lookup(h, hash_ids[i], ids_row_stride[i], T, background,
+                                           p->side);
         if (rc != ENGRAM_OK) return rc;
         if (cudaEventRecord(p->done[i], p->side) != cudaSuccess) return ENGRAM_ERR_CUDA;
         p->pending[i] = true;
@@ -160,6 +197,10 @@ int engram_prefetch_forward(engram_prefetch_t* p, int32_t layer, const void* hid
     if (!g.ok) return ENGRAM_ERR_CUDA;
     if (cudaStreamWaitEvent(stream, p->done[layer], 0) != cudaSuccess) return ENGRAM_ERR_CUDA;
     p->pending[layer] = false;
+    if (p->kv_ready[layer])  // the post-wkv kernel of EngramPrefetch.forward
+        return engram_gate_noalloc(hidden, hidden_strides, p->kv[layer], h->N, h->q, h->k,
+                                   token_mask, out, out_strides, T, h->cfg.hc_mult, h->cfg.dim,
+                                   h->cfg.eps, h->cfg.clamp, stream);
     return engram_forward(h, hidden, hidden_strides, nullptr, 0, token_mask, out, out_strides, T,
                           stream);
 }

@@ -276,6 +276,19 @@ int engram_profile_read(engram_t* h, float ms[3]);
  * normally.  Synchronous.  Nothing faults, traps or hangs. */
 int engram_debug_barrier_skew(engram_t* h, int64_t delta);
 
+/* The wkv projection alone: kv = rows . wkv^T rounded to bf16, the output of
+ * Engram.forward's wkv (class Engram on the page
+ * "vllm.models.deepseek_v4_1.common.engram"): keys of copies h = 0..H-1 in
+ * columns [h*D, (h+1)*D), then the value in [H*D, N).  rows are gathered
+ * from hash_ids (device int32 [T, C], row stride >= C), or with hash_ids
+ * NULL taken from the last engram_lookup of the same T.  kv: device bf16
+ * [T, kv_row_stride], 16-byte aligned, kv_row_stride >= N and a multiple of
+ * 8.  Decode-sized T only (the configurations engram_forward runs in one
+ * fused launch: T <= 256, MXFP8 T <= 128); others return
+ * ENGRAM_ERR_UNSUPPORTED.  engram_gate_noalloc finishes the layer from kv. */
+int engram_wkv(engram_t* h, const int32_t* hash_ids, int64_t ids_row_stride, void* kv,
+               int64_t kv_row_stride, int64_t T, cudaStream_t stream);
+
 /* ------------------------------------------------------------------------
  * Lookups of several layers run ahead on a side stream.  This follows the
  * prefetch page ("vllm.models.deepseek_v41.nvidia.specialized_decode.
@@ -288,6 +301,11 @@ int engram_debug_barrier_skew(engram_t* h, int64_t delta);
  *
  * Host-side orchestration only: no kernel of its own.
  * engram_prefetch_create
+ *   flags: 0, or ENGRAM_PREFETCH_WKV: where a layer's fused decode launch
+ *   serves the start's T, start runs engram_wkv instead of the lookup into
+ *   a kv buffer the prefetcher owns (allocated here), and the layer's
+ *   forward is engram_gate_noalloc over it -- the pages' side-stream wkv
+ *   chain; other T fall back to the lookup.
  *   layers: n_layers >= 1 handles on one device.  They are borrowed and must
  *   outlive the prefetcher; while it lives, only it may call engram_lookup
  *   on them.  It owns a non-blocking side stream and one event per layer.
@@ -316,7 +334,9 @@ int engram_debug_barrier_skew(engram_t* h, int64_t delta);
  * A stream capture of start / forward / join on one stream records the side
  * stream's work into the graph. */
 typedef struct engram_prefetch engram_prefetch_t;
-int engram_prefetch_create(engram_t* const* layers, int32_t n_layers, engram_prefetch_t** out);
+#define ENGRAM_PREFETCH_WKV 1  /* flags: also run each layer's wkv on the side stream */
+int engram_prefetch_create(engram_t* const* layers, int32_t n_layers, int32_t flags,
+                           engram_prefetch_t** out);
 int engram_prefetch_destroy(engram_prefetch_t* p);
 int engram_prefetch_start(engram_prefetch_t* p, const int32_t* const* hash_ids,
                           const int64_t* ids_row_stride, int64_t T, int background,

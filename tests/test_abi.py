@@ -78,10 +78,12 @@ def test_null_handle_arguments_are_rejected_without_a_gpu(lib):
 def test_prefetch_arguments_are_rejected_without_a_gpu(lib):
     out = ctypes.c_void_p()
     none = (ctypes.c_void_p * 2)(None, None)
-    assert lib.engram_prefetch_create(None, 1, ctypes.byref(out)) == -1
-    assert lib.engram_prefetch_create(none, 0, ctypes.byref(out)) == -1
-    assert lib.engram_prefetch_create(none, 2, ctypes.byref(out)) == -1  # null handles
-    assert lib.engram_prefetch_create(none, 2, None) == -1
+    assert lib.engram_prefetch_create(None, 1, 0, ctypes.byref(out)) == -1
+    assert lib.engram_prefetch_create(none, 0, 0, ctypes.byref(out)) == -1
+    assert lib.engram_prefetch_create(none, 2, 2, ctypes.byref(out)) == -1  # unknown flag
+    assert lib.engram_prefetch_create(none, 2, 0, ctypes.byref(out)) == -1  # null handles
+    assert lib.engram_prefetch_create(none, 2, 0, None) == -1
+    assert lib.engram_wkv(None, None, 0, None, 0, 1, None) == -1
     assert out.value is None
     st = (ctypes.c_int64 * 3)(0, 0, 1)
     assert lib.engram_prefetch_start(None, none, st, 1, 1, None) == -1

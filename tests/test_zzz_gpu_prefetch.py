@@ -7,9 +7,13 @@ also compared with the oracle.  Ordering is tested directly: the hash ids
 are written on the caller's stream behind a spin of a few milliseconds, so
 lookups that did not wait for the caller's stream would gather stale ids.
 Also covered: join and the plain fallback, and a CUDA-graph capture of a
-whole prefetched step.  Runs after the other GPU tests (file order)."""
+whole prefetched step.  The wkv mode (engram_wkv: the projection alone, in
+bf16, ahead on the side stream; the layer then runs only the gate and
+residual) is checked against the oracle's kv and outputs.  Runs after the
+other GPU tests (file order)."""
 import dataclasses
 
+import numpy as np
 import pytest
 import torch
 
@@ -153,5 +157,108 @@ def test_graph_capture_of_a_prefetched_step(cases):
             torch.cuda.synchronize()
             for l in range(3):
                 assert _same(outs[l], ref[l]), l
+    finally:
+        pf.close()
+
+
+# ---------------------------------------------------------------- wkv mode
+
+def _kv_close(kv_gpu, kv_ref):
+    """bf16 kv against the oracle's fp64 kv: the kernel rounds an fp32 sum,
+    so at most one bf16 rounding (2^-8 relative) plus fp32 summation error."""
+    got = kv_gpu.float().cpu().numpy().astype(np.float64)
+    scale = np.abs(kv_ref).max()
+    assert np.all(np.abs(got - kv_ref) <= 2.0 ** -8 * np.abs(kv_ref) + 1e-5 * scale)
+
+
+@pytest.mark.parametrize("T", [1, 16, 100])
+def test_wkv_matches_the_oracle_kv(cases, T):
+    c = cases[0]
+    inp = c.step_inputs(T=T, step=31 + T)
+    kv = c.layer.wkv(inp["hash_ids"])
+    torch.cuda.synchronize()
+    _kv_close(kv, c.oracle(inp)["kv"])
+    # the rows it staged serve a later forward
+    out = c.layer.forward(inp["hidden"], None, inp["token_mask"])
+    ref = c.layer.forward(inp["hidden"], inp["hash_ids"], inp["token_mask"])
+    torch.cuda.synchronize()
+    assert _same(out, ref)
+
+
+def test_wkv_decode_configuration():
+    c = Case(W.DECODE, max_tokens=64)
+    try:
+        inp = c.step_inputs()
+        kv = c.layer.wkv(inp["hash_ids"])
+        torch.cuda.synchronize()
+        _kv_close(kv, c.oracle(inp)["kv"])
+        assert c.layer.device_error() == 0
+    finally:
+        c.layer.close()
+
+
+def test_wkv_mxfp8():
+    wl = dataclasses.replace(W.TINY_MXFP8, name="tiny_mx_pf", seed=1311)
+    c = Case(wl, max_tokens=128)
+    try:
+        inp = c.step_inputs(T=40, step=3)
+        kv = c.layer.wkv(inp["hash_ids"])
+        torch.cuda.synchronize()
+        _kv_close(kv, c.oracle(inp, quantize_act=True)["kv"])
+    finally:
+        c.layer.close()
+
+
+@pytest.mark.parametrize("T", [16, 300])  # wkv ahead / beyond the fused range: lookups only
+def test_prefetch_wkv_mode(cases, T):
+    inps = _inputs(cases, T, step=40 + T)
+    ref = _plain(cases, inps)
+    pf = EngramPrefetch([c.layer for c in cases], wkv=True)
+    try:
+        pf.start([i["hash_ids"] for i in inps])
+        outs = [pf.forward(l, inps[l]["hidden"], None, inps[l]["token_mask"]) for l in (1, 2, 0)]
+        outs = [outs[2], outs[0], outs[1]]
+        torch.cuda.synchronize()
+        for l, c in enumerate(cases):
+            if T > 256:  # the plain path, bit for bit
+                assert _same(outs[l], ref[l]), l
+            # kv in bf16 before the gate: the value is rounded as in the
+            # prefill tiles
+            compare(c, inps[l], outs[l], c.oracle(inps[l]), value_rtol=2.0 ** -8 + 1e-3)
+            assert c.layer.device_error() == 0
+    finally:
+        pf.close()
+
+
+def test_graph_capture_of_the_wkv_mode(cases):
+    T = 16
+    inps = _inputs(cases, T, step=57)
+    pf = EngramPrefetch([c.layer for c in cases], wkv=True)
+    try:
+        s = torch.cuda.Stream()
+        outs = [torch.empty_like(i["hidden"]) for i in inps]
+        ids = [i["hash_ids"] for i in inps]
+
+        def step():
+            pf.start(ids, stream=s)
+            for l in range(3):
+                pf.forward(l, inps[l]["hidden"], None, inps[l]["token_mask"], out=outs[l],
+                           stream=s)
+
+        s.wait_stream(torch.cuda.current_stream())
+        with torch.cuda.stream(s):
+            step()
+        s.synchronize()
+        first = [o.clone() for o in outs]
+        g = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(g, stream=s):
+            step()
+        for _ in range(3):
+            for o in outs:
+                o.zero_()
+            g.replay()
+            torch.cuda.synchronize()
+            for l in range(3):
+                assert _same(outs[l], first[l]), l
     finally:
         pf.close()
