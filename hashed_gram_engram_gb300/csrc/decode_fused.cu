@@ -119,6 +119,7 @@ struct FusedArgs {
     float eps, clamp, inv_d, inv_sqrt_d;
     unsigned* err;
     uint32_t x_off, qk_off, bar_off;
+    int hv8;  // hidden rows and strides 32-byte aligned: 32-byte loads
 };
 
 __device__ __forceinline__ int first_granule(int cta, int n, int G) {
@@ -547,8 +548,12 @@ __global__ void __launch_bounds__(kThreads, 1)
                     const int n0 = k0 + ci * 16;
                     const int h = n0 / a.D, d0 = n0 - h * a.D;
                     const uint16_t* hp = a.hidden + t * a.hs_t + h * a.hs_h + d0;
-                    hv[2 * ci] = ld_nc_v4(hp);
-                    hv[2 * ci + 1] = ld_nc_v4(hp + 8);
+                    if (a.hv8) {
+                        ld_nc_v8(hp, hv[2 * ci], hv[2 * ci + 1]);
+                    } else {
+                        hv[2 * ci] = ld_nc_v4(hp);
+                        hv[2 * ci + 1] = ld_nc_v4(hp + 8);
+                    }
                 }
             }
             if (m == 0) {
@@ -914,6 +919,10 @@ FusedSmem fused_smem(const FusedLayout& L, const FusedPlan& p, bool mx) {
     m.x_off = static_cast<uint32_t>(stages) * m.w_stage_bytes;
     m.qk_off = m.x_off + m.x_ring;
     m.bar_off = m.qk_off + qk_bytes;
+    // after barrier 2 the q*k area holds the gates of the tokens a CTA's
+    // residual items touch
+    const int nb = L.VG * 16 / 256, items = (p.Tn * nb + L.grid - 1) / L.grid;
+    if ((items / (nb > 0 ? nb : 1) + 2) * kMaxCopies > kMaxFusedSlice) m.ok = false;
     return m;
 }
 
@@ -1001,6 +1010,9 @@ cudaError_t launch_decode_fused(engram_handle* h, const void* hidden, const int6
     a.hidden = static_cast<const uint16_t*>(hidden);
     a.hs_t = hs != nullptr ? hs[0] : 0;
     a.hs_h = hs != nullptr ? hs[1] : 0;
+    // (key runs start on 16-dim granules, so aligned rows keep 32-byte loads aligned)
+    a.hv8 = (reinterpret_cast<uintptr_t>(hidden) % 32 == 0 && a.hs_t % 16 == 0 &&
+             a.hs_h % 16 == 0) ? 1 : 0;
     a.out = static_cast<uint16_t*>(out);
     a.os_t = os != nullptr ? os[0] : 0;
     a.os_h = os != nullptr ? os[1] : 0;

@@ -441,6 +441,14 @@ __device__ __forceinline__ uint4 ld_nc_v4(const void* p) {
 }
 
 // Streaming read: no L1 allocation (rows of a huge table are touched once).
+// 32 bytes (two 16-byte halves) through the read-only path; p 32-byte aligned.
+__device__ __forceinline__ void ld_nc_v8(const void* p, uint4& lo, uint4& hi) {
+    asm volatile("ld.global.nc.v8.b32 {%0, %1, %2, %3, %4, %5, %6, %7}, [%8];"
+                 : "=r"(lo.x), "=r"(lo.y), "=r"(lo.z), "=r"(lo.w), "=r"(hi.x), "=r"(hi.y),
+                   "=r"(hi.z), "=r"(hi.w)
+                 : "l"(p));
+}
+
 __device__ __forceinline__ uint4 ld_stream_v4(const void* p) {
     uint4 v;
     asm volatile("ld.global.nc.L1::no_allocate.v4.u32 {%0, %1, %2, %3}, [%4];"

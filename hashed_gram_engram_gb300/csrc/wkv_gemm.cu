@@ -62,6 +62,7 @@ struct GemmArgs {
     const uint8_t* sfa;  // MXFP8: scale atoms of the staged codes
     const uint8_t* sfb;  // MXFP8: scale atoms of wkv
     unsigned* err;
+    int hv8;  // hidden rows and strides 32-byte aligned: 32-byte loads
 };
 
 struct Unit {
@@ -304,10 +305,18 @@ __global__ void __launch_bounds__(threads_for(kMx), 1)
                 if (h < a.H) {
                     uint4 hv[kHalfCh * 4];
                     const uint16_t* hp = a.hidden + t * a.hs_t + h * a.hs_h + d0 + c0;
+                    if (a.hv8) {  // half the load instructions
 #pragma unroll
-                    for (int i = 0; i < kHalfCh * 4; ++i)
-                        hv[i] = (live && c0 + 8 * i < BN) ? ld_nc_v4(hp + 8 * i)
-                                                          : make_uint4(0, 0, 0, 0);
+                        for (int i = 0; i < kHalfCh * 4; i += 2) {
+                            hv[i] = hv[i + 1] = make_uint4(0, 0, 0, 0);
+                            if (live && c0 + 8 * i < BN) ld_nc_v8(hp + 8 * i, hv[i], hv[i + 1]);
+                        }
+                    } else {
+#pragma unroll
+                        for (int i = 0; i < kHalfCh * 4; ++i)
+                            hv[i] = (live && c0 + 8 * i < BN) ? ld_nc_v4(hp + 8 * i)
+                                                              : make_uint4(0, 0, 0, 0);
+                    }
                     if (!mbar_wait(&tfull[acc], apar, abort_v)) {
                         ok = false;
                         break;
@@ -324,9 +333,14 @@ __global__ void __launch_bounds__(threads_for(kMx), 1)
                         tmem_ld_wait();
 #pragma unroll
                         for (int j = 0; j < 32; j += 8) {
-                            const float4 q0 = __ldg(reinterpret_cast<const float4*>(qkp + c + j));
-                            const float4 q1 = __ldg(reinterpret_cast<const float4*>(qkp + c + j + 4));
-                            const float qk[8] = {q0.x, q0.y, q0.z, q0.w, q1.x, q1.y, q1.z, q1.w};
+                            // eight q*k values in one 32-byte load (one address for
+                            // the whole warp; 32-byte aligned: tiles start on 32 dims)
+                            uint4 q0, q1;
+                            ld_nc_v8(qkp + c + j, q0, q1);
+                            const float qk[8] = {__uint_as_float(q0.x), __uint_as_float(q0.y),
+                                                 __uint_as_float(q0.z), __uint_as_float(q0.w),
+                                                 __uint_as_float(q1.x), __uint_as_float(q1.y),
+                                                 __uint_as_float(q1.z), __uint_as_float(q1.w)};
                             const uint4 hw = hv[(c + j) / 8];
                             const uint32_t w[4] = {hw.x, hw.y, hw.z, hw.w};
 #pragma unroll
@@ -459,12 +473,13 @@ cudaError_t gemm_setup_attributes() {
     return cudaSuccess;
 }
 
-static cudaError_t launch(const void* fn, int grid, int threads, const CUtensorMap& tmA,
-                          const CUtensorMap& tmB, const GemmArgs& a, cudaStream_t s, bool pdl) {
+static cudaError_t launch(const void* fn, int grid, int threads, uint32_t smem_bytes,
+                          const CUtensorMap& tmA, const CUtensorMap& tmB, const GemmArgs& a,
+                          cudaStream_t s, bool pdl) {
     cudaLaunchConfig_t cfg = {};
     cfg.gridDim = dim3(static_cast<unsigned>(grid));
     cfg.blockDim = dim3(static_cast<unsigned>(threads));
-    cfg.dynamicSmemBytes = kGemmSmemBytes;
+    cfg.dynamicSmemBytes = smem_bytes;
     cfg.stream = s;
     cudaLaunchAttribute attr[1];
     attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
@@ -510,6 +525,10 @@ cudaError_t launch_wkv_tokens_m(const engram_handle* h, const void* hidden, int6
     a.hidden = static_cast<const uint16_t*>(hidden);
     a.hs_t = hs_t;
     a.hs_h = hs_h;
+    // tile starts are multiples of 128 dims, so rows at 32-byte aligned
+    // addresses keep every 32-byte load aligned
+    a.hv8 = (reinterpret_cast<uintptr_t>(hidden) % 32 == 0 && hs_t % 16 == 0 && hs_h % 16 == 0)
+                ? 1 : 0;
     a.qk = h->ws.qk;
     a.partials = h->ws.partials;
     a.value = h->ws.value;
@@ -522,7 +541,10 @@ cudaError_t launch_wkv_tokens_m(const engram_handle* h, const void* hidden, int6
             : (bn == kBNPrefillMxWide
                    ? reinterpret_cast<const void*>(wkv_gemm_kernel<true, kBNPrefillMxWide>)
                    : reinterpret_cast<const void*>(wkv_gemm_kernel<true, kBNPrefillMx>));
-    return launch(fn, grid, threads_for(mx), h->tm_act_m, h->tm_w_n, a, s, pdl);
+    // the shared memory the stages and barriers need, and no more: the
+    // epilogue's loads go through the L1 that shares the SM's memory
+    const uint32_t smem_bytes = static_cast<uint32_t>(a.stages) * stride + 2048u;
+    return launch(fn, grid, threads_for(mx), smem_bytes, h->tm_act_m, h->tm_w_n, a, s, pdl);
 }
 
 }  // namespace engram

@@ -121,6 +121,36 @@ def test_in_place_and_strided_views(tiny):
     assert torch.equal(h2.view(torch.int16), ov.contiguous().view(torch.int16))
 
 
+def test_prefill_path_views(tiny):
+    """The prefill kernels (T > 256) on strided, broadcast and in-place views:
+    padded copies and tokens (hidden staged by TMA boxes), copies broadcast
+    with a zero stride (a view TMA cannot describe: the GEMM's plain-load
+    instance), and out = hidden."""
+    T = 600
+    inp = tiny.step_inputs(T=T, step=13)
+    ref = tiny.oracle(inp)
+    H, D = W.TINY.hc_mult, W.TINY.dim
+    big = torch.zeros((T + 3, H + 1, D + 64), dtype=torch.bfloat16, device="cuda")
+    big[:T, :H, :D] = inp["hidden"]
+    hv = big[:T, :H, :D]
+    out = tiny.layer.forward(hv, inp["hash_ids"], inp["token_mask"])
+    torch.cuda.synchronize()
+    compare(tiny, inp, out, ref, value_rtol=2.0 ** -8 + 1e-3)
+    # copies broadcast from one row per token
+    hb = inp["hidden"][:, 0, :].clone()[:, None, :].expand(T, H, D)
+    assert hb.stride(1) == 0
+    inp_b = dict(inp, hidden=hb)
+    out_b = tiny.layer.forward(hb, inp["hash_ids"], inp["token_mask"])
+    torch.cuda.synchronize()
+    compare(tiny, inp_b, out_b, tiny.oracle(inp_b), value_rtol=2.0 ** -8 + 1e-3)
+    # in place
+    h2 = inp["hidden"].clone()
+    tiny.layer.forward(h2, inp["hash_ids"], inp["token_mask"], out=h2)
+    torch.cuda.synchronize()
+    assert torch.equal(h2.view(torch.int16), out.view(torch.int16))
+    assert tiny.layer.device_error() == 0
+
+
 def test_strided_hash_ids(tiny):
     T = 70
     inp = tiny.step_inputs(T=T, step=12)
