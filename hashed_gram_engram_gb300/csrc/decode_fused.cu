@@ -722,32 +722,56 @@ __global__ void __launch_bounds__(kThreads, 1)
             for (int h = 0; h < kMaxCopies; ++h)
                 if (h < a.H) x[h] = ld_nc_v4(a.hidden + t0 * a.hs_t + h * a.hs_h + d0);
         }
-        for (int r = warp; r < ntok * a.H; r += kWarps) {
-            const int t = tok0 + r / a.H, h = r - (r / a.H) * a.H;
-            const float4* rr = a.rec + a.rec_base[h] + static_cast<int64_t>(t) * a.nh[h];
-            float s_hh = 0.f, s_kk = 0.f, s_hk = 0.f;
-            for (int j = lane; j < a.nh[h]; j += 32) {
-                const float4 v = __ldcg(rr + j);
-                s_hh += v.x;
-                s_kk += v.y;
-                s_hk += v.z;
+        // (two rows per warp at a time, their records loaded together, so a
+        // CTA whose items touch two tokens still takes one round trip)
+        for (int r0 = warp; r0 < ntok * a.H; r0 += 2 * kWarps) {
+            float acc[2][3] = {{0.f, 0.f, 0.f}, {0.f, 0.f, 0.f}};
+            const int nrow = r0 + kWarps < ntok * a.H ? 2 : 1;
+            const float4* rr[2];
+            int nhr[2], tr[2], hr_[2];
+#pragma unroll
+            for (int k = 0; k < 2; ++k) {
+                const int r = r0 + k * kWarps;
+                tr[k] = tok0 + (k < nrow ? r / a.H : 0);
+                hr_[k] = k < nrow ? r - (r / a.H) * a.H : 0;
+                nhr[k] = k < nrow ? a.nh[hr_[k]] : 0;
+                rr[k] = a.rec + a.rec_base[hr_[k]] + static_cast<int64_t>(tr[k]) * nhr[k];
+            }
+            const int nmax = nhr[0] > nhr[1] ? nhr[0] : nhr[1];
+            for (int j = lane; j < nmax; j += 32) {
+                float4 v[2];
+#pragma unroll
+                for (int k = 0; k < 2; ++k)
+                    v[k] = j < nhr[k] ? __ldcg(rr[k] + j) : make_float4(0.f, 0.f, 0.f, 0.f);
+#pragma unroll
+                for (int k = 0; k < 2; ++k) {
+                    if (j >= nhr[k]) continue;
+                    acc[k][0] += v[k].x;
+                    acc[k][1] += v[k].y;
+                    acc[k][2] += v[k].z;
+                }
             }
 #pragma unroll
-            for (int o = 16; o > 0; o >>= 1) {
-                s_hh += __shfl_xor_sync(0xFFFFFFFFu, s_hh, o);
-                s_kk += __shfl_xor_sync(0xFFFFFFFFu, s_kk, o);
-                s_hk += __shfl_xor_sync(0xFFFFFFFFu, s_hk, o);
-            }
-            if (lane == 0) {
-                const bool active = a.mask == nullptr || a.mask[t] != 0;
-                const float hr = 1.0f / sqrtf(s_hh * a.inv_d + a.eps);
-                const float kr = 1.0f / sqrtf(s_kk * a.inv_d + a.eps);
-                const float dot = s_hk * hr * kr * a.inv_sqrt_d;
-                float gi = sqrtf(fmaxf(fabsf(dot), a.clamp));
-                if (dot < 0.0f) gi = -gi;
-                const float g = active ? 1.0f / (1.0f + expf(-gi)) : 0.0f;
-                gate_s[r] = g;
-                a.gate_out[t * a.H + h] = g;  // (CTAs sharing a token write the same bits)
+            for (int k = 0; k < 2; ++k) {
+                float s_hh = acc[k][0], s_kk = acc[k][1], s_hk = acc[k][2];
+#pragma unroll
+                for (int o = 16; o > 0; o >>= 1) {
+                    s_hh += __shfl_xor_sync(0xFFFFFFFFu, s_hh, o);
+                    s_kk += __shfl_xor_sync(0xFFFFFFFFu, s_kk, o);
+                    s_hk += __shfl_xor_sync(0xFFFFFFFFu, s_hk, o);
+                }
+                if (lane == 0 && k < nrow) {
+                    const int t = tr[k], h = hr_[k];
+                    const bool active = a.mask == nullptr || a.mask[t] != 0;
+                    const float hr = 1.0f / sqrtf(s_hh * a.inv_d + a.eps);
+                    const float kr = 1.0f / sqrtf(s_kk * a.inv_d + a.eps);
+                    const float dot = s_hk * hr * kr * a.inv_sqrt_d;
+                    float gi = sqrtf(fmaxf(fabsf(dot), a.clamp));
+                    if (dot < 0.0f) gi = -gi;
+                    const float g = active ? 1.0f / (1.0f + expf(-gi)) : 0.0f;
+                    gate_s[r0 + k * kWarps] = g;
+                    a.gate_out[t * a.H + h] = g;  // (CTAs sharing a token write the same bits)
+                }
             }
         }
         __syncthreads();
