@@ -310,6 +310,7 @@ int engram_create(const engram_config* cfg, const engram_weights* w, engram_t** 
     const int elem = mx ? 1 : 2;
     const void* act = mx ? static_cast<const void*>(ws.staged_q) : static_cast<const void*>(ws.staged);
     bool ok = make_map(&h->tm_w_n, h->wkv, dt, elem, K, N, prefill_bn(h)) &&
+              make_map(&h->tm_w_half, h->wkv, dt, elem, K, N, prefill_bn(h) / 2) &&
               make_map(&h->tm_act_m, act, dt, elem, K, ws.rows_alloc, kBM);
     for (int i = 0; i < 16 && ok; ++i)
         ok = make_map(&h->tm_act_n[i], act, dt, elem, K, ws.rows_alloc, 16 * (i + 1));
@@ -317,6 +318,7 @@ int engram_create(const engram_config* cfg, const engram_weights* w, engram_t** 
         free_handle(h);
         return ENGRAM_ERR_CUDA;
     }
+    h->gemm_pair_clusters = gemm_pair_capacity(h);
     *out = h;
     return ENGRAM_OK;
 }

@@ -110,6 +110,8 @@ struct engram_handle {
     engram::Workspace ws;
     // TMA descriptors
     CUtensorMap tm_w_n;        // wkv, prefill B operand (box BN rows x 128 bytes)
+    CUtensorMap tm_w_half;     // the same, box BN/2 rows (a CTA's half in a CTA-pair GEMM)
+    int gemm_pair_clusters;    // CTA-pair GEMM clusters that fit at once (0: single CTAs)
     CUtensorMap tm_act_m;      // staged rows (bf16, or e4m3 codes), box 128 rows x 128 bytes
     CUtensorMap tm_act_n[16];  // the same, box 16 * (i + 1) rows (the fused kernel's tile)
     engram::FusedLayout fused;
@@ -135,6 +137,7 @@ cudaError_t launch_wkv_tokens_m(const engram_handle* h, const void* hidden, int6
                                 int64_t hs_h, int64_t T, cudaStream_t s, bool pdl);
 cudaError_t gemm_setup_attributes();
 int prefill_bn(const engram_handle* h);  // kv columns per prefill tile
+int gemm_pair_capacity(const engram_handle* h);
 cudaError_t pack_scale_atoms(const engram_handle* h, cudaStream_t s);
 cudaError_t launch_unpack_scales(const engram_handle* h, uint8_t* out, int64_t T, cudaStream_t s);
 

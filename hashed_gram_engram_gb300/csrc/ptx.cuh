@@ -50,6 +50,37 @@ __device__ __forceinline__ void mbar_arrive_expect_tx(uint64_t* bar, uint32_t by
         : "memory");
 }
 
+// ---------------------------------------------------------------- cluster
+// This CTA's rank in its cluster.
+__device__ __forceinline__ uint32_t cluster_ctarank() {
+    uint32_t r;
+    asm volatile("mov.u32 %0, %%cluster_ctarank;" : "=r"(r));
+    return r;
+}
+
+// A barrier over every thread of the cluster: shared-memory writes and
+// barrier initialisations before it are visible to the other CTAs after it.
+__device__ __forceinline__ void cluster_sync() {
+    asm volatile(
+        "barrier.cluster.arrive.release.aligned;\n\t"
+        "barrier.cluster.wait.acquire.aligned;" ::: "memory");
+}
+
+// The shared::cluster address of the variable at `p`'s offset in the shared
+// memory of cluster CTA `rank`.
+__device__ __forceinline__ uint32_t cluster_addr(const void* p, uint32_t rank) {
+    uint32_t r;
+    asm volatile("mapa.shared::cluster.u32 %0, %1, %2;" : "=r"(r) : "r"(smem_addr(p)), "r"(rank));
+    return r;
+}
+
+// Arrive on an mbarrier given by its shared::cluster address (possibly in
+// another CTA), releasing this thread's earlier work at cluster scope.
+__device__ __forceinline__ void mbar_arrive_cluster(uint32_t bar_cluster) {
+    asm volatile("mbarrier.arrive.release.cluster.shared::cluster.b64 _, [%0];" ::"r"(bar_cluster)
+                 : "memory");
+}
+
 __device__ __forceinline__ uint32_t mbar_try_wait(uint64_t* bar, uint32_t parity) {
     uint32_t done;
     asm volatile(
@@ -62,15 +93,32 @@ __device__ __forceinline__ uint32_t mbar_try_wait(uint64_t* bar, uint32_t parity
     return done;
 }
 
+// The same test with acquire semantics at cluster scope: the phase was
+// completed by arrivals of threads of another CTA of the cluster, whose
+// earlier work must be visible after it.
+__device__ __forceinline__ uint32_t mbar_try_wait_cluster(uint64_t* bar, uint32_t parity) {
+    uint32_t done;
+    asm volatile(
+        "{\n\t.reg .pred p;\n\t"
+        "mbarrier.try_wait.parity.acquire.cluster.shared::cta.b64 p, [%1], %2;\n\t"
+        "selp.u32 %0, 1, 0, p;\n\t}"
+        : "=r"(done)
+        : "r"(smem_addr(bar)), "r"(parity)
+        : "memory");
+    return done;
+}
+
 // Wait for the phase of `bar` with the given parity to complete.  Returns
 // false when the wall-clock or iteration limit runs out, or when `abort`
-// (shared memory, may be null) becomes non-zero.
+// (shared memory, may be null) becomes non-zero.  `cluster`: acquire at
+// cluster scope (arrivals from another CTA).
 __device__ __forceinline__ bool mbar_wait(uint64_t* bar, uint32_t parity,
-                                          const volatile int* abort) {
-    if (mbar_try_wait(bar, parity)) return true;
+                                          const volatile int* abort, bool cluster = false) {
+    auto test = [&]() { return cluster ? mbar_try_wait_cluster(bar, parity) : mbar_try_wait(bar, parity); };
+    if (test()) return true;
     const uint64_t t0 = globaltimer_ns();
     for (uint32_t i = 1; i < kWaitLimitIters; ++i) {
-        if (mbar_try_wait(bar, parity)) return true;
+        if (test()) return true;
         if ((i & 31u) == 0) {
             if (abort != nullptr && *abort) return false;
             if (globaltimer_ns() - t0 > kWaitLimitNs) return false;
@@ -122,6 +170,29 @@ __device__ __forceinline__ void tma_load_2d_hint(void* dst, const CUtensorMap* m
         ".L2::cache_hint [%0], [%1, {%3, %4}], [%2], %5;" ::"r"(smem_addr(dst)),
         "l"(reinterpret_cast<uint64_t>(map)), "r"(smem_addr(bar)), "r"(c0), "r"(c1),
         "l"(policy)
+        : "memory");
+}
+
+// A 2D box into this CTA's shared memory whose completion (transaction
+// bytes) lands on the mbarrier at `bar_cluster`, a shared::cluster address
+// in this CTA or its peer of the CTA pair (the pair's MMA issuer waits
+// there for both CTAs' operands).
+__device__ __forceinline__ void tma_load_2d_pair(void* dst, const CUtensorMap* map,
+                                                 uint32_t bar_cluster, int32_t c0, int32_t c1) {
+    asm volatile(
+        "cp.async.bulk.tensor.2d.cta_group::2.shared::cluster.global.mbarrier::complete_tx::bytes"
+        " [%0], [%1, {%3, %4}], [%2];" ::"r"(smem_addr(dst)),
+        "l"(reinterpret_cast<uint64_t>(map)), "r"(bar_cluster), "r"(c0), "r"(c1)
+        : "memory");
+}
+
+__device__ __forceinline__ void tma_load_2d_pair_hint(void* dst, const CUtensorMap* map,
+                                                      uint32_t bar_cluster, int32_t c0, int32_t c1,
+                                                      uint64_t policy) {
+    asm volatile(
+        "cp.async.bulk.tensor.2d.cta_group::2.shared::cluster.global.mbarrier::complete_tx::bytes"
+        ".L2::cache_hint [%0], [%1, {%3, %4}], [%2], %5;" ::"r"(smem_addr(dst)),
+        "l"(reinterpret_cast<uint64_t>(map)), "r"(bar_cluster), "r"(c0), "r"(c1), "l"(policy)
         : "memory");
 }
 
@@ -270,20 +341,39 @@ __device__ __forceinline__ uint64_t policy_evict_last() {
 
 // ---------------------------------------------------------------- tcgen05
 // TMEM allocation is warp-wide (.sync.aligned): the whole warp must call.
+// G = 2 (a CTA pair sharing MMAs): one warp of each CTA of the pair calls,
+// and the pair gets the same columns.  Every tcgen05 instruction of a
+// kernel uses the same G.
+template <int G = 1>
 __device__ __forceinline__ void tmem_alloc(uint32_t* dst_smem, uint32_t ncols) {
-    asm volatile("tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(
-                     smem_addr(dst_smem)),
-                 "r"(ncols)
-                 : "memory");
+    if constexpr (G == 2)
+        asm volatile("tcgen05.alloc.cta_group::2.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(
+                         smem_addr(dst_smem)),
+                     "r"(ncols)
+                     : "memory");
+    else
+        asm volatile("tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(
+                         smem_addr(dst_smem)),
+                     "r"(ncols)
+                     : "memory");
 }
 
+template <int G = 1>
 __device__ __forceinline__ void tmem_relinquish() {
-    asm volatile("tcgen05.relinquish_alloc_permit.cta_group::1.sync.aligned;" ::: "memory");
+    if constexpr (G == 2)
+        asm volatile("tcgen05.relinquish_alloc_permit.cta_group::2.sync.aligned;" ::: "memory");
+    else
+        asm volatile("tcgen05.relinquish_alloc_permit.cta_group::1.sync.aligned;" ::: "memory");
 }
 
+template <int G = 1>
 __device__ __forceinline__ void tmem_dealloc(uint32_t taddr, uint32_t ncols) {
-    asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;" ::"r"(taddr), "r"(ncols)
-                 : "memory");
+    if constexpr (G == 2)
+        asm volatile("tcgen05.dealloc.cta_group::2.sync.aligned.b32 %0, %1;" ::"r"(taddr), "r"(ncols)
+                     : "memory");
+    else
+        asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;" ::"r"(taddr), "r"(ncols)
+                     : "memory");
 }
 
 __device__ __forceinline__ void tc_fence_before() {
@@ -301,6 +391,20 @@ __device__ __forceinline__ void mma_bf16_ss(uint32_t d_tmem, uint64_t adesc, uin
         "{\n\t.reg .pred p;\n\t"
         "setp.ne.b32 p, %4, 0;\n\t"
         "tcgen05.mma.cta_group::1.kind::f16 [%0], %1, %2, %3, p;\n\t}" ::"r"(d_tmem),
+        "l"(adesc), "l"(bdesc), "r"(idesc), "r"(accumulate)
+        : "memory");
+}
+
+// The CTA pair's MMA (issued by the even CTA): A = 2 x 128 rows, one half
+// in each CTA's shared memory at the descriptor's offset; B = N rows, the
+// first N/2 in the issuer's shared memory, the rest in the peer's; D rows
+// 0..127 in the issuer's TMEM, 128..255 in the peer's, at d_tmem.
+__device__ __forceinline__ void mma_bf16_ss_pair(uint32_t d_tmem, uint64_t adesc, uint64_t bdesc,
+                                                 uint32_t idesc, uint32_t accumulate) {
+    asm volatile(
+        "{\n\t.reg .pred p;\n\t"
+        "setp.ne.b32 p, %4, 0;\n\t"
+        "tcgen05.mma.cta_group::2.kind::f16 [%0], %1, %2, %3, p;\n\t}" ::"r"(d_tmem),
         "l"(adesc), "l"(bdesc), "r"(idesc), "r"(accumulate)
         : "memory");
 }
@@ -325,6 +429,23 @@ __device__ __forceinline__ void mma_commit(uint64_t* bar) {
     asm volatile(
         "tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];" ::"r"(
             smem_addr(bar))
+        : "memory");
+}
+
+// Pair forms: arrive once the pair's earlier MMAs issued by this thread
+// have completed, on the mbarrier at bar's offset in this CTA (commit_pair)
+// or in every CTA of cta_mask (commit_pair_mc).
+__device__ __forceinline__ void mma_commit_pair(uint64_t* bar) {
+    asm volatile(
+        "tcgen05.commit.cta_group::2.mbarrier::arrive::one.shared::cluster.b64 [%0];" ::"r"(
+            smem_addr(bar))
+        : "memory");
+}
+
+__device__ __forceinline__ void mma_commit_pair_mc(uint64_t* bar, uint16_t cta_mask) {
+    asm volatile(
+        "tcgen05.commit.cta_group::2.mbarrier::arrive::one.shared::cluster.multicast::cluster.b64"
+        " [%0], %1;" ::"r"(smem_addr(bar)), "h"(cta_mask)
         : "memory");
 }
 

@@ -70,16 +70,28 @@ struct Unit {
 };
 
 // Tiles of this CTA in order: blockIdx.x, blockIdx.x + gridDim.x, ...
+// CTA pairs (kPair): the unit is 256 tokens x BN columns, pair k (CTAs 2k,
+// 2k + 1, one cluster) takes units k, k + gridDim.x / 2, ..., and CTA rank r
+// of the pair holds token tile 2i + r of unit (i, n).  When the token tiles
+// are odd in number the last pair's second tile lies past T (rows the
+// staging buffer holds, padded to 256; the epilogue skips them).
+template <bool kPair>
 struct Schedule {
     const GemmArgs& a;
-    int64_t cur, end;
+    int64_t cur, end, step;
+    int rank;
     __device__ explicit Schedule(const GemmArgs& args)
-        : a(args), cur(blockIdx.x), end(static_cast<int64_t>(args.m_tiles) * args.n_tiles) {}
+        : a(args),
+          cur(kPair ? blockIdx.x >> 1 : blockIdx.x),
+          end(static_cast<int64_t>(kPair ? (args.m_tiles + 1) / 2 : args.m_tiles) * args.n_tiles),
+          step(kPair ? gridDim.x >> 1 : gridDim.x),
+          rank(kPair ? static_cast<int>(blockIdx.x & 1u) : 0) {}
     __device__ bool next(Unit& u) {
         if (cur >= end) return false;
-        u.m = static_cast<int>(cur / a.n_tiles);
+        const int mi = static_cast<int>(cur / a.n_tiles);
+        u.m = kPair ? 2 * mi + rank : mi;
         u.n = static_cast<int>(cur % a.n_tiles);
-        cur += gridDim.x;
+        cur += step;
         return true;
     }
 };
@@ -89,17 +101,26 @@ __device__ __forceinline__ void fail(int* abort_flag, unsigned* err) {
     atomicOr(err, ENGRAM_DEVERR_TIMEOUT);
 }
 
-template <bool kMx, int BN>
+// kPair (bf16): CTA pairs of one cluster share each MMA (tcgen05
+// cta_group::2, M = 256): each CTA's shared memory holds its 128 token rows
+// and half of the tile's BN weight rows (tmBh: boxes of BN/2 rows), so a
+// CTA loads 2/3 of the operand bytes of an unpaired 128 x BN tile for the
+// same MMA work.  The even CTA issues the MMAs; its full barriers count
+// both CTAs' copies; its commits reach both CTAs' empty and tfull barriers;
+// both CTAs' epilogues release its tempty barriers.
+template <bool kMx, int BN, bool kPair>
 __global__ void __launch_bounds__(threads_for(kMx), 1)
     wkv_gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
-                    const GemmArgs a) {
+                    const __grid_constant__ CUtensorMap tmBh, const GemmArgs a) {
+    static_assert(!(kPair && kMx), "CTA pairs: bf16 weights only");
+    constexpr int G = kPair ? 2 : 1;  // tcgen05 CTA group
     constexpr int kKElems = kMx ? 128 : 64;  // k per 128-byte block
     constexpr uint32_t kBAtoms = (BN + 127) / 128;  // weight scale atoms per k-block
     constexpr uint32_t kAtoms = kMx ? 512u * (1u + kBAtoms) : 0u;  // scale atoms per stage
     extern __shared__ uint8_t smem_raw[];
     uint8_t* smem = reinterpret_cast<uint8_t*>(
         (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~static_cast<uintptr_t>(1023));
-    const uint32_t tx_bytes = a.a_bytes + a.b_bytes + kAtoms;  // copied per stage
+    const uint32_t tx_bytes = a.a_bytes + a.b_bytes + kAtoms;  // copied per stage and CTA
     const uint32_t stage_bytes = (tx_bytes + 1023u) & ~1023u;   // stride: swizzle atoms stay aligned
     uint64_t* full = reinterpret_cast<uint64_t*>(smem + a.stages * stage_bytes);
     uint64_t* empty = full + kMaxStages;
@@ -112,6 +133,15 @@ __global__ void __launch_bounds__(threads_for(kMx), 1)
 
     const int warp = threadIdx.x >> 5;
     const int lane = threadIdx.x & 31;
+    const uint32_t rank = kPair ? (blockIdx.x & 1u) : 0u;  // == %cluster_ctarank
+    // an epilogue warp is done with an accumulator (pair: the even CTA's
+    // barrier, which counts both CTAs' warps)
+    auto release_acc = [](uint64_t* bar) {
+        if constexpr (kPair)
+            mbar_arrive_cluster(cluster_addr(bar, 0));
+        else
+            mbar_arrive(bar);
+    };
 
     if (threadIdx.x == 0) {
         for (int s = 0; s < a.stages; ++s) {
@@ -120,17 +150,19 @@ __global__ void __launch_bounds__(threads_for(kMx), 1)
         }
         for (int i = 0; i < 2; ++i) {
             mbar_init(&tfull[i], 1);
-            mbar_init(&tempty[i], kMx ? 8 : 4);  // every epilogue warp
+            mbar_init(&tempty[i], kPair ? 8 : (kMx ? 8 : 4));  // every epilogue warp (of the pair)
         }
         mbar_init(drain, 1);
         *abort_flag = 0;
         fence_barrier_init();
         tma_prefetch_desc(&tmA);
-        tma_prefetch_desc(&tmB);
+        tma_prefetch_desc(kPair ? &tmBh : &tmB);
     }
+    // both CTAs' barriers are initialised before either signals the other's
+    if constexpr (kPair) cluster_sync();
     if (warp == 1) {
-        tmem_alloc(tmem_slot, kTmemCols);
-        tmem_relinquish();
+        tmem_alloc<G>(tmem_slot, kTmemCols);
+        tmem_relinquish<G>();
     }
     tc_fence_before();
     __syncthreads();
@@ -146,13 +178,16 @@ __global__ void __launch_bounds__(threads_for(kMx), 1)
             // token tile (and, MXFP8, its scale atom) of stage s
             auto load_x = [&](int s, int kb, int row) {
                 uint8_t* sx = smem + s * stage_bytes;
-                tma_load_2d(sx, &tmA, &full[s], kb * kKElems, row);
+                if constexpr (kPair)
+                    tma_load_2d_pair(sx, &tmA, cluster_addr(&full[s], 0), kb * kKElems, row);
+                else
+                    tma_load_2d(sx, &tmA, &full[s], kb * kKElems, row);
                 if constexpr (kMx)
                     bulk_load(sx + a.a_bytes + a.b_bytes,
                               a.sfa + (static_cast<int64_t>(row / kBM) * a.kb128 + kb) * 512, 512,
                               &full[s]);
             };
-            Schedule sch(a);
+            Schedule<kPair> sch(a);
             Unit u;
             bool ok = true, waited = false;
             int pro_kb[kMaxStages], pro_row[kMaxStages], pro_s[kMaxStages];
@@ -176,8 +211,15 @@ __global__ void __launch_bounds__(threads_for(kMx), 1)
                     }
                     uint8_t* sw = smem + s * stage_bytes + a.a_bytes;
                     const int x_row = u.m * kBM;
-                    mbar_arrive_expect_tx(&full[s], tx_bytes);
-                    tma_load_2d_hint(sw, &tmB, &full[s], kb * kKElems, u.n * BN, pol_w);
+                    if constexpr (kPair) {
+                        // the even CTA's barrier counts both CTAs' bytes
+                        if (rank == 0) mbar_arrive_expect_tx(&full[s], 2 * tx_bytes);
+                        tma_load_2d_pair_hint(sw, &tmBh, cluster_addr(&full[s], 0), kb * kKElems,
+                                              u.n * BN + static_cast<int>(rank) * (BN / 2), pol_w);
+                    } else {
+                        mbar_arrive_expect_tx(&full[s], tx_bytes);
+                        tma_load_2d_hint(sw, &tmB, &full[s], kb * kKElems, u.n * BN, pol_w);
+                    }
                     if constexpr (kMx)
                         bulk_load(sw + a.b_bytes + 512,
                                   a.sfb + (static_cast<int64_t>(u.n) * a.kb128 + kb) * (512 * kBAtoms),
@@ -205,8 +247,8 @@ __global__ void __launch_bounds__(threads_for(kMx), 1)
             if (!ok) fail(abort_flag, a.err);
         }
     } else if (warp == 1) {
-        if (lane == 0) {
-            Schedule sch(a);
+        if (lane == 0 && rank == 0) {  // (a pair's odd CTA issues no MMA)
+            Schedule<kPair> sch(a);
             Unit u;
             bool ok = true;
             int nu = 0;
@@ -225,7 +267,7 @@ __global__ void __launch_bounds__(threads_for(kMx), 1)
             while (ok && sch.next(u)) {
                 const int acc = nu & 1;
                 const uint32_t apar = static_cast<uint32_t>((nu >> 1) & 1);
-                if (!mbar_wait(&tempty[acc], apar ^ 1u, abort_v)) {
+                if (!mbar_wait(&tempty[acc], apar ^ 1u, abort_v, kPair)) {
                     ok = false;
                     break;
                 }
@@ -250,13 +292,21 @@ __global__ void __launch_bounds__(threads_for(kMx), 1)
                             mma_mxf8_ss(d_tmem, adesc + 2 * k, bdesc + 2 * k,
                                         idesc_mxf8(kBM, BN, k, k), sf, sf + 8,
                                         (kb > 0 || k > 0) ? 1u : 0u);
+                    } else if constexpr (kPair) {
+#pragma unroll
+                        for (int k = 0; k < 4; ++k)
+                            mma_bf16_ss_pair(d_tmem, adesc + 2 * k, bdesc + 2 * k, a.idesc,
+                                             (kb > 0 || k > 0) ? 1u : 0u);
                     } else {
 #pragma unroll
                         for (int k = 0; k < 4; ++k)  // 4 x K16 per 64-element block
                             mma_bf16_ss(d_tmem, adesc + 2 * k, bdesc + 2 * k, a.idesc,
                                         (kb > 0 || k > 0) ? 1u : 0u);
                     }
-                    mma_commit(&empty[s]);
+                    if constexpr (kPair)
+                        mma_commit_pair_mc(&empty[s], static_cast<uint16_t>(3));
+                    else
+                        mma_commit(&empty[s]);
                     if (++s == a.stages) {
                         s = 0;
                         par ^= 1u;
@@ -272,7 +322,10 @@ __global__ void __launch_bounds__(threads_for(kMx), 1)
                     }
                 }
                 if (!ok) break;
-                mma_commit(&tfull[acc]);
+                if constexpr (kPair)
+                    mma_commit_pair_mc(&tfull[acc], static_cast<uint16_t>(3));
+                else
+                    mma_commit(&tfull[acc]);
                 ++nu;
             }
             if (!ok) fail(abort_flag, a.err);
@@ -287,7 +340,7 @@ __global__ void __launch_bounds__(threads_for(kMx), 1)
         constexpr int kHalfCh = kMx ? (BN / 32 + 1) / 2 : BN / 32;  // chunks of this warp
         const int half = kMx ? (warp - 2) >> 2 : 0;
         const int c0 = half * kHalfCh * 32;          // first column of this warp's half
-        Schedule sch(a);
+        Schedule<kPair> sch(a);
         Unit u;
         bool ok = true;
         int nu = 0;
@@ -355,7 +408,7 @@ __global__ void __launch_bounds__(threads_for(kMx), 1)
                     }
                     tc_fence_before();
                     __syncwarp();
-                    if (lane == 0) mbar_arrive(&tempty[acc]);
+                    if (lane == 0) release_acc(&tempty[acc]);
                     if (live)  // (MXFP8: J = 2 records per tile, one per half)
                         a.partials[(static_cast<int64_t>(t) * a.H + h) * a.J +
                                    (kMx ? 2 * (d0 / BN) + half : d0 / BN)] =
@@ -388,7 +441,7 @@ __global__ void __launch_bounds__(threads_for(kMx), 1)
                     }
                     tc_fence_before();
                     __syncwarp();
-                    if (lane == 0) mbar_arrive(&tempty[acc]);
+                    if (lane == 0) release_acc(&tempty[acc]);
                 }
             }
             ++nu;
@@ -404,17 +457,41 @@ __global__ void __launch_bounds__(threads_for(kMx), 1)
     tc_fence_after();
     if (*abort_v) {
         if (warp == 0 && lane == 0) {
-            const int64_t first = issued > a.stages ? issued - a.stages : 0;
-            for (int64_t j = first; j < issued; ++j)
-                mbar_wait(&full[j % a.stages], static_cast<uint32_t>((j / a.stages) & 1), nullptr);
+            if (rank == 0) {
+                const int64_t first = issued > a.stages ? issued - a.stages : 0;
+                for (int64_t j = first; j < issued; ++j)
+                    mbar_wait(&full[j % a.stages], static_cast<uint32_t>((j / a.stages) & 1),
+                              nullptr);
+            } else {
+                // a pair's odd CTA: its copies complete on the even CTA's
+                // barriers; give them 100 us to land
+                const uint64_t t0 = globaltimer_ns();
+                while (globaltimer_ns() - t0 < 100000ull) __nanosleep(1000);
+            }
         }
-        if (warp == 1 && lane == 0) {
-            mma_commit(drain);
+        if (warp == 1 && lane == 0 && rank == 0) {
+            if constexpr (kPair)
+                mma_commit_pair(drain);
+            else
+                mma_commit(drain);
             mbar_wait(drain, 0, nullptr);
         }
         __syncthreads();
+    } else if constexpr (kPair) {
+        // The even CTA's commits of the last stages have reached this CTA's
+        // empty barriers (none is in flight toward it when the pair leaves).
+        if (warp == 0 && lane == 0) {
+            const int64_t first = issued > a.stages ? issued - a.stages : 0;
+            for (int64_t j = first; j < issued; ++j)
+                mbar_wait(&empty[j % a.stages], static_cast<uint32_t>((j / a.stages) & 1),
+                          nullptr);
+        }
+        __syncthreads();
     }
-    if (warp == 1) tmem_dealloc(tmem_base, kTmemCols);
+    // a pair leaves together: neither CTA's shared memory or TMEM goes while
+    // the other may still signal, read or write it
+    if constexpr (kPair) cluster_sync();
+    if (warp == 1) tmem_dealloc<G>(tmem_base, kTmemCols);
 }
 
 // E8M0 [N/32][K/32] block scales of wkv -> atoms [N/bn][K/128][ceil(bn/128)][512]
@@ -462,9 +539,10 @@ cudaError_t launch_unpack_scales(const engram_handle* h, uint8_t* out, int64_t T
 }
 
 cudaError_t gemm_setup_attributes() {
-    const void* fns[] = {reinterpret_cast<const void*>(wkv_gemm_kernel<false, kBNPrefill>),
-                         reinterpret_cast<const void*>(wkv_gemm_kernel<true, kBNPrefillMx>),
-                         reinterpret_cast<const void*>(wkv_gemm_kernel<true, kBNPrefillMxWide>)};
+    const void* fns[] = {reinterpret_cast<const void*>(wkv_gemm_kernel<false, kBNPrefill, false>),
+                         reinterpret_cast<const void*>(wkv_gemm_kernel<false, kBNPrefill, true>),
+                         reinterpret_cast<const void*>(wkv_gemm_kernel<true, kBNPrefillMx, false>),
+                         reinterpret_cast<const void*>(wkv_gemm_kernel<true, kBNPrefillMxWide, false>)};
     for (const void* fn : fns) {
         const cudaError_t e =
             cudaFuncSetAttribute(fn, cudaFuncAttributeMaxDynamicSharedMemorySize, kGemmSmemBytes);
@@ -473,22 +551,66 @@ cudaError_t gemm_setup_attributes() {
     return cudaSuccess;
 }
 
-static cudaError_t launch(const void* fn, int grid, int threads, uint32_t smem_bytes,
-                          const CUtensorMap& tmA, const CUtensorMap& tmB, const GemmArgs& a,
-                          cudaStream_t s, bool pdl) {
+static cudaError_t launch(const void* fn, int grid, int threads, uint32_t smem_bytes, bool pair,
+                          const CUtensorMap& tmA, const CUtensorMap& tmB, const CUtensorMap& tmBh,
+                          const GemmArgs& a, cudaStream_t s, bool pdl) {
     cudaLaunchConfig_t cfg = {};
     cfg.gridDim = dim3(static_cast<unsigned>(grid));
     cfg.blockDim = dim3(static_cast<unsigned>(threads));
     cfg.dynamicSmemBytes = smem_bytes;
     cfg.stream = s;
-    cudaLaunchAttribute attr[1];
-    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
-    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    cudaLaunchAttribute attr[2];
+    int n = 0;
+    if (pair) {
+        attr[n].id = cudaLaunchAttributeClusterDimension;
+        attr[n].val.clusterDim.x = 2;
+        attr[n].val.clusterDim.y = 1;
+        attr[n].val.clusterDim.z = 1;
+        ++n;
+    }
+    if (pdl) {
+        attr[n].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+        attr[n].val.programmaticStreamSerializationAllowed = 1;
+        ++n;
+    }
     cfg.attrs = attr;
-    cfg.numAttrs = pdl ? 1 : 0;
+    cfg.numAttrs = n;
     void* args[] = {const_cast<CUtensorMap*>(&tmA), const_cast<CUtensorMap*>(&tmB),
-                    const_cast<GemmArgs*>(&a)};
+                    const_cast<CUtensorMap*>(&tmBh), const_cast<GemmArgs*>(&a)};
     return cudaLaunchKernelExC(&cfg, fn, args);
+}
+
+// Shared memory of the CTA-pair GEMM (bf16): stages of 128 token rows and
+// half of the 256 weight rows, 128 bytes of k each.
+static uint32_t pair_stride() { return (2u * kBM * kKBlockBytes + 1023u) & ~1023u; }
+static int pair_stages() {
+    const int n = static_cast<int>(kStageBudget / pair_stride());
+    return n > kMaxStages ? kMaxStages : n;
+}
+
+// How many CTA-pair clusters of the bf16 GEMM fit on the GPU at once (0:
+// none; the GEMM then runs on single CTAs).
+int gemm_pair_capacity(const engram_handle* h) {
+    if (h->cfg.wkv_format == ENGRAM_WKV_MXFP8) return 0;
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3(static_cast<unsigned>(2 * (h->num_sms / 2)));
+    cfg.blockDim = dim3(static_cast<unsigned>(threads_for(false)));
+    cfg.dynamicSmemBytes = static_cast<uint32_t>(pair_stages()) * pair_stride() + 2048u;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeClusterDimension;
+    attr[0].val.clusterDim.x = 2;
+    attr[0].val.clusterDim.y = 1;
+    attr[0].val.clusterDim.z = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    int clusters = 0;
+    if (cudaOccupancyMaxActiveClusters(
+            &clusters, reinterpret_cast<const void*>(wkv_gemm_kernel<false, kBNPrefill, true>),
+            &cfg) != cudaSuccess) {
+        cudaGetLastError();
+        return 0;
+    }
+    return clusters;
 }
 
 int prefill_bn(const engram_handle* h) {
@@ -535,16 +657,30 @@ cudaError_t launch_wkv_tokens_m(const engram_handle* h, const void* hidden, int6
     a.sfa = h->ws.staged_s;
     a.sfb = h->ws.wsf_atoms;
     a.err = h->ws.err;
+    if (!mx && h->gemm_pair_clusters > 0) {
+        // CTA pairs: 256 x 256 units, a CTA's stage = its 128 token rows and
+        // 128 of the unit's weight rows
+        a.b_bytes = static_cast<uint32_t>(bn / 2) * kKBlockBytes;
+        a.stages = pair_stages();
+        a.idesc = idesc_bf16(2 * kBM, kBNPrefill);
+        const int units = ((a.m_tiles + 1) / 2) * a.n_tiles;
+        const int clusters = units < h->gemm_pair_clusters ? units : h->gemm_pair_clusters;
+        const uint32_t smem_bytes = static_cast<uint32_t>(a.stages) * pair_stride() + 2048u;
+        return launch(reinterpret_cast<const void*>(wkv_gemm_kernel<false, kBNPrefill, true>),
+                      2 * clusters, threads_for(false), smem_bytes, true, h->tm_act_m, h->tm_w_n,
+                      h->tm_w_half, a, s, pdl);
+    }
     const int grid = a.total < h->num_sms ? a.total : h->num_sms;
     const void* fn =
-        !mx ? reinterpret_cast<const void*>(wkv_gemm_kernel<false, kBNPrefill>)
+        !mx ? reinterpret_cast<const void*>(wkv_gemm_kernel<false, kBNPrefill, false>)
             : (bn == kBNPrefillMxWide
-                   ? reinterpret_cast<const void*>(wkv_gemm_kernel<true, kBNPrefillMxWide>)
-                   : reinterpret_cast<const void*>(wkv_gemm_kernel<true, kBNPrefillMx>));
+                   ? reinterpret_cast<const void*>(wkv_gemm_kernel<true, kBNPrefillMxWide, false>)
+                   : reinterpret_cast<const void*>(wkv_gemm_kernel<true, kBNPrefillMx, false>));
     // the shared memory the stages and barriers need, and no more: the
     // epilogue's loads go through the L1 that shares the SM's memory
     const uint32_t smem_bytes = static_cast<uint32_t>(a.stages) * stride + 2048u;
-    return launch(fn, grid, threads_for(mx), smem_bytes, h->tm_act_m, h->tm_w_n, a, s, pdl);
+    return launch(fn, grid, threads_for(mx), smem_bytes, false, h->tm_act_m, h->tm_w_n,
+                  h->tm_w_half, a, s, pdl);
 }
 
 }  // namespace engram
