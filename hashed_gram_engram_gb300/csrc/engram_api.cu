@@ -56,6 +56,20 @@ bool make_map(CUtensorMap* m, const void* base, CUtensorMapDataType dt, int elem
               CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
+// Rows of 512 bytes (MXFP8 scale atoms, as 128 x 4-byte words), box =
+// box_rows whole rows, no swizzle: a TMA copy of atoms in their stored order.
+bool make_atom_map(CUtensorMap* m, const void* base, int64_t rows, int box_rows) {
+    EncodeTiledFn fn = encode_fn();
+    if (fn == nullptr) return false;
+    cuuint64_t dims[2] = {128, static_cast<cuuint64_t>(rows)};
+    cuuint64_t strides[1] = {512};
+    cuuint32_t box[2] = {128, static_cast<cuuint32_t>(box_rows)};
+    cuuint32_t estr[2] = {1, 1};
+    return fn(m, CU_TENSOR_MAP_DATA_TYPE_UINT32, 2, const_cast<void*>(base), dims, strides, box,
+              estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_NONE,
+              CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
 // Keeps the caller's current device across an entry point.
 struct DeviceGuard {
     int prev = -1;
@@ -314,6 +328,12 @@ int engram_create(const engram_config* cfg, const engram_weights* w, engram_t** 
               make_map(&h->tm_act_m, act, dt, elem, K, ws.rows_alloc, kBM);
     for (int i = 0; i < 16 && ok; ++i)
         ok = make_map(&h->tm_act_n[i], act, dt, elem, K, ws.rows_alloc, 16 * (i + 1));
+    if (ok && mx) {
+        const int bn = prefill_bn(h);
+        const int atoms = (bn + 127) / 128;  // per tile and k-block
+        ok = make_atom_map(&h->tm_sfa, ws.staged_s, ws.rows_alloc / kBM * (K / 128), 1) &&
+             make_atom_map(&h->tm_sfb, ws.wsf_atoms, (N / bn) * (K / 128) * atoms, atoms);
+    }
     if (!ok) {
         free_handle(h);
         return ENGRAM_ERR_CUDA;

@@ -111,6 +111,8 @@ struct engram_handle {
     // TMA descriptors
     CUtensorMap tm_w_n;        // wkv, prefill B operand (box BN rows x 128 bytes)
     CUtensorMap tm_w_half;     // the same, box BN/2 rows (a CTA's half in a CTA-pair GEMM)
+    CUtensorMap tm_sfa;        // MXFP8 scale atoms of the staged rows, rows of 512 bytes, box 1 row
+    CUtensorMap tm_sfb;        // MXFP8 scale atoms of wkv, box = one prefill tile's atoms
     int gemm_pair_clusters;    // CTA-pair GEMM clusters that fit at once (0: single CTAs)
     CUtensorMap tm_act_m;      // staged rows (bf16, or e4m3 codes), box 128 rows x 128 bytes
     CUtensorMap tm_act_n[16];  // the same, box 16 * (i + 1) rows (the fused kernel's tile)

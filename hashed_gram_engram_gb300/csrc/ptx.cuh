@@ -423,6 +423,21 @@ __device__ __forceinline__ void mma_mxf8_ss(uint32_t d_tmem, uint64_t adesc, uin
         : "memory");
 }
 
+// The CTA pair's block-scaled MMA (issued by the even CTA; operands split
+// as in mma_bf16_ss_pair): each CTA's TMEM holds, at sfa_tmem, the scales
+// of its 128 A rows and, at sfb_tmem, those of all N B rows.
+__device__ __forceinline__ void mma_mxf8_ss_pair(uint32_t d_tmem, uint64_t adesc, uint64_t bdesc,
+                                                 uint32_t idesc, uint32_t sfa_tmem,
+                                                 uint32_t sfb_tmem, uint32_t accumulate) {
+    asm volatile(
+        "{\n\t.reg .pred p;\n\t"
+        "setp.ne.b32 p, %6, 0;\n\t"
+        "tcgen05.mma.cta_group::2.kind::mxf8f6f4.block_scale.scale_vec::1X"
+        " [%0], %1, %2, %3, [%4], [%5], p;\n\t}" ::"r"(d_tmem),
+        "l"(adesc), "l"(bdesc), "r"(idesc), "r"(sfa_tmem), "r"(sfb_tmem), "r"(accumulate)
+        : "memory");
+}
+
 // Arrive on `bar` once every tcgen05 operation this thread issued so far has
 // completed.
 __device__ __forceinline__ void mma_commit(uint64_t* bar) {
@@ -496,6 +511,14 @@ __device__ __forceinline__ void tmem_st4(uint32_t taddr, uint32_t a, uint32_t b,
 // bytes): line i goes to lanes i, 32 + i, 64 + i and 96 + i, four columns.
 __device__ __forceinline__ void tmem_cp_atom(uint32_t taddr, uint64_t sdesc) {
     asm volatile("tcgen05.cp.cta_group::1.32x128b.warpx4 [%0], %1;" ::"r"(taddr), "l"(sdesc)
+                 : "memory");
+}
+
+// The CTA pair's form (issued by the even CTA): in each CTA of the pair,
+// the atom at the descriptor's offset of that CTA's shared memory goes to
+// taddr of that CTA's TMEM.
+__device__ __forceinline__ void tmem_cp_atom_pair(uint32_t taddr, uint64_t sdesc) {
+    asm volatile("tcgen05.cp.cta_group::2.32x128b.warpx4 [%0], %1;" ::"r"(taddr), "l"(sdesc)
                  : "memory");
 }
 

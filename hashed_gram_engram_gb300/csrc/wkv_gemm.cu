@@ -101,18 +101,22 @@ __device__ __forceinline__ void fail(int* abort_flag, unsigned* err) {
     atomicOr(err, ENGRAM_DEVERR_TIMEOUT);
 }
 
-// kPair (bf16): CTA pairs of one cluster share each MMA (tcgen05
-// cta_group::2, M = 256): each CTA's shared memory holds its 128 token rows
-// and half of the tile's BN weight rows (tmBh: boxes of BN/2 rows), so a
-// CTA loads 2/3 of the operand bytes of an unpaired 128 x BN tile for the
-// same MMA work.  The even CTA issues the MMAs; its full barriers count
-// both CTAs' copies; its commits reach both CTAs' empty and tfull barriers;
-// both CTAs' epilogues release its tempty barriers.
+// kPair: CTA pairs of one cluster share each MMA (tcgen05 cta_group::2,
+// M = 256): each CTA's shared memory holds its 128 token rows and half of
+// the tile's BN weight rows (tmBh: boxes of BN/2 rows), so a CTA loads
+// about 2/3 of the operand bytes of an unpaired 128 x BN tile for the same
+// MMA work.  The even CTA issues the MMAs; its full barriers count both
+// CTAs' copies; its commits reach both CTAs' empty and tfull barriers; both
+// CTAs' epilogues release its tempty barriers.  MXFP8: each CTA also loads
+// its token rows' scale atom and all BN weight rows' atoms (tmSA, tmSB:
+// the atom arrays as rows of 512 bytes, so that the odd CTA's copies can
+// complete on the even CTA's barrier), and the even CTA's tcgen05.cp moves
+// each CTA's atoms into its own TMEM.
 template <bool kMx, int BN, bool kPair>
 __global__ void __launch_bounds__(threads_for(kMx), 1)
     wkv_gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
-                    const __grid_constant__ CUtensorMap tmBh, const GemmArgs a) {
-    static_assert(!(kPair && kMx), "CTA pairs: bf16 weights only");
+                    const __grid_constant__ CUtensorMap tmBh, const __grid_constant__ CUtensorMap tmSA,
+                    const __grid_constant__ CUtensorMap tmSB, const GemmArgs a) {
     constexpr int G = kPair ? 2 : 1;  // tcgen05 CTA group
     constexpr int kKElems = kMx ? 128 : 64;  // k per 128-byte block
     constexpr uint32_t kBAtoms = (BN + 127) / 128;  // weight scale atoms per k-block
@@ -150,7 +154,7 @@ __global__ void __launch_bounds__(threads_for(kMx), 1)
         }
         for (int i = 0; i < 2; ++i) {
             mbar_init(&tfull[i], 1);
-            mbar_init(&tempty[i], kPair ? 8 : (kMx ? 8 : 4));  // every epilogue warp (of the pair)
+            mbar_init(&tempty[i], (kPair ? 2 : 1) * (kMx ? 8 : 4));  // every epilogue warp (of the pair)
         }
         mbar_init(drain, 1);
         *abort_flag = 0;
@@ -182,7 +186,10 @@ __global__ void __launch_bounds__(threads_for(kMx), 1)
                     tma_load_2d_pair(sx, &tmA, cluster_addr(&full[s], 0), kb * kKElems, row);
                 else
                     tma_load_2d(sx, &tmA, &full[s], kb * kKElems, row);
-                if constexpr (kMx)
+                if constexpr (kMx && kPair)
+                    tma_load_2d_pair(sx + a.a_bytes + a.b_bytes, &tmSA, cluster_addr(&full[s], 0), 0,
+                                     (row / kBM) * a.kb128 + kb);
+                else if constexpr (kMx)
                     bulk_load(sx + a.a_bytes + a.b_bytes,
                               a.sfa + (static_cast<int64_t>(row / kBM) * a.kb128 + kb) * 512, 512,
                               &full[s]);
@@ -220,7 +227,10 @@ __global__ void __launch_bounds__(threads_for(kMx), 1)
                         mbar_arrive_expect_tx(&full[s], tx_bytes);
                         tma_load_2d_hint(sw, &tmB, &full[s], kb * kKElems, u.n * BN, pol_w);
                     }
-                    if constexpr (kMx)
+                    if constexpr (kMx && kPair)
+                        tma_load_2d_pair(sw + a.b_bytes + 512, &tmSB, cluster_addr(&full[s], 0), 0,
+                                         (u.n * a.kb128 + kb) * static_cast<int>(kBAtoms));
+                    else if constexpr (kMx)
                         bulk_load(sw + a.b_bytes + 512,
                                   a.sfb + (static_cast<int64_t>(u.n) * a.kb128 + kb) * (512 * kBAtoms),
                                   512 * kBAtoms, &full[s]);
@@ -283,15 +293,28 @@ __global__ void __launch_bounds__(threads_for(kMx), 1)
                         // this stage's 16-column scale slot: tokens' cells at
                         // +0, wkv's at +8 (4 columns per 128 tile rows)
                         const uint32_t atoms = sa + a.a_bytes + a.b_bytes;
-                        tmem_cp_atom(sf, smem_desc_atom(atoms));
+                        if constexpr (kPair) {
+                            tmem_cp_atom_pair(sf, smem_desc_atom(atoms));
 #pragma unroll
-                        for (uint32_t b = 0; b < kBAtoms; ++b)
-                            tmem_cp_atom(sf + 8 + 4 * b, smem_desc_atom(atoms + 512 * (1 + b)));
+                            for (uint32_t b = 0; b < kBAtoms; ++b)
+                                tmem_cp_atom_pair(sf + 8 + 4 * b,
+                                                  smem_desc_atom(atoms + 512 * (1 + b)));
 #pragma unroll
-                        for (int k = 0; k < 4; ++k)  // 4 x K32, scale byte k of each cell
-                            mma_mxf8_ss(d_tmem, adesc + 2 * k, bdesc + 2 * k,
-                                        idesc_mxf8(kBM, BN, k, k), sf, sf + 8,
-                                        (kb > 0 || k > 0) ? 1u : 0u);
+                            for (int k = 0; k < 4; ++k)
+                                mma_mxf8_ss_pair(d_tmem, adesc + 2 * k, bdesc + 2 * k,
+                                                 idesc_mxf8(2 * kBM, BN, k, k), sf, sf + 8,
+                                                 (kb > 0 || k > 0) ? 1u : 0u);
+                        } else {
+                            tmem_cp_atom(sf, smem_desc_atom(atoms));
+#pragma unroll
+                            for (uint32_t b = 0; b < kBAtoms; ++b)
+                                tmem_cp_atom(sf + 8 + 4 * b, smem_desc_atom(atoms + 512 * (1 + b)));
+#pragma unroll
+                            for (int k = 0; k < 4; ++k)  // 4 x K32, scale byte k of each cell
+                                mma_mxf8_ss(d_tmem, adesc + 2 * k, bdesc + 2 * k,
+                                            idesc_mxf8(kBM, BN, k, k), sf, sf + 8,
+                                            (kb > 0 || k > 0) ? 1u : 0u);
+                        }
                     } else if constexpr (kPair) {
 #pragma unroll
                         for (int k = 0; k < 4; ++k)
@@ -538,22 +561,32 @@ cudaError_t launch_unpack_scales(const engram_handle* h, uint8_t* out, int64_t T
     return cudaGetLastError();
 }
 
+// The kernel of a configuration: bf16 or MXFP8 weights, tile width, pairs.
+static const void* gemm_kernel(bool mx, int bn, bool pair) {
+    if (!mx)
+        return pair ? reinterpret_cast<const void*>(wkv_gemm_kernel<false, kBNPrefill, true>)
+                    : reinterpret_cast<const void*>(wkv_gemm_kernel<false, kBNPrefill, false>);
+    if (bn == kBNPrefillMxWide)
+        return pair ? reinterpret_cast<const void*>(wkv_gemm_kernel<true, kBNPrefillMxWide, true>)
+                    : reinterpret_cast<const void*>(wkv_gemm_kernel<true, kBNPrefillMxWide, false>);
+    return pair ? reinterpret_cast<const void*>(wkv_gemm_kernel<true, kBNPrefillMx, true>)
+                : reinterpret_cast<const void*>(wkv_gemm_kernel<true, kBNPrefillMx, false>);
+}
+
 cudaError_t gemm_setup_attributes() {
-    const void* fns[] = {reinterpret_cast<const void*>(wkv_gemm_kernel<false, kBNPrefill, false>),
-                         reinterpret_cast<const void*>(wkv_gemm_kernel<false, kBNPrefill, true>),
-                         reinterpret_cast<const void*>(wkv_gemm_kernel<true, kBNPrefillMx, false>),
-                         reinterpret_cast<const void*>(wkv_gemm_kernel<true, kBNPrefillMxWide, false>)};
-    for (const void* fn : fns) {
-        const cudaError_t e =
-            cudaFuncSetAttribute(fn, cudaFuncAttributeMaxDynamicSharedMemorySize, kGemmSmemBytes);
-        if (e != cudaSuccess) return e;
-    }
+    for (int mx = 0; mx < 2; ++mx)
+        for (int pair = 0; pair < 2; ++pair)
+            for (int bn : {kBNPrefillMx, kBNPrefillMxWide}) {
+                const cudaError_t e =
+                    cudaFuncSetAttribute(gemm_kernel(mx != 0, bn, pair != 0),
+                                         cudaFuncAttributeMaxDynamicSharedMemorySize, kGemmSmemBytes);
+                if (e != cudaSuccess) return e;
+            }
     return cudaSuccess;
 }
 
 static cudaError_t launch(const void* fn, int grid, int threads, uint32_t smem_bytes, bool pair,
-                          const CUtensorMap& tmA, const CUtensorMap& tmB, const CUtensorMap& tmBh,
-                          const GemmArgs& a, cudaStream_t s, bool pdl) {
+                          const engram_handle* h, const GemmArgs& a, cudaStream_t s, bool pdl) {
     cudaLaunchConfig_t cfg = {};
     cfg.gridDim = dim3(static_cast<unsigned>(grid));
     cfg.blockDim = dim3(static_cast<unsigned>(threads));
@@ -575,27 +608,48 @@ static cudaError_t launch(const void* fn, int grid, int threads, uint32_t smem_b
     }
     cfg.attrs = attr;
     cfg.numAttrs = n;
-    void* args[] = {const_cast<CUtensorMap*>(&tmA), const_cast<CUtensorMap*>(&tmB),
-                    const_cast<CUtensorMap*>(&tmBh), const_cast<GemmArgs*>(&a)};
+    void* args[] = {const_cast<CUtensorMap*>(&h->tm_act_m), const_cast<CUtensorMap*>(&h->tm_w_n),
+                    const_cast<CUtensorMap*>(&h->tm_w_half), const_cast<CUtensorMap*>(&h->tm_sfa),
+                    const_cast<CUtensorMap*>(&h->tm_sfb), const_cast<GemmArgs*>(&a)};
     return cudaLaunchKernelExC(&cfg, fn, args);
 }
 
-// Shared memory of the CTA-pair GEMM (bf16): stages of 128 token rows and
-// half of the 256 weight rows, 128 bytes of k each.
-static uint32_t pair_stride() { return (2u * kBM * kKBlockBytes + 1023u) & ~1023u; }
-static int pair_stages() {
-    const int n = static_cast<int>(kStageBudget / pair_stride());
-    return n > kMaxStages ? kMaxStages : n;
+// Pipeline shape of a configuration: bytes per stage (a CTA's token rows,
+// its weight rows -- half the tile's in a pair -- and, MXFP8, the scale
+// atoms, rounded to 1024) and the number of stages (MXFP8: two accumulators
+// plus a 16-column scale slot per stage in TMEM).
+struct Pipe {
+    uint32_t a_bytes, b_bytes, stride;
+    int stages;
+};
+
+static Pipe pipe_shape(bool mx, int bn, bool pair) {
+    Pipe p;
+    p.a_bytes = kBM * kKBlockBytes;
+    p.b_bytes = static_cast<uint32_t>(pair ? bn / 2 : bn) * kKBlockBytes;
+    const uint32_t atoms = mx ? 512u * (1u + static_cast<uint32_t>((bn + 127) / 128)) : 0u;
+    p.stride = (p.a_bytes + p.b_bytes + atoms + 1023u) & ~1023u;
+    p.stages = static_cast<int>(kStageBudget / p.stride);
+    if (p.stages > kMaxStages) p.stages = kMaxStages;
+    if (mx && p.stages > (512 - 2 * bn) / 16) p.stages = (512 - 2 * bn) / 16;
+    return p;
 }
 
-// How many CTA-pair clusters of the bf16 GEMM fit on the GPU at once (0:
-// none; the GEMM then runs on single CTAs).
+// the shared memory the stages and barriers need, and no more: the
+// epilogue's loads go through the L1 that shares the SM's memory
+static uint32_t smem_request(const Pipe& p) {
+    return static_cast<uint32_t>(p.stages) * p.stride + 2048u;
+}
+
+// How many CTA-pair clusters of this configuration's GEMM fit on the GPU at
+// once (0: none; the GEMM then runs on single CTAs).
 int gemm_pair_capacity(const engram_handle* h) {
-    if (h->cfg.wkv_format == ENGRAM_WKV_MXFP8) return 0;
+    const bool mx = h->cfg.wkv_format == ENGRAM_WKV_MXFP8;
+    const int bn = prefill_bn(h);
     cudaLaunchConfig_t cfg = {};
     cfg.gridDim = dim3(static_cast<unsigned>(2 * (h->num_sms / 2)));
-    cfg.blockDim = dim3(static_cast<unsigned>(threads_for(false)));
-    cfg.dynamicSmemBytes = static_cast<uint32_t>(pair_stages()) * pair_stride() + 2048u;
+    cfg.blockDim = dim3(static_cast<unsigned>(threads_for(mx)));
+    cfg.dynamicSmemBytes = smem_request(pipe_shape(mx, bn, true));
     cudaLaunchAttribute attr[1];
     attr[0].id = cudaLaunchAttributeClusterDimension;
     attr[0].val.clusterDim.x = 2;
@@ -604,9 +658,7 @@ int gemm_pair_capacity(const engram_handle* h) {
     cfg.attrs = attr;
     cfg.numAttrs = 1;
     int clusters = 0;
-    if (cudaOccupancyMaxActiveClusters(
-            &clusters, reinterpret_cast<const void*>(wkv_gemm_kernel<false, kBNPrefill, true>),
-            &cfg) != cudaSuccess) {
+    if (cudaOccupancyMaxActiveClusters(&clusters, gemm_kernel(mx, bn, true), &cfg) != cudaSuccess) {
         cudaGetLastError();
         return 0;
     }
@@ -624,6 +676,10 @@ cudaError_t launch_wkv_tokens_m(const engram_handle* h, const void* hidden, int6
                                 int64_t hs_h, int64_t T, cudaStream_t s, bool pdl) {
     const bool mx = h->cfg.wkv_format == ENGRAM_WKV_MXFP8;
     const int bn = prefill_bn(h);
+    // CTA pairs (256-token units, each CTA loading half the weight rows)
+    // whenever their clusters fit
+    const bool pair = h->gemm_pair_clusters > 0;
+    const Pipe p = pipe_shape(mx, bn, pair);
     GemmArgs a = {};
     a.m_tiles = static_cast<int>((T + kBM - 1) / kBM);
     a.n_tiles = static_cast<int>(h->N / bn);
@@ -632,15 +688,10 @@ cudaError_t launch_wkv_tokens_m(const engram_handle* h, const void* hidden, int6
     a.total = a.m_tiles * a.n_tiles;
     a.T = static_cast<int>(T);
     a.bn = bn;
-    a.a_bytes = kBM * kKBlockBytes;
-    a.b_bytes = static_cast<uint32_t>(bn) * kKBlockBytes;
-    const uint32_t atoms = mx ? 512u * (1u + static_cast<uint32_t>((bn + 127) / 128)) : 0u;
-    const uint32_t stride = (a.a_bytes + a.b_bytes + atoms + 1023u) & ~1023u;
-    a.stages = static_cast<int>(kStageBudget / stride);
-    if (a.stages > kMaxStages) a.stages = kMaxStages;
-    // MXFP8: two accumulators plus a 16-column scale slot per stage in TMEM
-    if (mx && a.stages > (512 - 2 * bn) / 16) a.stages = (512 - 2 * bn) / 16;
-    a.idesc = idesc_bf16(kBM, kBNPrefill);  // bf16 only: MXFP8 builds one per k step
+    a.a_bytes = p.a_bytes;
+    a.b_bytes = p.b_bytes;
+    a.stages = p.stages;
+    a.idesc = idesc_bf16(pair ? 2 * kBM : kBM, kBNPrefill);  // bf16 only: MXFP8 builds one per k step
     a.D = static_cast<int>(h->cfg.dim);
     a.H = static_cast<int>(h->cfg.hc_mult);
     a.J = (mx ? 2 : 1) * (a.D / bn);  // MXFP8: a partial record per half tile
@@ -657,30 +708,15 @@ cudaError_t launch_wkv_tokens_m(const engram_handle* h, const void* hidden, int6
     a.sfa = h->ws.staged_s;
     a.sfb = h->ws.wsf_atoms;
     a.err = h->ws.err;
-    if (!mx && h->gemm_pair_clusters > 0) {
-        // CTA pairs: 256 x 256 units, a CTA's stage = its 128 token rows and
-        // 128 of the unit's weight rows
-        a.b_bytes = static_cast<uint32_t>(bn / 2) * kKBlockBytes;
-        a.stages = pair_stages();
-        a.idesc = idesc_bf16(2 * kBM, kBNPrefill);
+    int grid;
+    if (pair) {
         const int units = ((a.m_tiles + 1) / 2) * a.n_tiles;
-        const int clusters = units < h->gemm_pair_clusters ? units : h->gemm_pair_clusters;
-        const uint32_t smem_bytes = static_cast<uint32_t>(a.stages) * pair_stride() + 2048u;
-        return launch(reinterpret_cast<const void*>(wkv_gemm_kernel<false, kBNPrefill, true>),
-                      2 * clusters, threads_for(false), smem_bytes, true, h->tm_act_m, h->tm_w_n,
-                      h->tm_w_half, a, s, pdl);
+        grid = 2 * (units < h->gemm_pair_clusters ? units : h->gemm_pair_clusters);
+    } else {
+        grid = a.total < h->num_sms ? a.total : h->num_sms;
     }
-    const int grid = a.total < h->num_sms ? a.total : h->num_sms;
-    const void* fn =
-        !mx ? reinterpret_cast<const void*>(wkv_gemm_kernel<false, kBNPrefill, false>)
-            : (bn == kBNPrefillMxWide
-                   ? reinterpret_cast<const void*>(wkv_gemm_kernel<true, kBNPrefillMxWide, false>)
-                   : reinterpret_cast<const void*>(wkv_gemm_kernel<true, kBNPrefillMx, false>));
-    // the shared memory the stages and barriers need, and no more: the
-    // epilogue's loads go through the L1 that shares the SM's memory
-    const uint32_t smem_bytes = static_cast<uint32_t>(a.stages) * stride + 2048u;
-    return launch(fn, grid, threads_for(mx), smem_bytes, false, h->tm_act_m, h->tm_w_n,
-                  h->tm_w_half, a, s, pdl);
+    return launch(gemm_kernel(mx, bn, pair), grid, threads_for(mx), smem_request(p), pair, h, a, s,
+                  pdl);
 }
 
 }  // namespace engram
