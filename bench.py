@@ -226,6 +226,12 @@ def source_digest(names):
 
 DECODE_SOURCES = ("decode_fused.cu", "ptx.cuh", "internal.h")
 DECODE_PROFILE = os.path.join(ROOT, "profiles", "decode_fused_kernel_decode_T64.md")
+GEMM_SOURCES = ("wkv_gemm.cu", "ptx.cuh", "internal.h")
+GATE_SOURCES = ("gate.cu", "ptx.cuh", "internal.h")
+
+
+def profile_path(kernel, workload):
+    return os.path.join(ROOT, "profiles", f"{kernel}_{workload}.md")
 
 
 def stored_traffic(path, sources):
@@ -286,6 +292,19 @@ def algorithmic_bytes(wl):
         b += (wl.N // 32) * (wl.K // 32)
     if wl.table_location != "host":
         b += row_bytes(wl)
+    return b
+
+
+def gate_ring_bytes(wl, tile_cols):
+    """HBM bytes of the prefill gate kernel: hidden in, output out, the bf16
+    value, the GEMM's gate-partial records (16 bytes per token, copy and
+    record; MXFP8 writes two per tile), the fp32 gate it stores and the
+    token mask."""
+    records = (2 if wl.wkv_format == "mxfp8" else 1) * (wl.dim // tile_cols)
+    b = (2 * wl.T * wl.hc_mult * wl.dim * 2 + wl.T * wl.dim * 2
+         + wl.T * wl.hc_mult * records * 16 + wl.T * wl.hc_mult * 4)
+    if wl.mask_p is not None:
+        b += wl.T
     return b
 
 
@@ -597,7 +616,7 @@ def main():
     }
     launches = steps * len(samples)
 
-    def prefill_block(layer, pw, kernel_name, peak, peak_name):
+    def prefill_block(layer, pw, kernel_name, peak, peak_name, tile_cols):
         """Per-step time of a prefill forward and its kernels' event times."""
         pstep = W.make_step_inputs(pw, "cuda", step=rank)
         ph, pids, pmask = pstep["hidden"], pstep["hash_ids"], pstep["token_mask"]
@@ -625,6 +644,8 @@ def main():
         pw_ms = float(np.median(pprof[:, 1]))
         flops = 2.0 * pw.T * pw.N * pw.K
         tf = flops / (pw_ms * 1e-3) / 1e12
+        gate_ms = float(np.median(pprof[:, 2]))
+        gb = gate_ring_bytes(pw, tile_cols)
         return pk * 3 + 30, {
             "workload": pw.name, "T": pw.T, "tokens_per_s": world * pw.T / (p_ms * 1e-3),
             "ms_per_step": p_ms, "l2": "inputs larger than L2 (hidden "
@@ -633,12 +654,21 @@ def main():
                           "gate": float(np.median(pprof[:, 2]))},
             "roofline": {"bound": "tensor", "kernel": kernel_name, "achieved": tf,
                          "peak": peak, "unit": "TFLOP/s", "frac": tf / peak,
-                         "peak_kind": peak_name},
+                         "peak_kind": peak_name,
+                         "traffic": stored_traffic(profile_path("wkv_gemm_kernel", pw.name),
+                                                   GEMM_SOURCES)},
+            "gate_roofline": {"bound": "hbm", "kernel": "gate_ring_kernel",
+                              "achieved": gb / (gate_ms * 1e-3) / 1e9, "peak": hbm_peak,
+                              "unit": "GB/s", "frac": gb / (gate_ms * 1e-3) / 1e9 / hbm_peak,
+                              "algorithmic_bytes": gb, "peak_kind": peak_kind,
+                              "traffic": stored_traffic(profile_path("gate_ring_kernel", pw.name),
+                                                        GATE_SOURCES)},
         }
 
     if not args.no_prefill:
-        n, line["prefill"] = prefill_block(L0["layer"], W.PREFILL, "wkv_gemm_kernel<bf16>",
-                                           bf16_peak, peak_kind)
+        n, line["prefill"] = prefill_block(
+            L0["layer"], W.PREFILL, "wkv_gemm_kernel<bf16> (CTA pairs, cta_group::2)", bf16_peak,
+            peak_kind, 256)
         launches += n
 
     if rank == 0 and world == 1 and not args.no_cpu_baseline:
@@ -687,9 +717,10 @@ def main():
             else:
                 fp8_peak, fp8_kind = 2.0 * bf16_peak, f"{peak_kind} bf16 x 2 (nominal ratio)"
             line["fp8_peak_measured"] = fp8
+            mxp = W.MXFP8_PREFILL
             n, line["mxfp8_prefill"] = prefill_block(
-                mlayers[0]["layer"], W.MXFP8_PREFILL, "wkv_gemm_kernel<mxfp8>", fp8_peak,
-                fp8_kind)
+                mlayers[0]["layer"], mxp, "wkv_gemm_kernel<mxfp8> (CTA pairs, cta_group::2)",
+                fp8_peak, fp8_kind, 224 if mxp.dim % 224 == 0 else 128)
             launches += n
         for L in mlayers:
             L["layer"].close()
