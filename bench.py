@@ -230,8 +230,9 @@ GEMM_SOURCES = ("wkv_gemm.cu", "ptx.cuh", "internal.h")
 GATE_SOURCES = ("gate.cu", "ptx.cuh", "internal.h")
 
 
-def profile_path(kernel, workload):
-    return os.path.join(ROOT, "profiles", f"{kernel}_{workload}.md")
+def profile_path(kernel, wl):
+    """The committed ncu summary of a kernel on a workload."""
+    return os.path.join(ROOT, "profiles", f"{kernel}_{wl.name}_T{wl.T}.md")
 
 
 def stored_traffic(path, sources):
@@ -655,13 +656,13 @@ def main():
             "roofline": {"bound": "tensor", "kernel": kernel_name, "achieved": tf,
                          "peak": peak, "unit": "TFLOP/s", "frac": tf / peak,
                          "peak_kind": peak_name,
-                         "traffic": stored_traffic(profile_path("wkv_gemm_kernel", pw.name),
+                         "traffic": stored_traffic(profile_path("wkv_gemm_kernel", pw),
                                                    GEMM_SOURCES)},
             "gate_roofline": {"bound": "hbm", "kernel": "gate_ring_kernel",
                               "achieved": gb / (gate_ms * 1e-3) / 1e9, "peak": hbm_peak,
                               "unit": "GB/s", "frac": gb / (gate_ms * 1e-3) / 1e9 / hbm_peak,
                               "algorithmic_bytes": gb, "peak_kind": peak_kind,
-                              "traffic": stored_traffic(profile_path("gate_ring_kernel", pw.name),
+                              "traffic": stored_traffic(profile_path("gate_ring_kernel", pw),
                                                         GATE_SOURCES)},
         }
 
