@@ -82,6 +82,18 @@ def test_tiny_mxfp8_prefill_path(tiny_mx, T):
     _check_all(tiny_mx, inp, out, gate, value)
 
 
+@pytest.mark.parametrize("T", [300, 600])
+def test_tiny_mxfp8_max_tokens_with_odd_token_tiles(T):
+    """As the bf16 case: T = max_tokens with an odd number of 128-token
+    tiles, so the last CTA pair's second tile (codes and scale atoms) lies
+    in the staging buffers' padding."""
+    case = Case(W.TINY_MXFP8, max_tokens=T)
+    inp = case.step_inputs(T=T, step=T + 13)
+    out, gate, value = _run(case, inp)
+    _check_all(case, inp, out, gate, value)
+    case.layer.close()
+
+
 def test_tiny_mxfp8_lookup_then_forward(tiny_mx):
     inp = tiny_mx.step_inputs(T=48, step=5)
     out, _, _ = _run(tiny_mx, inp)

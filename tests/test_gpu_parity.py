@@ -2,9 +2,11 @@
 
 Element-by-element on sizes the oracle finishes in seconds (several tiles
 and ragged tails on both wkv schedules), whole-output at the decode
-config, sampled tokens at the prefill config, plus the edge cases: T = 0,
-maximum T, all-False masks, in-place and strided views, out-of-range ids,
-and run-to-run determinism."""
+config, every token of the prefill config (the oracle spread over the
+host's cores), plus the edge cases: T = 0, maximum T (also with an odd
+number of 128-token tiles, where the GEMM's last CTA pair reads padding),
+all-False masks, in-place and strided views, out-of-range ids, and
+run-to-run determinism."""
 
 import numpy as np
 import pytest
@@ -61,6 +63,19 @@ def test_tokens_as_m_path_ragged_T(tiny, T):
     inp = tiny.step_inputs(T=T, step=T)
     out, gate, value = _run(tiny, inp)
     compare(tiny, inp, out, tiny.oracle(inp), gate=gate, value=value)
+
+
+@pytest.mark.parametrize("T", [300, 600])
+def test_max_tokens_with_odd_token_tiles(T):
+    """T = max_tokens with 3 or 5 tiles of 128 tokens: the prefill GEMM's CTA
+    pairs take tiles 2i and 2i + 1, so the last pair's second tile lies past
+    T, in the staging buffer's padding (max_tokens rounded up to 256); its
+    rows must leave no trace in the output."""
+    case = Case(W.TINY, max_tokens=T)
+    inp = case.step_inputs(T=T, step=T + 11)
+    out, gate, value = _run(case, inp)
+    compare(case, inp, out, case.oracle(inp), gate=gate, value=value)
+    case.layer.close()
 
 
 def test_separate_lookup_then_forward(tiny):
