@@ -7,14 +7,17 @@
 // ("vllm.models.deepseek_v4_1.common.engram", Engram.__init__ and forward).
 //
 // This is the prefill schedule (T > 256; decode runs in decode_fused.cu):
-// 128 tokens x 256 kv columns per tile, persistent CTAs stride over tiles.
+// persistent clusters of two CTAs stride over units of 256 tokens x BN kv
+// columns (BN = 256 for bf16), the pair sharing each MMA (see kPair below);
+// where no pair cluster fits, single CTAs stride over 128-token tiles.
 // The epilogue never writes keys: for a key tile it reduces
 // (sum hidden^2, sum key^2, sum hidden*q*k*key) over the tile's dims -- the
 // split-dim gate partials of _engram_gate_partials_kernel
 // ("vllm.models.deepseek_v41.amd.engram"), here per N tile instead of per
 // TP rank -- and for a value tile it stores the value in bf16.
 //
-// Roles: warp 0 = TMA producer, warp 1 = TMEM owner and MMA issuer, then
+// Roles: warp 0 = TMA producer, warp 1 = TMEM owner and (in a pair, the
+// even CTA's only) MMA issuer, then
 // the epilogue warps (TMEM lane quarter = warp % 4): 4 for bf16 (192
 // threads); 8 for MXFP8 (320 threads, two per quarter taking half of the
 // tile's columns each), whose short fp8 MMAs otherwise wait for the
@@ -24,9 +27,9 @@
 // programmatic-launch wait, overlapping the gather kernel.
 //
 // MXFP8 wkv: e4m3 codes of the rows (quantised by the gather) times e4m3
-// weights, tcgen05 kind::mxf8f6f4 block_scale, 128 x 224 tiles when 224
-// divides dim (two accumulators of 224 columns and four 16-column scale
-// slots fill the 512 TMEM columns), else 128 x 128.  Each stage also brings
+// weights, tcgen05 kind::mxf8f6f4 block_scale, 224 kv columns per unit when
+// 224 divides dim (two accumulators of 224 columns and four 16-column scale
+// slots fill the 512 TMEM columns), else 128.  Each stage also brings
 // the 512-byte scale-factor atoms of its k-block (the tokens', and one per
 // 128 tile rows of the weights', packed per tile at create); the MMA
 // thread copies them into that stage's TMEM scale slot
