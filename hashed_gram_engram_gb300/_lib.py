@@ -43,7 +43,8 @@ ENGRAM_FUSED_PLAN_FIELDS = 16
 # Every symbol include/engram.h declares.
 EXPORTED = (
     "engram_create", "engram_destroy", "engram_lookup", "engram_forward",
-    "engram_forward_host", "engram_last_error", "engram_device_error", "engram_layout",
+    "engram_forward_host", "engram_forward_host_pipelined", "engram_last_error",
+    "engram_device_error", "engram_layout",
     "engram_debug_intermediates", "engram_debug_staged_rows", "engram_profile_enable",
     "engram_profile_read", "engram_gate_noalloc", "engram_debug_staged_mx",
     "engram_debug_fused_plan",
@@ -104,6 +105,7 @@ def load(path: str | None = None):
             "engram_lookup": [vp, vp, i64, i64, ctypes.c_int, vp],
             "engram_forward": [vp, vp, vp, vp, i64, vp, vp, vp, i64, vp],
             "engram_forward_host": [vp, vp, vp, vp, vp, i64, vp],
+            "engram_forward_host_pipelined": [vp, vp, vp, vp, vp, i64, vp],
             "engram_last_error": [vp, ctypes.c_int],
             "engram_device_error": [vp, vp, ctypes.c_int],
             "engram_layout": [i64, i32, i32, i32, vp, vp],
@@ -192,6 +194,13 @@ def engram_forward_host(h, hidden_host, hash_ids_host, token_mask_host, out_host
     return _check(load().engram_forward_host(
         h, _ptr(hidden_host), _ptr(hash_ids_host), _ptr(token_mask_host), _ptr(out_host),
         int(T), _stream(stream)), "engram_forward_host")
+
+
+def engram_forward_host_pipelined(h, hidden_host, hash_ids_host, token_mask_host, out_host, T,
+                                  stream=None):
+    return _check(load().engram_forward_host_pipelined(
+        h, _ptr(hidden_host), _ptr(hash_ids_host), _ptr(token_mask_host), _ptr(out_host),
+        int(T), _stream(stream)), "engram_forward_host_pipelined")
 
 
 def engram_last_error(h, sync=0) -> int:

@@ -105,9 +105,16 @@ void free_handle(engram_handle* h) {
                     h->ws.staged_s,  h->ws.partials, h->ws.value,
                     h->ws.gate,      h->ws.qk,       h->ws.wsf_atoms, h->ws.err,
                     h->ws.wpack,     h->ws.fpart,    h->ws.fvalue,   h->ws.grid_bar,
-                    h->ws.host_hidden, h->ws.host_ids, h->ws.host_mask};
+                    h->ws.host_hidden, h->ws.host_ids, h->ws.host_mask,
+                    h->ws.pipe_hidden[0], h->ws.pipe_hidden[1], h->ws.pipe_ids[0],
+                    h->ws.pipe_ids[1], h->ws.pipe_mask[0], h->ws.pipe_mask[1]};
     for (void* p : ptrs)
         if (p) cudaFree(p);
+    for (int b = 0; b < 2; ++b)
+        for (cudaEvent_t ev : {h->pipe_ev_in[b], h->pipe_ev_fwd[b], h->pipe_ev_out[b]})
+            if (ev) cudaEventDestroy(ev);
+    if (h->pipe_in) cudaStreamDestroy(h->pipe_in);
+    if (h->pipe_out) cudaStreamDestroy(h->pipe_out);
     for (cudaEvent_t ev : h->ev)
         if (ev) cudaEventDestroy(ev);
     delete h;
@@ -542,6 +549,71 @@ int engram_forward_host(engram_t* h, const void* hidden_host, const int32_t* has
                             T, stream);
     if (rc != ENGRAM_OK) return rc;
     e = cudaMemcpyAsync(out_host, ws.host_hidden, hb, cudaMemcpyDeviceToHost, stream);
+    return cuda_err(h, e);
+}
+
+int engram_forward_host_pipelined(engram_t* h, const void* hidden_host,
+                                  const int32_t* hash_ids_host, const uint8_t* token_mask_host,
+                                  void* out_host, int64_t T, cudaStream_t stream) {
+    if (h == nullptr) return ENGRAM_ERR_INVALID_ARG;
+    if (T < 0) return set_err(h, ENGRAM_ERR_INVALID_ARG);
+    if (T > h->cfg.max_tokens) return set_err(h, ENGRAM_ERR_T_EXCEEDS_MAX);
+    if (T == 0) return set_err(h, ENGRAM_OK);
+    if (hidden_host == nullptr || hash_ids_host == nullptr || out_host == nullptr)
+        return set_err(h, ENGRAM_ERR_INVALID_ARG);
+    DeviceGuard guard(h->cfg.device);
+    if (!guard.ok) return set_err(h, ENGRAM_ERR_CUDA);
+    cudaStreamCaptureStatus cap = cudaStreamCaptureStatusNone;
+    cudaError_t e = cudaStreamIsCapturing(stream, &cap);
+    if (e != cudaSuccess) return cuda_err(h, e);
+    if (cap != cudaStreamCaptureStatusNone)  // a graph holds one ordered sequence
+        return engram_forward_host(h, hidden_host, hash_ids_host, token_mask_host, out_host, T,
+                                   stream);
+    const int64_t H = h->cfg.hc_mult, D = h->cfg.dim, C = h->C;
+    Workspace& ws = h->ws;
+    if (h->pipe_in == nullptr) {
+        for (int b = 0; b < 2 && e == cudaSuccess; ++b) {
+            e = dalloc(reinterpret_cast<uint16_t**>(&ws.pipe_hidden[b]), ws.rows_alloc * H * D * 2,
+                       false);
+            if (e == cudaSuccess) e = dalloc(&ws.pipe_ids[b], ws.rows_alloc * C * sizeof(int32_t), false);
+            if (e == cudaSuccess) e = dalloc(&ws.pipe_mask[b], ws.rows_alloc, false);
+            for (cudaEvent_t* ev : {&h->pipe_ev_in[b], &h->pipe_ev_fwd[b], &h->pipe_ev_out[b]})
+                if (e == cudaSuccess) e = cudaEventCreateWithFlags(ev, cudaEventDisableTiming);
+        }
+        if (e == cudaSuccess) e = cudaStreamCreateWithFlags(&h->pipe_out, cudaStreamNonBlocking);
+        if (e == cudaSuccess) e = cudaStreamCreateWithFlags(&h->pipe_in, cudaStreamNonBlocking);
+        if (e != cudaSuccess) return cuda_err(h, e);  // (freed with the handle)
+    }
+    const int b = static_cast<int>(h->pipe_calls & 1u);
+    const size_t hb = static_cast<size_t>(T * H * D * 2);
+    // inputs into slot b once the call two back has copied its output out of
+    // it (that copy followed its forward, the slot's last reader)
+    if (h->pipe_calls >= 2) e = cudaStreamWaitEvent(h->pipe_in, h->pipe_ev_out[b], 0);
+    if (e == cudaSuccess)
+        e = cudaMemcpyAsync(ws.pipe_hidden[b], hidden_host, hb, cudaMemcpyHostToDevice, h->pipe_in);
+    if (e == cudaSuccess)
+        e = cudaMemcpyAsync(ws.pipe_ids[b], hash_ids_host, static_cast<size_t>(T * C * 4),
+                            cudaMemcpyHostToDevice, h->pipe_in);
+    if (e == cudaSuccess && token_mask_host != nullptr)
+        e = cudaMemcpyAsync(ws.pipe_mask[b], token_mask_host, static_cast<size_t>(T),
+                            cudaMemcpyHostToDevice, h->pipe_in);
+    if (e == cudaSuccess) e = cudaEventRecord(h->pipe_ev_in[b], h->pipe_in);
+    // the forward on the caller's stream, in place in slot b
+    if (e == cudaSuccess) e = cudaStreamWaitEvent(stream, h->pipe_ev_in[b], 0);
+    if (e != cudaSuccess) return cuda_err(h, e);
+    const int64_t st[3] = {H * D, D, 1};
+    const int rc = engram_forward(h, ws.pipe_hidden[b], st, ws.pipe_ids[b], C,
+                                  token_mask_host != nullptr ? ws.pipe_mask[b] : nullptr,
+                                  ws.pipe_hidden[b], st, T, stream);
+    if (rc != ENGRAM_OK) return rc;
+    // the output copy on the output stream; the caller's stream waits for it
+    e = cudaEventRecord(h->pipe_ev_fwd[b], stream);
+    if (e == cudaSuccess) e = cudaStreamWaitEvent(h->pipe_out, h->pipe_ev_fwd[b], 0);
+    if (e == cudaSuccess)
+        e = cudaMemcpyAsync(out_host, ws.pipe_hidden[b], hb, cudaMemcpyDeviceToHost, h->pipe_out);
+    if (e == cudaSuccess) e = cudaEventRecord(h->pipe_ev_out[b], h->pipe_out);
+    if (e == cudaSuccess) e = cudaStreamWaitEvent(stream, h->pipe_ev_out[b], 0);
+    if (e == cudaSuccess) ++h->pipe_calls;
     return cuda_err(h, e);
 }
 

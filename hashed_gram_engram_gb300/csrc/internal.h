@@ -68,6 +68,10 @@ struct Workspace {
     void* host_hidden = nullptr;
     int32_t* host_ids = nullptr;
     uint8_t* host_mask = nullptr;
+    // engram_forward_host_pipelined: two slots used in turn
+    void* pipe_hidden[2] = {nullptr, nullptr};
+    int32_t* pipe_ids[2] = {nullptr, nullptr};
+    uint8_t* pipe_mask[2] = {nullptr, nullptr};
 };
 
 // Column ownership of the fused decode kernel: N = D*(H+1) columns in
@@ -126,6 +130,11 @@ struct engram_handle {
     int profiling;
     cudaEvent_t ev[4];
     bool ev_ran[3];
+    // engram_forward_host_pipelined: input and output copy streams, and per
+    // slot the events "inputs copied", "forward done", "output copied"
+    cudaStream_t pipe_in, pipe_out;
+    cudaEvent_t pipe_ev_in[2], pipe_ev_fwd[2], pipe_ev_out[2];
+    uint64_t pipe_calls;
 };
 
 namespace engram {

@@ -174,6 +174,26 @@ int engram_forward_host(engram_t* h, const void* hidden_host, const int32_t* has
                         const uint8_t* token_mask_host, void* out_host, int64_t T,
                         cudaStream_t stream);
 
+/* engram_forward_host for back-to-back calls (a serving loop): the input
+ * copies of a call are NOT ordered after earlier work on `stream`; they
+ * start on a handle-owned copy stream as soon as the call is made, so they
+ * run during the previous call's forward and output copy.  The host buffers
+ * must therefore already hold the inputs when the call is made (written by
+ * the CPU, not by work still pending on a stream).  The forward runs on
+ * `stream` after both its inputs and earlier work on `stream`; the output
+ * copy runs on a second handle-owned stream, and `stream` waits for it, so
+ * later work on `stream` (and a synchronisation of it) sees out_host
+ * written.  Calls alternate between two handle-owned device slots, so a
+ * call's input copy never overwrites what the previous call is still
+ * reading or copying out.  The handle's copy streams are shared by every
+ * caller stream: calls on one handle from several streams are serialised
+ * on them.  While `stream` is being captured into a CUDA graph the call
+ * behaves as engram_forward_host (all on `stream`).  The first call
+ * allocates the slots and creates the streams. */
+int engram_forward_host_pipelined(engram_t* h, const void* hidden_host,
+                                  const int32_t* hash_ids_host, const uint8_t* token_mask_host,
+                                  void* out_host, int64_t T, cudaStream_t stream);
+
 /* Host-side error of the last call on this handle.  With sync != 0 the
  * device is synchronised and the sticky device error word is read and
  * cleared: a non-zero word returns ENGRAM_ERR_DEVICE. */
