@@ -33,6 +33,25 @@ def test_algorithmic_bytes_per_workload():
     assert bench.row_bytes(W.DECODE_E4M3) == 64 * 1024 + 64 * 1024 // 32
 
 
+def test_gate_kernel_bytes_per_workload():
+    # hidden read and output written (bf16), the bf16 value row, one 16-byte
+    # partial record per token, copy and 256-column tile (MXFP8: two per
+    # 224-column tile), the fp32 gate, and the mask byte
+    T, H, D = 8192, 4, 4096
+    assert bench.gate_ring_bytes(W.PREFILL, 256) == \
+        2 * T * H * D * 2 + T * D * 2 + T * H * (D // 256) * 16 + T * H * 4 + T == 612_507_648
+    T, D = 4096, 7168
+    assert bench.gate_ring_bytes(W.MXFP8_PREFILL, 224) == \
+        2 * T * H * D * 2 + T * D * 2 + T * H * 2 * (D // 224) * 16 + T * H * 4 == 545_325_056
+
+
+def test_profile_names_follow_kernel_and_workload():
+    assert bench.profile_path("wkv_gemm_kernel", W.PREFILL).endswith(
+        "profiles/wkv_gemm_kernel_prefill_T8192.md")
+    assert bench.profile_path("gate_ring_kernel", W.MXFP8_PREFILL).endswith(
+        "profiles/gate_ring_kernel_mxfp8_prefill_T4096.md")
+
+
 def test_source_digest_ignores_comments_only():
     d = bench.source_digest(bench.DECODE_SOURCES)
     assert len(d) == 12 and d == bench.source_digest(bench.DECODE_SOURCES)
