@@ -577,26 +577,37 @@ def main():
     out_h = torch.empty_like(hid_h).pin_memory()
     ne = min(args.steps, 500)
 
-    def e2e_ms_per_step(pipelined):
+    def e2e_ms_per_step(mode):
         def fwd(i):
-            L = layers[i % NL]
+            L = layers[i % NL]["layer"]
             hid, ids = host_in[i % NL]
-            call = L["layer"].forward_host_pipelined if pipelined else L["layer"].forward_host
-            call(hid, ids, None, out_h, stream=stream)
+            if mode == "serial":
+                L.forward_host(hid, ids, None, out_h, stream=stream)
+            else:
+                L.forward_host_pipelined(hid, ids, None, out_h, stream=stream,
+                                         defer_output=mode == "deferred")
+
+        def flush():
+            if mode == "deferred":
+                for L in layers:
+                    L["layer"].flush_host(stream)
         for i in range(3 * NL):
             fwd(i)
+        flush()
         torch.cuda.synchronize()
         b0 = torch.cuda.Event(enable_timing=True)
         b1 = torch.cuda.Event(enable_timing=True)
         b0.record(stream)
         for i in range(ne):
             fwd(i)
+        flush()  # every step's output copy inside the timed region
         b1.record(stream)
         torch.cuda.synchronize()
         return max_over_ranks(b0.elapsed_time(b1) / ne)
 
-    e2e_ms = e2e_ms_per_step(True)
-    e2e_serial_ms = e2e_ms_per_step(False)
+    e2e_ms = e2e_ms_per_step("deferred")
+    e2e_ordered_ms = e2e_ms_per_step("pipelined")
+    e2e_serial_ms = e2e_ms_per_step("serial")
 
     line = {
         "metric": METRIC, "value": value, "unit": "tokens/s", "n_gpus": world,
@@ -626,9 +637,13 @@ def main():
                 "h2d_bytes_per_step": int(hid_h.numel() * 2 + ids_h.numel() * 4),
                 "d2h_bytes_per_step": int(out_h.numel() * 2),
                 "ms_per_step": e2e_ms, "steps": ne,
-                "how": f"engram_forward_host_pipelined, {ne} back-to-back steps rotating over "
-                       f"{NL} layers (a step's input copy overlaps the previous step's forward "
-                       f"and output copy), CUDA events around all of them",
+                "how": f"engram_forward_host_pipelined with ENGRAM_HOST_DEFER_OUTPUT, {ne} "
+                       f"back-to-back steps rotating over {NL} layers (a step's input copy "
+                       f"overlaps the previous step, its output copy the next one), then "
+                       f"engram_forward_host_flush; CUDA events around all of it",
+                "ordered_value": world * wl.T / (e2e_ordered_ms * 1e-3),
+                "ordered_how": "engram_forward_host_pipelined: the stream waits for each "
+                               "step's output copy before the next step",
                 "serial_value": world * wl.T / (e2e_serial_ms * 1e-3),
                 "serial_how": "engram_forward_host: each step's copies and forward in order"},
         "gpu_launches": steps * len(samples),

@@ -18,7 +18,8 @@ from . import _lib
 from ._lib import (EngramError, engram_config, engram_create, engram_debug_intermediates,
                    engram_debug_keep_value, engram_debug_staged_mx, engram_debug_staged_rows,
                    engram_destroy, engram_device_error,
-                   engram_forward, engram_forward_host, engram_forward_host_pipelined,
+                   engram_forward, engram_forward_host, engram_forward_host_flush,
+                   engram_forward_host_pipelined, ENGRAM_HOST_DEFER_OUTPUT,
                    engram_gate_noalloc,
                    engram_last_error, engram_layout,
                    engram_lookup, engram_profile_enable, engram_profile_read,
@@ -31,7 +32,7 @@ from ._lib import (EngramError, engram_config, engram_create, engram_debug_inter
 __all__ = [
     "Engram", "EngramPrefetch", "EngramError", "engram_config", "engram_weights", "engram_create",
     "engram_destroy", "engram_lookup", "engram_forward", "engram_forward_host",
-    "engram_forward_host_pipelined",
+    "engram_forward_host_pipelined", "engram_forward_host_flush", "ENGRAM_HOST_DEFER_OUTPUT",
     "engram_gate_noalloc", "engram_debug_staged_mx", "engram_debug_keep_value",
     "engram_last_error", "engram_device_error", "engram_layout", "engram_debug_intermediates",
     "engram_debug_staged_rows", "engram_profile_enable", "engram_profile_read",
@@ -153,13 +154,20 @@ class Engram:
                             T, stream)
 
     def forward_host_pipelined(self, hidden_host, hash_ids_host, token_mask_host, out_host,
-                               stream=None):
+                               stream=None, defer_output=False):
         """forward_host whose input copies overlap the previous call (the host
-        inputs must be ready when the call is made); see
+        inputs must be ready when the call is made); with defer_output the
+        output copy also overlaps the next call, and out_host is complete
+        after the next call (or flush_host()) on the stream; see
         engram_forward_host_pipelined in include/engram.h."""
         T = hidden_host.shape[0]
         engram_forward_host_pipelined(self.handle, hidden_host, hash_ids_host, token_mask_host,
-                                      out_host, T, stream)
+                                      out_host, T,
+                                      ENGRAM_HOST_DEFER_OUTPUT if defer_output else 0, stream)
+
+    def flush_host(self, stream=None):
+        """The stream waits for the last pipelined call's output copy."""
+        engram_forward_host_flush(self.handle, stream)
 
     def device_error(self, clear=True) -> int:
         return engram_device_error(self.handle, int(clear))

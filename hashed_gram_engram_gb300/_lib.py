@@ -39,11 +39,13 @@ ENGRAM_TABLE_HOST_PINNED = 1
 ENGRAM_TABLE_FORMAT_BF16 = 0
 ENGRAM_TABLE_FORMAT_E4M3 = 1
 ENGRAM_FUSED_PLAN_FIELDS = 16
+ENGRAM_HOST_DEFER_OUTPUT = 1
 
 # Every symbol include/engram.h declares.
 EXPORTED = (
     "engram_create", "engram_destroy", "engram_lookup", "engram_forward",
-    "engram_forward_host", "engram_forward_host_pipelined", "engram_last_error",
+    "engram_forward_host", "engram_forward_host_pipelined", "engram_forward_host_flush",
+    "engram_last_error",
     "engram_device_error", "engram_layout",
     "engram_debug_intermediates", "engram_debug_staged_rows", "engram_profile_enable",
     "engram_profile_read", "engram_gate_noalloc", "engram_debug_staged_mx",
@@ -105,7 +107,8 @@ def load(path: str | None = None):
             "engram_lookup": [vp, vp, i64, i64, ctypes.c_int, vp],
             "engram_forward": [vp, vp, vp, vp, i64, vp, vp, vp, i64, vp],
             "engram_forward_host": [vp, vp, vp, vp, vp, i64, vp],
-            "engram_forward_host_pipelined": [vp, vp, vp, vp, vp, i64, vp],
+            "engram_forward_host_pipelined": [vp, vp, vp, vp, vp, i64, ctypes.c_uint32, vp],
+            "engram_forward_host_flush": [vp, vp],
             "engram_last_error": [vp, ctypes.c_int],
             "engram_device_error": [vp, vp, ctypes.c_int],
             "engram_layout": [i64, i32, i32, i32, vp, vp],
@@ -197,10 +200,15 @@ def engram_forward_host(h, hidden_host, hash_ids_host, token_mask_host, out_host
 
 
 def engram_forward_host_pipelined(h, hidden_host, hash_ids_host, token_mask_host, out_host, T,
-                                  stream=None):
+                                  flags=0, stream=None):
     return _check(load().engram_forward_host_pipelined(
         h, _ptr(hidden_host), _ptr(hash_ids_host), _ptr(token_mask_host), _ptr(out_host),
-        int(T), _stream(stream)), "engram_forward_host_pipelined")
+        int(T), int(flags), _stream(stream)), "engram_forward_host_pipelined")
+
+
+def engram_forward_host_flush(h, stream=None):
+    return _check(load().engram_forward_host_flush(h, _stream(stream)),
+                  "engram_forward_host_flush")
 
 
 def engram_last_error(h, sync=0) -> int:

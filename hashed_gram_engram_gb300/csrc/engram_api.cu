@@ -554,9 +554,9 @@ int engram_forward_host(engram_t* h, const void* hidden_host, const int32_t* has
 
 int engram_forward_host_pipelined(engram_t* h, const void* hidden_host,
                                   const int32_t* hash_ids_host, const uint8_t* token_mask_host,
-                                  void* out_host, int64_t T, cudaStream_t stream) {
+                                  void* out_host, int64_t T, uint32_t flags, cudaStream_t stream) {
     if (h == nullptr) return ENGRAM_ERR_INVALID_ARG;
-    if (T < 0) return set_err(h, ENGRAM_ERR_INVALID_ARG);
+    if (T < 0 || (flags & ~ENGRAM_HOST_DEFER_OUTPUT) != 0u) return set_err(h, ENGRAM_ERR_INVALID_ARG);
     if (T > h->cfg.max_tokens) return set_err(h, ENGRAM_ERR_T_EXCEEDS_MAX);
     if (T == 0) return set_err(h, ENGRAM_OK);
     if (hidden_host == nullptr || hash_ids_host == nullptr || out_host == nullptr)
@@ -612,8 +612,27 @@ int engram_forward_host_pipelined(engram_t* h, const void* hidden_host,
     if (e == cudaSuccess)
         e = cudaMemcpyAsync(out_host, ws.pipe_hidden[b], hb, cudaMemcpyDeviceToHost, h->pipe_out);
     if (e == cudaSuccess) e = cudaEventRecord(h->pipe_ev_out[b], h->pipe_out);
-    if (e == cudaSuccess) e = cudaStreamWaitEvent(stream, h->pipe_ev_out[b], 0);
+    // the caller's stream waits for this output copy, or (deferred) for the
+    // previous call's, which the forward just run has long overtaken
+    if (e == cudaSuccess) {
+        if (!(flags & ENGRAM_HOST_DEFER_OUTPUT))
+            e = cudaStreamWaitEvent(stream, h->pipe_ev_out[b], 0);
+        else if (h->pipe_calls >= 1)
+            e = cudaStreamWaitEvent(stream, h->pipe_ev_out[b ^ 1], 0);
+    }
     if (e == cudaSuccess) ++h->pipe_calls;
+    return cuda_err(h, e);
+}
+
+int engram_forward_host_flush(engram_t* h, cudaStream_t stream) {
+    if (h == nullptr) return ENGRAM_ERR_INVALID_ARG;
+    if (h->pipe_calls == 0) return set_err(h, ENGRAM_OK);
+    DeviceGuard guard(h->cfg.device);
+    if (!guard.ok) return set_err(h, ENGRAM_ERR_CUDA);
+    cudaStreamCaptureStatus cap = cudaStreamCaptureStatusNone;
+    cudaError_t e = cudaStreamIsCapturing(stream, &cap);
+    if (e == cudaSuccess && cap == cudaStreamCaptureStatusNone)
+        e = cudaStreamWaitEvent(stream, h->pipe_ev_out[(h->pipe_calls - 1) & 1u], 0);
     return cuda_err(h, e);
 }
 

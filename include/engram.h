@@ -188,11 +188,26 @@ int engram_forward_host(engram_t* h, const void* hidden_host, const int32_t* has
  * reading or copying out.  The handle's copy streams are shared by every
  * caller stream: calls on one handle from several streams are serialised
  * on them.  While `stream` is being captured into a CUDA graph the call
- * behaves as engram_forward_host (all on `stream`).  The first call
- * allocates the slots and creates the streams. */
+ * behaves as engram_forward_host (all on `stream`) and flags are ignored.
+ * The first call allocates the slots and creates the streams.
+ *
+ * flags = ENGRAM_HOST_DEFER_OUTPUT: `stream` waits for the PREVIOUS
+ * pipelined call's output copy instead of this one's, so this call's output
+ * copy overlaps the next call's forward.  After the call returns, later
+ * work on `stream` sees the previous call's out_host written; this call's
+ * out_host is written once engram_forward_host_flush has been called on
+ * the handle and `stream` has reached that point.  Invalid flags:
+ * ENGRAM_ERR_INVALID_ARG. */
+#define ENGRAM_HOST_DEFER_OUTPUT 1u
 int engram_forward_host_pipelined(engram_t* h, const void* hidden_host,
                                   const int32_t* hash_ids_host, const uint8_t* token_mask_host,
-                                  void* out_host, int64_t T, cudaStream_t stream);
+                                  void* out_host, int64_t T, uint32_t flags, cudaStream_t stream);
+
+/* Make `stream` wait for the output copy of the handle's last
+ * engram_forward_host_pipelined call (nothing to wait for: no-op; also a
+ * no-op while `stream` is being captured, where the calls are ordered on
+ * the stream anyway). */
+int engram_forward_host_flush(engram_t* h, cudaStream_t stream);
 
 /* Host-side error of the last call on this handle.  With sync != 0 the
  * device is synchronised and the sticky device error word is read and

@@ -1,5 +1,6 @@
 """engram_forward_host_pipelined: host-buffer forwards whose input copies
-overlap the previous call.  Several calls in a row with different inputs
+overlap the previous call (and, with ENGRAM_HOST_DEFER_OUTPUT, whose output
+copies overlap the next one).  Several calls in a row with different inputs
 (the two device slots alternate) must give, bit for bit, what
 engram_forward_host gives for the same inputs; so must calls captured into
 a CUDA graph, where the entry point keeps every step on the caller's
@@ -9,6 +10,7 @@ import torch
 
 import workloads as W
 from engram_case import Case
+from hashed_gram_engram_gb300 import EngramError, _lib
 
 pytestmark = pytest.mark.gpu
 
@@ -81,4 +83,32 @@ def test_graph_capture_keeps_the_calls_on_the_stream():
     torch.cuda.synchronize()
     for o, r in zip(outs, ref):
         assert torch.equal(o, r)
+    case.layer.close()
+
+
+@pytest.mark.parametrize("name, T", [("decode", 64), ("tiny", 300)])
+def test_deferred_output_lags_one_call_then_flushes(name, T):
+    wl = W.DECODE if name == "decode" else W.TINY
+    case = Case(wl, max_tokens=T)
+    inputs = _host_inputs(case, 5, T)
+    ref = _serial(case, inputs)
+    stream = torch.cuda.Stream()
+    outs = [torch.zeros_like(h).pin_memory() for h, _, _ in inputs]
+    for i, ((hid, ids, mask), o) in enumerate(zip(inputs, outs)):
+        case.layer.forward_host_pipelined(hid, ids, mask, o, stream=stream, defer_output=True)
+        if i >= 1:  # the previous call's output is written once the stream gets here
+            stream.synchronize()
+            assert torch.equal(outs[i - 1], ref[i - 1]), f"call {i - 1}"
+    case.layer.flush_host(stream)
+    stream.synchronize()
+    assert torch.equal(outs[-1], ref[-1])
+    # back to ordered calls on the same slots
+    last = torch.empty_like(outs[0]).pin_memory()
+    hid, ids, mask = inputs[2]
+    case.layer.forward_host_pipelined(hid, ids, mask, last, stream=stream)
+    stream.synchronize()
+    assert torch.equal(last, ref[2])
+    with pytest.raises(EngramError) as e:
+        _lib.engram_forward_host_pipelined(case.layer.handle, hid, ids, mask, last, T, 2, stream)
+    assert e.value.code == _lib.ENGRAM_ERR_INVALID_ARG
     case.layer.close()
