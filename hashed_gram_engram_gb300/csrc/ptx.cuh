@@ -51,13 +51,6 @@ __device__ __forceinline__ void mbar_arrive_expect_tx(uint64_t* bar, uint32_t by
 }
 
 // ---------------------------------------------------------------- cluster
-// This CTA's rank in its cluster.
-__device__ __forceinline__ uint32_t cluster_ctarank() {
-    uint32_t r;
-    asm volatile("mov.u32 %0, %%cluster_ctarank;" : "=r"(r));
-    return r;
-}
-
 // A barrier over every thread of the cluster: shared-memory writes and
 // barrier initialisations before it are visible to the other CTAs after it.
 __device__ __forceinline__ void cluster_sync() {
@@ -114,7 +107,9 @@ __device__ __forceinline__ uint32_t mbar_try_wait_cluster(uint64_t* bar, uint32_
 // cluster scope (arrivals from another CTA).
 __device__ __forceinline__ bool mbar_wait(uint64_t* bar, uint32_t parity,
                                           const volatile int* abort, bool cluster = false) {
-    auto test = [&]() { return cluster ? mbar_try_wait_cluster(bar, parity) : mbar_try_wait(bar, parity); };
+    auto test = [&]() {
+        return cluster ? mbar_try_wait_cluster(bar, parity) : mbar_try_wait(bar, parity);
+    };
     if (test()) return true;
     const uint64_t t0 = globaltimer_ns();
     for (uint32_t i = 1; i < kWaitLimitIters; ++i) {

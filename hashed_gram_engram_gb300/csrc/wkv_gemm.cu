@@ -140,7 +140,7 @@ __global__ void __launch_bounds__(threads_for(kMx), 1)
 
     const int warp = threadIdx.x >> 5;
     const int lane = threadIdx.x & 31;
-    const uint32_t rank = kPair ? (blockIdx.x & 1u) : 0u;  // == %cluster_ctarank
+    const uint32_t rank = kPair ? (blockIdx.x & 1u) : 0u;  // rank in the 2-CTA cluster
     // an epilogue warp is done with an accumulator (pair: the even CTA's
     // barrier, which counts both CTAs' warps)
     auto release_acc = [](uint64_t* bar) {
