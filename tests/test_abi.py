@@ -73,6 +73,9 @@ def test_null_handle_arguments_are_rejected_without_a_gpu(lib):
     out = ctypes.c_void_p()
     assert lib.engram_create(None, None, ctypes.byref(out)) == -1
     assert out.value is None
+    assert lib.engram_forward_host(None, None, None, None, None, 1, None) == -1
+    assert lib.engram_forward_host_pipelined(None, None, None, None, None, 1, 0, None) == -1
+    assert lib.engram_forward_host_flush(None, None) == -1
 
 
 def test_prefetch_arguments_are_rejected_without_a_gpu(lib):
